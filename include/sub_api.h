@@ -1,0 +1,256 @@
+/*
+ * sub_api.h -- C ABI of the SubSpec draft-and-verify decode library (sm_103a).
+ *
+ * SubSpec (substitute speculative decoding) accelerates a dense decoder that
+ * does not fit in GPU memory: the offloaded target layers get 4-bit
+ * substitutes kept on the GPU; the draft = the target's own resident layers +
+ * the substitutes, sharing the target's KV cache, and it drafts a deep static
+ * token tree from temperature-sharpened probabilities; the target verifies the
+ * whole tree in one pass and the longest matching path is accepted, so the
+ * output equals plain target decoding token for token.
+ *   "Speculate Deep and Accurate: Lossless and Training-Free Acceleration for
+ *    Offloaded LLMs via Substitute Speculative Decoding" -- abstract and the
+ *    summary card (Problem, Approach);
+ *   "SubSpec: Using the Target Model's Own Low-Bit Shadow as Its Draft Model"
+ *    -- reading report, 2.2 Step 4, 4.1, 6.2 (Leviathan et al.), 6.3 (SpecInfer).
+ *
+ * Conventions (every entry point):
+ *   - returns int32_t status: SUB_OK or a SUB_E* code; nothing aborts or
+ *     throws across the ABI; sub_last_error() gives a message for the calling
+ *     thread's last failure.
+ *   - pointers are DEVICE pointers unless the name ends in _host.  The caller
+ *     owns every buffer it passes; the library keeps no caller pointer past the
+ *     call except those stored in a sub_model (weights, see sub_model_desc).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default).
+ *     Kernel entry points only enqueue work; sub_generate synchronises.
+ *   - bf16 tensors are raw uint16 bit patterns (sub_bf16), row-major.
+ *   - group must be 64 (SUB_EUNSUPPORTED otherwise).
+ */
+#ifndef SUB_API_H
+#define SUB_API_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t sub_bf16;
+
+enum {
+  SUB_OK = 0,
+  SUB_EINVAL = 1,        /* bad argument: size, null pointer, alignment */
+  SUB_ENOMEM = 2,        /* device or pinned allocation failed */
+  SUB_ECUDA = 3,         /* a CUDA runtime call or kernel launch failed */
+  SUB_EUNSUPPORTED = 4,  /* valid but not implemented (e.g. group != 64) */
+  SUB_ETIMEOUT = 5       /* a bounded device wait gave up */
+};
+
+/* Message of the calling thread's last failed call ("" if none). */
+const char* sub_last_error(void);
+
+/* Library version string and the compile target, e.g. "0.1 sm_103a". */
+const char* sub_version(void);
+
+/* ------------------------------------------------------------------------ */
+/* Int4 substitutes.  The draft replaces each offloaded target layer by a
+ * data-free 4-bit copy ("Low-Bit Shadow" report 2.2 Step 4; card, Approach).
+ * This library's quantiser: per row n and group g of 64 consecutive inputs
+ * along K,  s = bf16(fp32(hi-lo)/15) (s = 1 if that is 0),
+ * z = bf16(fp32(-lo)/s),  q = clamp(rint_even(fp32(w/s) + z), 0, 15),
+ * dequantised value bf16((q - z) * s).  Layout: q is uint8 [N, ceil(K/64)*32]
+ * (byte j of a group: element 2j in the low nibble, 2j+1 in the high nibble;
+ * nibbles past K are 0); scale and zero are bf16 [N, ceil(K/64)].          */
+
+/* Quantise W (bf16 [N, K]) into q, scale, zero.  Bit-exact with the rule
+ * above.  K >= 1, N >= 1; W rows must be 16-byte aligned (K % 8 == 0). */
+int32_t sub_w4_pack(const sub_bf16* W, int64_t N, int64_t K, int32_t group,
+                    uint8_t* q, sub_bf16* scale, sub_bf16* zero, void* stream);
+
+/* Dequantise to bf16 W_out [N, K] (a test and debugging aid). */
+int32_t sub_w4_dequant(const uint8_t* q, const sub_bf16* scale, const sub_bf16* zero,
+                       int64_t N, int64_t K, int32_t group, sub_bf16* W_out, void* stream);
+
+/* Y[M, N] (bf16) = X[M, K] (bf16) . deq(W)^T, fp32 accumulation.
+ * M <= 16 runs the warp-level GEMV (one pass over the packed weights);
+ * larger M runs the tiled tensor-core kernel.  K % 8 == 0. */
+int32_t sub_w4_gemm(const sub_bf16* X, int64_t M, const uint8_t* q, const sub_bf16* scale,
+                    const sub_bf16* zero, int64_t N, int64_t K, int32_t group,
+                    sub_bf16* Y, void* stream);
+
+/* Y[M, N] (bf16) = X[M, K] . W[N, K]^T for bf16 weights (resident layers and
+ * streamed originals).  Same kernel family the decode path uses. K % 8 == 0. */
+int32_t sub_bf16_gemm(const sub_bf16* X, int64_t M, const sub_bf16* W, int64_t N, int64_t K,
+                      sub_bf16* Y, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Shared paged KV cache.  The draft attends over the target's committed KV
+ * ("Low-Bit Shadow" report 4.1 point 2: draft and target see the same
+ * attention context; card, measured effects: shared KV-cache).
+ * Pools k and v hold, for each layer l and physical page p,
+ * [n_heads_kv][page_size][head_dim] bf16 at element offset
+ * (l * n_pages + p) * n_heads_kv * page_size * head_dim.
+ * Logical cache position t lives in page page_table[t / page_size] at row
+ * t % page_size.  page_table has ceil(capacity / page_size) entries.      */
+typedef struct {
+  sub_bf16* k;
+  sub_bf16* v;
+  const int32_t* page_table;   /* device */
+  int32_t n_layers;
+  int32_t n_heads_kv;
+  int32_t head_dim;            /* 64 or 128 */
+  int32_t page_size;           /* multiple of 16 */
+  int32_t n_pages;
+  int64_t capacity;            /* logical positions covered by page_table */
+} sub_kv_cache;
+
+/* Tree-masked GQA attention ("Low-Bit Shadow" report 6.3, SpecInfer: one
+ * target pass verifies every tree node).  Query i (Q [n_q, Hq, d] bf16) reads
+ *   - the committed keys at positions [0, n_prefix), and
+ *   - the tree keys of its root path: for j in 0..depth[i], slot anc[i*anc_stride + j]
+ *     stored at cache position tree_base + slot (anc lists root .. self).
+ * anc == NULL means a chain: query i is slot i with path 0..i (a causal block,
+ * as in prefill).  n_slots bounds the slot indices (max slot + 1, <= 16384).
+ * O [n_q, Hq, d] bf16 = softmax(q K^T * softmax_scale) V, softmax in fp32.
+ * Hq % Hkv == 0; head_dim 64 or 128.  Splits over the keys use temporary
+ * device memory taken with cudaMallocAsync on `stream`. */
+int32_t sub_tree_attn(const sub_bf16* Q, int32_t n_q, int32_t n_heads_q,
+                      const sub_kv_cache* kv, int32_t layer, int64_t n_prefix, int64_t tree_base,
+                      int32_t n_slots, const int32_t* anc, int32_t anc_stride,
+                      const int32_t* depth, float softmax_scale, sub_bf16* O, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Static token tree ("Low-Bit Shadow" report 6.3/6.4: deep, narrow, static,
+ * k nodes per level, depth D).  Slot 0 is the root; level l in 1..D holds
+ * slots 1+(l-1)k .. lk.  Device arrays sized for 1 + D*k slots;
+ * anc is [1 + D*k][D + 1] (root .. self, -1 padded). */
+typedef struct {
+  int32_t* token;
+  int32_t* parent;
+  int32_t* depth;
+  float* score;       /* cumulative sharpened log-probability */
+  int32_t* anc;
+  int32_t width;      /* k */
+  int32_t max_depth;  /* D; anc row stride is D + 1 */
+} sub_tree;
+
+/* Expand level `level` (0 = root alone; else its k slots) into level+1.
+ * logits: fp32 [k_prev, V] draft logits of the level's slots in slot order.
+ * For each frontier node j: lp = z/T - logsumexp(z/T) (T = temperature,
+ * "sharpened" draft probabilities: card, Approach; report 3.4), candidates =
+ * its own top-k tokens (ties -> smaller id), score = S_j + lp; level+1 keeps
+ * the global top-k (ties -> smaller parent slot, then smaller id) in
+ * descending score order, writing token/parent/depth/score/anc.
+ * 1 <= k <= 16, level < max_depth. */
+int32_t sub_draft_expand(const float* logits, int64_t V, float temperature,
+                         const sub_tree* tree, int32_t level, void* stream);
+
+/* Verify + accept.  choice(u) = argmax_v logits[u, v] (mode 0, greedy) or
+ * argmax_v logits[u, v]/T + g(seed, root_pos + depth(u) + 1, v) (mode 1,
+ * Gumbel-max with Philox4x32-10 noise, Salmon et al. SC'11; counter
+ * (v/4, position, 0, 0), key (seed lo, seed hi), word v%4, x = ((r>>9)+0.5)*2^-23,
+ * g = -log(-log x)); ties -> smaller id.  Walk from the root to the child
+ * whose token equals choice(current) while one exists ("Low-Bit Shadow"
+ * report 6.2/6.3).  Writes accepted_slots[0..a), *n_accepted = a, *bonus_token
+ * = choice(last), and choice[n_nodes] if choice != NULL. */
+int32_t sub_verify_accept(const float* logits, const sub_tree* tree, int32_t n_nodes, int64_t V,
+                          int32_t mode, float temperature, uint64_t seed, int64_t root_pos,
+                          int32_t* accepted_slots, int32_t* n_accepted, int32_t* bonus_token,
+                          int32_t* choice, void* stream);
+
+/* Commit the accepted path: for every layer and KV head, copy K,V of tree
+ * slot accepted_slots[j-1] (at position root_pos + slot) to position
+ * root_pos + j, j = 1..*n_accepted (read on the device).  The root stays at
+ * root_pos.  Safe in place: all rows of a (layer, head) are read before any
+ * is written. */
+int32_t sub_kv_compact(const sub_kv_cache* kv, int64_t root_pos, const int32_t* accepted_slots,
+                       const int32_t* n_accepted, int32_t max_accept, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Model.  Layers [0, n_resident) keep bf16 weights on the device; layers
+ * [n_resident, n_layers) are offloaded: their bf16 originals live in pinned
+ * host memory and stream over the host link into a device staging ring for
+ * every target pass, while their int4 substitutes (from sub_w4_pack) serve
+ * the draft ("Low-Bit Shadow" report 2.1, 2.2 Step 4; card, measured
+ * effects: asynchronous data transfer).  All weight matrices are
+ * [out_features, in_features] row-major. */
+typedef struct {
+  const uint8_t* q;
+  const sub_bf16* scale;
+  const sub_bf16* zero;
+} sub_w4;
+
+typedef struct {
+  /* bf16 originals: device pointers (resident) or pinned host pointers (offloaded) */
+  const sub_bf16 *wq, *wk, *wv, *wo, *wg, *wu, *wd;
+  const sub_bf16 *attn_norm, *ffn_norm;            /* device [hidden] */
+  sub_w4 q4, k4, v4, o4, g4, u4, d4;                /* offloaded layers only */
+} sub_layer_desc;
+
+typedef struct {
+  int32_t n_layers, hidden, n_heads_q, n_heads_kv, head_dim, ffn, vocab, n_resident;
+  float rope_theta, rms_eps;
+  const sub_bf16* embed;        /* device [vocab, hidden] */
+  const sub_bf16* lm_head;      /* device [vocab, hidden] */
+  const sub_bf16* final_norm;   /* device [hidden] */
+  const sub_layer_desc* layers; /* host array [n_layers] */
+  int32_t max_seq;              /* prompt + generated tokens the cache must hold */
+  int32_t max_depth, max_width; /* largest tree the workspace is sized for */
+  int32_t staging_layers;       /* device ring slots for streamed originals; 0 = all */
+  int32_t max_prompt;           /* largest prompt (prefill rows) */
+} sub_model_desc;
+
+typedef struct sub_model sub_model;
+
+int32_t sub_model_create(const sub_model_desc* desc, sub_model** out);
+int32_t sub_model_destroy(sub_model* model);
+
+/* Device memory the model holds (weights it allocated + workspace), bytes. */
+int32_t sub_model_memory(const sub_model* model, int64_t* device_bytes);
+
+/* One forward of the target (which = 0) or the draft (which = 1) over rows
+ * that are tree slots [slot0, slot0 + n_rows) placed after a committed prefix of
+ * n_prefix tokens: row r (slot s = slot0 + r) carries token tokens[r] at
+ * position n_prefix + depth[r], reads positions [0, n_prefix) and the slots of
+ * anc[r * anc_stride ...] (root .. self), and writes its K,V at position
+ * n_prefix + s.  anc == NULL: chain (row r is slot slot0 + r, path 0..s).
+ * logits: fp32 [n_rows, vocab], or NULL.  A prefill is a chain with
+ * n_prefix = 0; a plain decode step is one row at slot 0. */
+int32_t sub_model_forward(sub_model* model, int32_t which, const int32_t* tokens, int32_t n_rows,
+                          int32_t slot0, const int32_t* depth, const int32_t* anc,
+                          int32_t anc_stride, int64_t n_prefix, float* logits, void* stream);
+
+/* The model's KV cache (for tests that inspect it). */
+int32_t sub_model_kv(sub_model* model, sub_kv_cache* out);
+
+typedef struct {
+  int32_t depth;          /* D >= 0; 0 = plain target decoding */
+  int32_t width;          /* k >= 1 */
+  float draft_temp;       /* 0.2 in the pages */
+  int32_t mode;           /* 0 greedy, 1 Gumbel-max sampling */
+  float target_temp;
+  uint64_t seed;
+  int32_t use_graph;      /* capture one decode cycle as a CUDA graph */
+} sub_decode_cfg;
+
+typedef struct {
+  int64_t cycles;         /* verify passes after the prefill */
+  int64_t emitted;        /* tokens generated (= n_new) */
+  double tau;             /* tokens per verify pass, counting the bonus */
+  double t_prefill_ms;
+  double t_decode_ms;
+  int64_t accept_hist[65];/* cycles that accepted a tokens, a <= 64 */
+} sub_stats;
+
+/* Generate n_new tokens after prompt_host (int32 [n_prompt], host) into
+ * out_tokens_host (int32 [n_new], host): prefill, then draft/verify/accept
+ * cycles until n_new tokens are emitted (the first comes from the prefill;
+ * the last cycle is truncated).  Synchronous.  stats may be NULL. */
+int32_t sub_generate(sub_model* model, const int32_t* prompt_host, int32_t n_prompt,
+                     int32_t n_new, const sub_decode_cfg* cfg, int32_t* out_tokens_host,
+                     sub_stats* stats);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SUB_API_H */

@@ -1,0 +1,376 @@
+// Tree-masked GQA attention over the paged shared KV cache.
+//
+// Tree verification scores every node of the draft tree in one target pass:
+// node u reads the committed prefix plus the keys of its own root path
+// ("SubSpec: Using the Target Model's Own Low-Bit Shadow as Its Draft Model",
+// 6.3 SpecInfer); the draft reads the same shared cache (report 4.1 point 2).
+//
+// Key index space of one call: j < n_prefix is cache position j (visible to
+// every query); j = n_prefix + s is tree slot s at position tree_base + s,
+// visible to query i when s is on i's root path (a per-query bitmap built in
+// shared memory from the ancestor lists; a chain when no lists are given).
+//
+// Rows are (query, head-in-group) pairs of one KV head, so the Hq/Hkv query
+// heads that share a KV head read each K/V tile once.  A CTA of four warps
+// owns 64 rows; S = Q K^T and O += P V run on mma.sync m16n8k16 with fp32
+// accumulators and an online softmax in fp32 (FlashAttention-2 style).  Keys
+// may be split over CTAs (grid.z); partial (max, sum, O) are then merged in a
+// fixed order by attn_combine_kernel.
+#include <mutex>
+#include "attn.cuh"
+
+namespace sub {
+
+namespace {
+constexpr int ROWS = 64, KT = 64, THREADS = 128;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool pred) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
+               "r"(pred ? 16 : 0));
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+}  // namespace
+
+// D = head_dim (64 or 128).  smem: Q [64][D], K/V double-buffered [2][64][D], bitmap.
+template <int D>
+__global__ void __launch_bounds__(THREADS) tree_attn_kernel(AttnArgs a) {
+  constexpr int CH = D / 8;  // 16-byte chunks per row
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* sQ = smem;
+  uint8_t* sK = sQ + ROWS * D * 2;
+  uint8_t* sV = sK + 2 * KT * D * 2;
+  uint32_t* sBits = reinterpret_cast<uint32_t*>(sV + 2 * KT * D * 2);
+  auto sw = [](int row, int ch) { return row * CH + (ch ^ (row & 7)); };
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int kvh = blockIdx.y;
+  const int G = a.n_heads_q / a.n_heads_kv;
+  const int n_rows = a.n_q * G;
+  const int row0 = blockIdx.x * ROWS;
+  const int n_prefix = a.n_prefix_dev ? *a.n_prefix_dev : (int)a.n_prefix;
+  const int64_t tree_base = a.tree_base_dev ? (int64_t)*a.tree_base_dev : a.tree_base;
+  const int n_keys = n_prefix + a.n_slots;
+  // this split's key range, whole tiles
+  const int tiles_total = (n_keys + KT - 1) / KT;
+  const int tiles_per = (tiles_total + gridDim.z - 1) / gridDim.z;
+  const int t_begin = blockIdx.z * tiles_per;
+  const int t_end = min(tiles_total, t_begin + tiles_per);
+
+  const int q_lo = row0 / G;
+  const int q_hi = min(a.n_q - 1, (row0 + ROWS - 1) / G);
+  const int words = (a.n_slots + 31) / 32;
+
+  // ---- visibility bitmaps of this CTA's queries ----
+  if (a.anc) {
+    const int nq = q_hi - q_lo + 1;
+    for (int i = tid; i < nq * words; i += THREADS) sBits[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < nq * a.anc_stride; i += THREADS) {
+      const int qq = i / a.anc_stride, j = i % a.anc_stride;
+      const int q = q_lo + qq;
+      if (j > a.depth[q]) continue;
+      const int s = a.anc[(int64_t)q * a.anc_stride + j];
+      if (s >= 0 && s < a.n_slots) atomicOr(&sBits[qq * words + (s >> 5)], 1u << (s & 31));
+    }
+  }
+
+  // ---- Q tile ----
+  const size_t q_row_stride = (size_t)a.n_heads_q * D;
+  for (int c = tid; c < ROWS * CH; c += THREADS) {
+    const int r = c / CH, ch = c % CH;
+    const int gr = row0 + r;
+    const bool ok = gr < n_rows;
+    const int q = ok ? gr / G : 0, h = ok ? gr % G : 0;
+    const uint16_t* src = a.Q + (size_t)q * q_row_stride + (size_t)(kvh * G + h) * D + ch * 8;
+    cp_async16(smem_u32(sQ + sw(r, ch) * 16), src, ok);
+  }
+  cp_commit();
+
+  const size_t head_stride = (size_t)a.page_size * D;
+  const size_t page_stride = (size_t)a.n_heads_kv * head_stride;
+  const size_t layer_off = (size_t)a.layer * a.n_pages * page_stride;
+  auto key_pos = [&](int j) -> int64_t {
+    return j < n_prefix ? (int64_t)j : tree_base + (j - n_prefix);
+  };
+  auto load_kv = [&](int buf, int t) {
+    for (int c = tid; c < KT * CH; c += THREADS) {
+      const int r = c / CH, ch = c % CH;
+      const int j = t * KT + r;
+      const bool ok = j < n_keys;
+      size_t off = 0;
+      if (ok) {
+        const int64_t p = key_pos(j);
+        const int page = a.page_table[p / a.page_size];
+        off = layer_off + (size_t)page * page_stride + (size_t)kvh * head_stride +
+              (size_t)(p % a.page_size) * D + ch * 8;
+      }
+      cp_async16(smem_u32(sK + buf * KT * D * 2 + sw(r, ch) * 16), a.k + off, ok);
+      cp_async16(smem_u32(sV + buf * KT * D * 2 + sw(r, ch) * 16), a.v + off, ok);
+    }
+  };
+
+  if (t_begin < t_end) load_kv(0, t_begin);
+  cp_commit();
+
+  // per-lane rows: g and g+8 of this warp's 16
+  const int g = lane >> 2, tig = lane & 3;
+  const int wrow = warp * 16;
+  int rq[2];      // query index of each of the lane's two rows (-1 if none)
+  int rslot[2];   // chain mode: the query's own slot
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int gr = row0 + wrow + g + 8 * h;
+    rq[h] = gr < n_rows ? gr / G : -1;
+    rslot[h] = rq[h] >= 0 ? a.chain_slot0 + rq[h] : -1;
+  }
+
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+  float o[D / 8][4];
+#pragma unroll
+  for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+
+  cp_wait<1>();   // Q landed
+  __syncthreads();
+  uint32_t qf[D / 16][4];
+  {
+    const uint32_t qb = smem_u32(sQ);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk)
+      ldsm_x4(qb + sw(wrow + (lane & 15), kk * 2 + (lane >> 4)) * 16, qf[kk][0], qf[kk][1],
+              qf[kk][2], qf[kk][3]);
+  }
+  const float sl2 = a.scale * 1.4426950408889634f;   // scores in log2 units
+
+  for (int t = t_begin; t < t_end; ++t) {
+    const int buf = (t - t_begin) & 1;
+    if (t + 1 < t_end) load_kv(buf ^ 1, t + 1);
+    cp_commit();
+    cp_wait<1>();
+    __syncthreads();
+
+    const uint32_t kb = smem_u32(sK + buf * KT * D * 2);
+    const uint32_t vb = smem_u32(sV + buf * KT * D * 2);
+    float s[KT / 8][4];
+#pragma unroll
+    for (int j = 0; j < KT / 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk)
+#pragma unroll
+      for (int jj = 0; jj < KT / 16; ++jj) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kb + sw(jj * 16 + (lane & 7) + ((lane >> 4) << 3), kk * 2 + ((lane >> 3) & 1)) * 16,
+                b0, b1, b2, b3);
+        mma_bf16_16816(s[2 * jj], qf[kk], b0, b1);
+        mma_bf16_16816(s[2 * jj + 1], qf[kk], b2, b3);
+      }
+    // mask, scale, online softmax
+    float tmax[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int j = 0; j < KT / 8; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int h = e >> 1;
+        const int key = t * KT + j * 8 + 2 * tig + (e & 1);
+        bool vis = false;
+        if (rq[h] >= 0 && key < n_keys) {
+          if (key < n_prefix) vis = true;
+          else {
+            const int sl = key - n_prefix;
+            if (a.anc) vis = (sBits[(rq[h] - q_lo) * words + (sl >> 5)] >> (sl & 31)) & 1u;
+            else vis = sl <= rslot[h];
+          }
+        }
+        const float v = vis ? s[j][e] * sl2 : -INFINITY;
+        s[j][e] = v;
+        tmax[h] = fmaxf(tmax[h], v);
+      }
+    float corr[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      tmax[h] = fmaxf(tmax[h], __shfl_xor_sync(0xffffffffu, tmax[h], 1));
+      tmax[h] = fmaxf(tmax[h], __shfl_xor_sync(0xffffffffu, tmax[h], 2));
+      const float m_new = fmaxf(m_run[h], tmax[h]);
+      corr[h] = (m_new == -INFINITY) ? 1.f : exp2f(m_run[h] - m_new);
+      m_run[h] = m_new;
+    }
+    float tsum[2] = {0.f, 0.f};
+    uint32_t pa[KT / 16][4];
+#pragma unroll
+    for (int j = 0; j < KT / 8; ++j) {
+      float p[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int h = e >> 1;
+        p[e] = (m_run[h] == -INFINITY) ? 0.f : exp2f(s[j][e] - m_run[h]);
+        tsum[h] += p[e];
+      }
+      // P as the A operand: n8 tiles 2i, 2i+1 form k16 step i
+      if (j & 1) {
+        pa[j >> 1][2] = pack_bf16x2(p[0], p[1]);
+        pa[j >> 1][3] = pack_bf16x2(p[2], p[3]);
+      } else {
+        pa[j >> 1][0] = pack_bf16x2(p[0], p[1]);
+        pa[j >> 1][1] = pack_bf16x2(p[2], p[3]);
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      tsum[h] += __shfl_xor_sync(0xffffffffu, tsum[h], 1);
+      tsum[h] += __shfl_xor_sync(0xffffffffu, tsum[h], 2);
+      l_run[h] = l_run[h] * corr[h] + tsum[h];
+    }
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) {
+      o[i][0] *= corr[0]; o[i][1] *= corr[0];
+      o[i][2] *= corr[1]; o[i][3] *= corr[1];
+    }
+#pragma unroll
+    for (int kk = 0; kk < KT / 16; ++kk)
+#pragma unroll
+      for (int dd = 0; dd < D / 16; ++dd) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vb + sw(kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3), dd * 2 + (lane >> 4)) * 16,
+                  b0, b1, b2, b3);
+        mma_bf16_16816(o[2 * dd], pa[kk], b0, b1);
+        mma_bf16_16816(o[2 * dd + 1], pa[kk], b2, b3);
+      }
+    __syncthreads();   // buffer reuse by the next prefetch
+  }
+
+  // ---- write out ----
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int gr = row0 + wrow + g + 8 * h;
+    if (gr >= n_rows) continue;
+    const int q = gr / G, hh = gr % G;
+    const size_t orow = (size_t)q * a.n_heads_q + kvh * G + hh;   // row of [n_q*Hq]
+    if (gridDim.z == 1) {
+      const float inv = l_run[h] > 0.f ? 1.f / l_run[h] : 0.f;
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i) {
+        const int c = i * 8 + 2 * tig;
+        *reinterpret_cast<uint32_t*>(a.O + orow * D + c) =
+            pack_bf16x2(o[i][2 * h] * inv, o[i][2 * h + 1] * inv);
+      }
+    } else {
+      const size_t base = ((size_t)blockIdx.z * a.n_q * a.n_heads_q + orow);
+      float* po = a.part_o + base * D;
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i) {
+        const int c = i * 8 + 2 * tig;
+        po[c] = o[i][2 * h];
+        po[c + 1] = o[i][2 * h + 1];
+      }
+      if (tig == 0) {
+        a.part_m[base] = m_run[h];
+        a.part_l[base] = l_run[h];
+      }
+    }
+  }
+}
+
+// Merge split partials in split order: O = sum_s w_s o_s / sum_s w_s l_s,
+// w_s = 2^(m_s - max_s m_s).  One warp per output row.
+template <int D>
+__global__ void attn_combine_kernel(AttnArgs a, int n_split) {
+  const int row = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  const int n_out = a.n_q * a.n_heads_q;
+  if (row >= n_out) return;
+  float mx = -INFINITY;
+  for (int s = 0; s < n_split; ++s) mx = fmaxf(mx, a.part_m[(size_t)s * n_out + row]);
+  float den = 0.f;
+  float num[D / 32];
+#pragma unroll
+  for (int i = 0; i < D / 32; ++i) num[i] = 0.f;
+  for (int s = 0; s < n_split; ++s) {
+    const float ms = a.part_m[(size_t)s * n_out + row];
+    const float w = (ms == -INFINITY) ? 0.f : exp2f(ms - mx);
+    den += w * a.part_l[(size_t)s * n_out + row];
+    const float* po = a.part_o + ((size_t)s * n_out + row) * D;
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i) num[i] += w * po[lane + 32 * i];
+  }
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+#pragma unroll
+  for (int i = 0; i < D / 32; ++i)
+    reinterpret_cast<__nv_bfloat16*>(a.O)[(size_t)row * D + lane + 32 * i] =
+        __float2bfloat16_rn(num[i] * inv);
+}
+
+int attn_smem_bytes(const AttnArgs& a) {
+  const int d = a.head_dim;
+  const int G = a.n_heads_q / a.n_heads_kv;
+  const int nq = ROWS / G + 2;
+  const int words = (a.n_slots + 31) / 32;
+  return ROWS * d * 2 + 4 * KT * d * 2 + (a.anc ? nq * words * 4 : 0);
+}
+
+int attn_pick_splits(const AttnArgs& a, int n_keys_hint) {
+  const int G = a.n_heads_q / a.n_heads_kv;
+  const int blocks = (a.n_q * G + ROWS - 1) / ROWS * a.n_heads_kv;
+  const int tiles = (n_keys_hint + KT - 1) / KT;
+  int s = (2 * 152 + blocks - 1) / blocks;
+  s = std::max(1, std::min(s, std::min(tiles, 32)));
+  return s;
+}
+
+// Opt the kernels into the largest dynamic shared memory once per process
+// (before any stream capture: model creation calls this).
+int32_t attn_init() {
+  static std::once_flag once;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    err = cudaFuncSetAttribute(tree_attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               ATTN_MAX_SMEM);
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(tree_attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 ATTN_MAX_SMEM);
+  });
+  if (err != cudaSuccess) return fail(SUB_ECUDA, std::string("attn_init: ") + cudaGetErrorString(err));
+  return SUB_OK;
+}
+
+int32_t launch_tree_attn(const AttnArgs& a, int n_split, cudaStream_t st) {
+  SUB_CHECK_ARG(a.head_dim == 64 || a.head_dim == 128, "attn: head_dim must be 64 or 128");
+  SUB_CHECK_ARG(a.n_heads_kv >= 1 && a.n_heads_q % a.n_heads_kv == 0, "attn: Hq % Hkv != 0");
+  SUB_CHECK_ARG(a.page_size % 16 == 0 && a.page_size > 0, "attn: page_size % 16 != 0");
+  SUB_CHECK_ARG(a.n_slots >= 0 && a.n_slots <= 16384, "attn: n_slots out of range");
+  SUB_CHECK_ARG(n_split >= 1 && n_split <= 64, "attn: bad split count");
+  if (a.n_q == 0) return SUB_OK;
+  const int G = a.n_heads_q / a.n_heads_kv;
+  const int smem = attn_smem_bytes(a);
+  SUB_CHECK_ARG(smem <= ATTN_MAX_SMEM, "attn: tree too large for the shared-memory bitmap");
+  SUB_TRY(attn_init());
+  dim3 grid((a.n_q * G + ROWS - 1) / ROWS, a.n_heads_kv, n_split);
+  if (a.head_dim == 128) tree_attn_kernel<128><<<grid, THREADS, smem, st>>>(a);
+  else tree_attn_kernel<64><<<grid, THREADS, smem, st>>>(a);
+  SUB_TRY(check_launch("tree_attn"));
+  if (n_split > 1) {
+    const int rows = a.n_q * a.n_heads_q;
+    const int wpb = 8;
+    if (a.head_dim == 128)
+      attn_combine_kernel<128><<<(rows + wpb - 1) / wpb, wpb * 32, 0, st>>>(a, n_split);
+    else
+      attn_combine_kernel<64><<<(rows + wpb - 1) / wpb, wpb * 32, 0, st>>>(a, n_split);
+    SUB_TRY(check_launch("attn_combine"));
+  }
+  return SUB_OK;
+}
+
+}  // namespace sub

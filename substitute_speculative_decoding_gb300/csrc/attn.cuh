@@ -1,0 +1,45 @@
+// Tree-masked GQA attention over the paged KV cache (see attn.cu).
+#pragma once
+#include <algorithm>
+#include "common.cuh"
+
+namespace sub {
+
+struct AttnArgs {
+  const uint16_t* Q;        // [n_q, Hq, D] bf16
+  uint16_t* O;              // [n_q, Hq, D] bf16
+  int n_q, n_heads_q, n_heads_kv, head_dim;
+  // cache
+  const uint16_t* k;
+  const uint16_t* v;
+  const int32_t* page_table;
+  int page_size, n_pages, layer;
+  // key space
+  int64_t n_prefix;             // committed keys [0, n_prefix) ...
+  const int32_t* n_prefix_dev;  // ... or read on the device when non-null
+  int64_t tree_base;            // position of tree slot 0 ...
+  const int32_t* tree_base_dev; // ... or read on the device when non-null
+  int n_slots;                  // tree slots [0, n_slots) addressable by this call
+  const int32_t* anc;           // [n_q, anc_stride] root..self slot lists, or null (chain)
+  int anc_stride;
+  const int32_t* depth;         // [n_q] path length - 1 (with anc)
+  int chain_slot0;              // chain mode: query i is slot chain_slot0 + i
+  float scale;
+  // split-K partials (n_split > 1): [n_split, n_q*Hq, D], [n_split, n_q*Hq] x2
+  float* part_o;
+  float* part_m;
+  float* part_l;
+};
+
+constexpr int ATTN_MAX_SMEM = 200 * 1024;
+int32_t attn_init();
+int attn_smem_bytes(const AttnArgs& a);
+int attn_pick_splits(const AttnArgs& a, int n_keys_hint);
+// Floats of split scratch needed for n_split splits.
+inline size_t attn_scratch_floats(const AttnArgs& a, int n_split) {
+  const size_t rows = (size_t)a.n_q * a.n_heads_q;
+  return n_split > 1 ? (size_t)n_split * rows * (a.head_dim + 2) : 0;
+}
+int32_t launch_tree_attn(const AttnArgs& a, int n_split, cudaStream_t st);
+
+}  // namespace sub

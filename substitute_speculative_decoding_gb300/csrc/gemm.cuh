@@ -1,0 +1,20 @@
+// Tiled tensor-core GEMM for tree-shaped products (M > 16 rows): the verify
+// pass over every tree node, the prefill, and int4 products at tree widths.
+// Y[m, n] = sum_k X[m, k] W[n, k]; rows are independent (no split over K that
+// depends on M), so a row's result does not depend on how many rows share
+// the pass.
+#pragma once
+#include "gemv.cuh"
+
+namespace sub {
+
+int32_t gemm_init();
+// Same argument block and epilogues as the GEMV (GemvArgs); M is unbounded.
+int32_t launch_gemm(const GemvArgs& a, bool is_w4, int epi, cudaStream_t stream);
+
+// Dispatch on M: GEMV for M <= 16, tiled GEMM otherwise.
+inline int32_t launch_matmul(const GemvArgs& a, bool is_w4, int epi, cudaStream_t stream) {
+  return a.M <= 16 ? launch_gemv(a, is_w4, epi, stream) : launch_gemm(a, is_w4, epi, stream);
+}
+
+}  // namespace sub

@@ -1,0 +1,102 @@
+// Row kernels of the decoder layer (see layers.cuh).  The residual stream is
+// fp32; matmul inputs and the KV cache are bf16, rounded to nearest even.
+#include "layers.cuh"
+
+namespace sub {
+
+__device__ __forceinline__ int row_depth(const RowSet& rs, int r) {
+  return rs.depth ? rs.depth[r] : rs.slot0 + r;
+}
+__device__ __forceinline__ int64_t row_base(const RowSet& rs) {
+  return rs.base_dev ? (int64_t)*rs.base_dev : rs.base;
+}
+
+__global__ void embed_kernel(const uint16_t* __restrict__ embed, int hidden, RowSet rs,
+                             float* __restrict__ x) {
+  const int r = blockIdx.x;
+  const int64_t tok = rs.tokens[r];
+  const uint16_t* src = embed + tok * hidden;
+  for (int i = threadIdx.x; i < hidden; i += blockDim.x)
+    x[(int64_t)r * hidden + i] = bf16_bits_to_f32(src[i]);
+}
+
+int32_t launch_embed(const uint16_t* embed, int hidden, const RowSet& rs, int rows, float* x,
+                     cudaStream_t st) {
+  if (rows <= 0) return SUB_OK;
+  embed_kernel<<<rows, 256, 0, st>>>(embed, hidden, rs, x);
+  return check_launch("embed");
+}
+
+// y = bf16(x * rsqrt(mean(x^2) + eps) * gain); one CTA per row, fixed-order sum.
+__global__ void rmsnorm_kernel(const float* __restrict__ x, const uint16_t* __restrict__ gain,
+                               int hidden, float eps, uint16_t* __restrict__ out) {
+  __shared__ float s_part[32];
+  const int r = blockIdx.x;
+  const float* xr = x + (int64_t)r * hidden;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < hidden; i += blockDim.x) ss = fmaf(xr[i], xr[i], ss);
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) s_part[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += s_part[w];
+  const float inv = rsqrtf(tot / (float)hidden + eps);
+  for (int i = threadIdx.x; i < hidden; i += blockDim.x)
+    reinterpret_cast<__nv_bfloat16*>(out)[(int64_t)r * hidden + i] =
+        __float2bfloat16_rn(xr[i] * inv * bf16_bits_to_f32(gain[i]));
+}
+
+int32_t launch_rmsnorm(const float* x, const uint16_t* gain, int rows, int hidden, float eps,
+                       uint16_t* out, cudaStream_t st) {
+  if (rows <= 0) return SUB_OK;
+  rmsnorm_kernel<<<rows, 256, 0, st>>>(x, gain, hidden, eps, out);
+  return check_launch("rmsnorm");
+}
+
+// One CTA per row: q heads get RoPE -> bf16 q_out; k heads RoPE -> cache;
+// v heads -> cache.  Rotate-half pairing: element i with i + D/2.
+__global__ void qkv_post_kernel(QkvPostArgs a) {
+  const int r = blockIdx.x;
+  const int D = a.head_dim, half = D / 2;
+  const int nh = a.n_heads_q + 2 * a.n_heads_kv;
+  const int64_t base = row_base(a.rs);
+  const int64_t pos = base + row_depth(a.rs, r);
+  const int64_t kvpos = base + a.rs.slot0 + r;
+  const float* src = a.qkv + (int64_t)r * nh * D;
+  const float2* cs = a.rope + (pos < a.max_pos ? pos : a.max_pos - 1) * half;
+  const size_t head_stride = (size_t)a.page_size * D;
+  const size_t page_stride = (size_t)a.n_heads_kv * head_stride;
+  const size_t slot_off = (size_t)a.layer * a.n_pages * page_stride +
+                          (size_t)a.page_table[kvpos / a.page_size] * page_stride +
+                          (size_t)(kvpos % a.page_size) * D;
+  for (int idx = threadIdx.x; idx < nh * half; idx += blockDim.x) {
+    const int h = idx / half, i = idx % half;
+    const float x1 = src[h * D + i], x2 = src[h * D + i + half];
+    if (h < a.n_heads_q + a.n_heads_kv) {
+      const float2 c = cs[i];
+      const float y1 = x1 * c.x - x2 * c.y;
+      const float y2 = x2 * c.x + x1 * c.y;
+      if (h < a.n_heads_q) {
+        uint16_t* q = a.q_out + ((int64_t)r * a.n_heads_q + h) * D;
+        q[i] = f32_to_bf16_bits(y1);
+        q[i + half] = f32_to_bf16_bits(y2);
+      } else {
+        uint16_t* k = a.k_cache + slot_off + (size_t)(h - a.n_heads_q) * head_stride;
+        k[i] = f32_to_bf16_bits(y1);
+        k[i + half] = f32_to_bf16_bits(y2);
+      }
+    } else {
+      uint16_t* v = a.v_cache + slot_off + (size_t)(h - a.n_heads_q - a.n_heads_kv) * head_stride;
+      v[i] = f32_to_bf16_bits(x1);
+      v[i + half] = f32_to_bf16_bits(x2);
+    }
+  }
+}
+
+int32_t launch_qkv_post(const QkvPostArgs& a, cudaStream_t st) {
+  if (a.rows <= 0) return SUB_OK;
+  qkv_post_kernel<<<a.rows, 256, 0, st>>>(a);
+  return check_launch("qkv_post");
+}
+
+}  // namespace sub

@@ -1,0 +1,794 @@
+// Model runtime: weights, shared paged KV cache, workspace, the streamed
+// originals of offloaded layers, the decoder forward, and the SubSpec decode
+// loop (draft D levels -> verify the tree in one target pass -> accept ->
+// compact), optionally captured once as a CUDA graph and replayed per cycle.
+//
+// Method: "SubSpec: Using the Target Model's Own Low-Bit Shadow as Its Draft
+// Model" (2.1 offloading, 2.2 Step 4 substitutes + sharing + prefetch, 6.3
+// tree verification) and "Speculate Deep and Accurate" (card: Approach and the
+// measured effects of shared KV, sharpening and asynchronous transfer).
+//
+// Streams: the compute stream runs every kernel; a copy stream moves the bf16
+// originals of offloaded layers from pinned host memory into a device ring of
+// staging slots.  A target pass waits per layer for its slot to be staged;
+// the copies for the first ring-full of layers are issued at the start of a
+// cycle, so they run under the draft.
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+#include <vector>
+#include "attn.cuh"
+#include "gemm.cuh"
+#include "layers.cuh"
+#include "tree.cuh"
+
+namespace sub {
+
+struct Matrices {
+  const void* w[7];   // wq wk wv wo wg wu wd (bf16 or packed int4)
+  const uint16_t* s[7];
+  const uint16_t* z[7];
+};
+
+// Decode state on the device (one int each).
+enum { ST_N = 0, ST_EMITTED = 1, ST_NACC = 2, ST_BONUS = 3, ST_COUNT = 8 };
+
+}  // namespace sub
+
+struct sub_model {
+  sub_model_desc d{};
+  std::vector<sub_layer_desc> layers;
+  int qkv_dim = 0, q_dim = 0, kv_dim = 0;
+  int rows_max = 0;         // largest forward (tree or prompt)
+  int logit_rows = 0;
+  int64_t dev_bytes = 0;
+  std::vector<void*> allocs;
+  // cache
+  uint16_t* kpool = nullptr;
+  uint16_t* vpool = nullptr;
+  int32_t* page_table = nullptr;
+  int page_size = 64, n_pages = 0;
+  int64_t capacity = 0;
+  float2* rope = nullptr;
+  int max_pos = 0;
+  // activations
+  float* x = nullptr;        // [rows, H]
+  uint16_t* xn = nullptr;    // [rows, H]
+  float* qkv = nullptr;      // [rows, qkv_dim]
+  uint16_t* q = nullptr;     // [rows, Hq*D]
+  uint16_t* attn = nullptr;  // [rows, Hq*D]
+  uint16_t* act = nullptr;   // [rows, F]
+  float* logits = nullptr;   // [logit_rows, V]
+  int32_t* rows_tok = nullptr;  // [rows] token ids staged for a forward
+  float* attn_part = nullptr;
+  size_t attn_part_floats = 0;
+  // tree + decode state
+  sub_tree tree{};
+  int32_t* state = nullptr;
+  int32_t* accepted = nullptr;
+  int32_t* choice = nullptr;
+  int32_t* out_tokens = nullptr;
+  int out_cap = 0;
+  int32_t* hist = nullptr;
+  unsigned long long* part_key = nullptr;
+  float* part_f = nullptr;
+  unsigned int* counters = nullptr;   // [0] expand, [1] accept
+  size_t part_keys = 0, part_floats = 0;
+  // staging ring
+  int n_off = 0, ring = 0;
+  size_t layer_bytes = 0;
+  size_t mat_off[7] = {};
+  size_t mat_bytes[7] = {};
+  std::vector<uint16_t*> slots;
+  cudaStream_t s_main = nullptr, s_copy = nullptr;
+  std::vector<cudaEvent_t> ev_staged, ev_free;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr, ev_t0 = nullptr, ev_t1 = nullptr;
+  int32_t* host_state = nullptr;   // pinned
+  // graph of one decode cycle
+  cudaGraphExec_t graph = nullptr;
+  sub_decode_cfg graph_cfg{};
+};
+
+namespace sub {
+
+static int32_t dalloc(sub_model* m, void** p, size_t bytes) {
+  if (bytes == 0) bytes = 16;
+  const cudaError_t e = cudaMalloc(p, bytes);
+  if (e != cudaSuccess) {
+    *p = nullptr;
+    return fail(SUB_ENOMEM, std::string("cudaMalloc(") + std::to_string(bytes) +
+                                "): " + cudaGetErrorString(e));
+  }
+  m->allocs.push_back(*p);
+  m->dev_bytes += (int64_t)bytes;
+  return SUB_OK;
+}
+template <class T>
+static int32_t dalloc_t(sub_model* m, T** p, size_t count) {
+  return dalloc(m, reinterpret_cast<void**>(p), count * sizeof(T));
+}
+
+static void free_model(sub_model* m) {
+  if (!m) return;
+  if (m->s_main) cudaStreamSynchronize(m->s_main);
+  if (m->s_copy) cudaStreamSynchronize(m->s_copy);
+  if (m->graph) cudaGraphExecDestroy(m->graph);
+  for (void* p : m->allocs) cudaFree(p);
+  for (cudaEvent_t e : m->ev_staged) cudaEventDestroy(e);
+  for (cudaEvent_t e : m->ev_free) cudaEventDestroy(e);
+  for (cudaEvent_t e : {m->ev_fork, m->ev_join, m->ev_t0, m->ev_t1})
+    if (e) cudaEventDestroy(e);
+  if (m->s_main) cudaStreamDestroy(m->s_main);
+  if (m->s_copy) cudaStreamDestroy(m->s_copy);
+  if (m->host_state) cudaFreeHost(m->host_state);
+  delete m;
+}
+
+static const uint16_t* const* mats_of(const sub_layer_desc& L) {
+  static thread_local const uint16_t* p[7];
+  p[0] = L.wq; p[1] = L.wk; p[2] = L.wv; p[3] = L.wo; p[4] = L.wg; p[5] = L.wu; p[6] = L.wd;
+  return p;
+}
+
+// Weights of layer l for the target (staged originals when offloaded) or the draft.
+static Matrices layer_mats(const sub_model* m, int l, bool draft) {
+  Matrices r{};
+  const sub_layer_desc& L = m->layers[l];
+  const bool off = l >= m->d.n_resident;
+  if (off && draft) {
+    const sub_w4* w4[7] = {&L.q4, &L.k4, &L.v4, &L.o4, &L.g4, &L.u4, &L.d4};
+    for (int i = 0; i < 7; ++i) {
+      r.w[i] = w4[i]->q;
+      r.s[i] = w4[i]->scale;
+      r.z[i] = w4[i]->zero;
+    }
+  } else if (off) {
+    const uint8_t* base = reinterpret_cast<const uint8_t*>(m->slots[(l - m->d.n_resident) % m->ring]);
+    for (int i = 0; i < 7; ++i) r.w[i] = base + m->mat_off[i];
+  } else {
+    const uint16_t* const* p = mats_of(L);
+    for (int i = 0; i < 7; ++i) r.w[i] = p[i];
+  }
+  return r;
+}
+
+// ---------------------------------------------------------------- streaming --
+static int32_t issue_copy(sub_model* m, int j) {
+  const sub_layer_desc& L = m->layers[m->d.n_resident + j];
+  uint8_t* dst = reinterpret_cast<uint8_t*>(m->slots[j % m->ring]);
+  const uint16_t* const* src = mats_of(L);
+  for (int i = 0; i < 7; ++i)
+    SUB_CUDA_TRY(cudaMemcpyAsync(dst + m->mat_off[i], src[i], m->mat_bytes[i],
+                                 cudaMemcpyHostToDevice, m->s_copy));
+  SUB_CUDA_TRY(cudaEventRecord(m->ev_staged[j], m->s_copy));
+  return SUB_OK;
+}
+
+// Fork the copy stream off the compute stream and stage the first ring-full.
+static int32_t begin_target_pass(sub_model* m) {
+  if (m->n_off == 0) return SUB_OK;
+  SUB_CUDA_TRY(cudaEventRecord(m->ev_fork, m->s_main));
+  SUB_CUDA_TRY(cudaStreamWaitEvent(m->s_copy, m->ev_fork, 0));
+  for (int j = 0; j < std::min(m->ring, m->n_off); ++j) SUB_TRY(issue_copy(m, j));
+  return SUB_OK;
+}
+// Join the copy stream back (always, so a capture ends with both streams joined).
+static int32_t end_target_pass(sub_model* m) {
+  if (m->n_off == 0) return SUB_OK;
+  SUB_CUDA_TRY(cudaEventRecord(m->ev_join, m->s_copy));
+  SUB_CUDA_TRY(cudaStreamWaitEvent(m->s_main, m->ev_join, 0));
+  return SUB_OK;
+}
+
+// ------------------------------------------------------------------ forward --
+struct FwdRows {
+  const int32_t* tokens;   // [n]
+  int n;
+  int slot0;
+  const int32_t* depth;    // [n] or null (chain)
+  const int32_t* anc;      // [n, stride] or null (chain)
+  int anc_stride;
+  int n_slots;
+  int64_t base;            // committed length (host) ...
+  const int32_t* base_dev; // ... or on the device
+  int64_t keys_hint;       // for the split heuristic
+};
+
+static GemvArgs mm_args(const void* X, int M, int K, const Matrices& W, const int* idx, int nseg,
+                        const int* rows, void* Y, int ldy) {
+  GemvArgs a{};
+  a.X = reinterpret_cast<const uint16_t*>(X);
+  a.M = M;
+  a.K = K;
+  a.ldx = K;
+  int acc = 0;
+  for (int i = 0; i < nseg; ++i) {
+    a.W[i] = W.w[idx[i]];
+    a.S[i] = W.s[idx[i]];
+    a.Z[i] = W.z[idx[i]];
+    acc += rows[i];
+    a.seg_end[i] = acc;
+  }
+  a.n_seg = nseg;
+  a.N = acc;
+  a.Y = Y;
+  a.ldy = ldy;
+  return a;
+}
+
+static int32_t forward(sub_model* m, bool draft, const FwdRows& r, float* logits, bool last_only) {
+  const sub_model_desc& d = m->d;
+  const cudaStream_t st = m->s_main;
+  const int H = d.hidden, F = d.ffn, D = d.head_dim;
+  const int M = r.n;
+  RowSet rs{};
+  rs.tokens = r.tokens;
+  rs.depth = r.depth;
+  rs.slot0 = r.slot0;
+  rs.base = r.base;
+  rs.base_dev = r.base_dev;
+  SUB_TRY(launch_embed(d.embed, H, rs, M, m->x, st));
+
+  AttnArgs at{};
+  at.Q = m->q;
+  at.O = m->attn;
+  at.n_q = M;
+  at.n_heads_q = d.n_heads_q;
+  at.n_heads_kv = d.n_heads_kv;
+  at.head_dim = D;
+  at.k = m->kpool;
+  at.v = m->vpool;
+  at.page_table = m->page_table;
+  at.page_size = m->page_size;
+  at.n_pages = m->n_pages;
+  at.n_prefix = r.base;
+  at.n_prefix_dev = r.base_dev;
+  at.tree_base = r.base;
+  at.tree_base_dev = r.base_dev;
+  at.n_slots = r.n_slots;
+  at.anc = r.anc;
+  at.anc_stride = r.anc_stride;
+  at.depth = r.depth;
+  at.chain_slot0 = r.slot0;
+  at.scale = 1.0f / sqrtf((float)D);
+  int splits = attn_pick_splits(at, (int)std::min<int64_t>(r.keys_hint, 1 << 30));
+  while (splits > 1 && attn_scratch_floats(at, splits) > m->attn_part_floats) --splits;
+  if (splits > 1) {
+    const size_t rows = (size_t)M * d.n_heads_q;
+    at.part_o = m->attn_part;
+    at.part_m = at.part_o + (size_t)splits * rows * D;
+    at.part_l = at.part_m + (size_t)splits * rows;
+  }
+
+  QkvPostArgs qp{};
+  qp.qkv = m->qkv;
+  qp.rows = M;
+  qp.n_heads_q = d.n_heads_q;
+  qp.n_heads_kv = d.n_heads_kv;
+  qp.head_dim = D;
+  qp.rope = m->rope;
+  qp.max_pos = m->max_pos;
+  qp.rs = rs;
+  qp.q_out = m->q;
+  qp.k_cache = m->kpool;
+  qp.v_cache = m->vpool;
+  qp.page_table = m->page_table;
+  qp.page_size = m->page_size;
+  qp.n_pages = m->n_pages;
+
+  const int qkv_rows[3] = {m->q_dim, m->kv_dim, m->kv_dim};
+  const int qkv_idx[3] = {0, 1, 2};
+  const int o_rows[1] = {H};
+  const int o_idx[1] = {3};
+  const int gu_rows[2] = {F, F};
+  const int gu_idx[2] = {4, 5};
+  const int dn_idx[1] = {6};
+
+  for (int l = 0; l < d.n_layers; ++l) {
+    const sub_layer_desc& L = m->layers[l];
+    const bool off = l >= d.n_resident;
+    const bool w4 = off && draft;
+    const int j = l - d.n_resident;
+    if (off && !draft) SUB_CUDA_TRY(cudaStreamWaitEvent(st, m->ev_staged[j], 0));
+    const Matrices W = layer_mats(m, l, draft);
+
+    SUB_TRY(launch_rmsnorm(m->x, L.attn_norm, M, H, d.rms_eps, m->xn, st));
+    SUB_TRY(launch_matmul(mm_args(m->xn, M, H, W, qkv_idx, 3, qkv_rows, m->qkv, m->qkv_dim), w4,
+                          EPI_F32, st));
+    qp.layer = l;
+    SUB_TRY(launch_qkv_post(qp, st));
+    at.layer = l;
+    SUB_TRY(launch_tree_attn(at, splits, st));
+    SUB_TRY(launch_matmul(mm_args(m->attn, M, m->q_dim, W, o_idx, 1, o_rows, m->x, H), w4,
+                          EPI_RESID, st));
+    SUB_TRY(launch_rmsnorm(m->x, L.ffn_norm, M, H, d.rms_eps, m->xn, st));
+    {
+      GemvArgs ga = mm_args(m->xn, M, H, W, gu_idx, 2, gu_rows, m->act, F);
+      ga.N = F;   // GLU: grid covers one segment's rows
+      SUB_TRY(launch_matmul(ga, w4, EPI_GLU, st));
+    }
+    SUB_TRY(launch_matmul(mm_args(m->act, M, F, W, dn_idx, 1, o_rows, m->x, H), w4, EPI_RESID, st));
+
+    if (off && !draft) {
+      // slot j % ring is free once this layer's kernels are done: stage layer j + ring
+      if (j + m->ring < m->n_off) {
+        SUB_CUDA_TRY(cudaEventRecord(m->ev_free[j], st));
+        SUB_CUDA_TRY(cudaStreamWaitEvent(m->s_copy, m->ev_free[j], 0));
+        SUB_TRY(issue_copy(m, j + m->ring));
+      }
+    }
+  }
+  // final norm + lm_head
+  const int first = last_only ? M - 1 : 0;
+  const int nrow = last_only ? 1 : M;
+  SUB_TRY(launch_rmsnorm(m->x + (size_t)first * H, d.final_norm, nrow, H, d.rms_eps, m->xn, st));
+  if (logits) {
+    Matrices lm{};
+    lm.w[0] = d.lm_head;
+    const int idx0[1] = {0};
+    const int vrows[1] = {d.vocab};
+    SUB_TRY(launch_matmul(mm_args(m->xn, nrow, H, lm, idx0, 1, vrows, logits, d.vocab), false,
+                          EPI_F32, st));
+  }
+  return SUB_OK;
+}
+
+// ------------------------------------------------------------ tiny kernels --
+// After accept: committed length += accepted + 1, the bonus becomes the root.
+__global__ void advance_kernel(int32_t* state, int32_t* root_token) {
+  state[ST_N] += state[ST_NACC] + 1;
+  *root_token = state[ST_BONUS];
+}
+
+}  // namespace sub
+
+using namespace sub;
+
+// ------------------------------------------------------------------ create --
+extern "C" int32_t sub_model_create(const sub_model_desc* desc, sub_model** out) {
+  SUB_CHECK_ARG(desc && out && desc->layers, "null pointer");
+  const sub_model_desc& d = *desc;
+  SUB_CHECK_ARG(d.n_layers >= 1 && d.hidden >= 64 && d.hidden % 64 == 0, "bad n_layers/hidden");
+  SUB_CHECK_ARG(d.head_dim == 64 || d.head_dim == 128, "head_dim must be 64 or 128");
+  SUB_CHECK_ARG(d.n_heads_kv >= 1 && d.n_heads_q % d.n_heads_kv == 0, "Hq % Hkv != 0");
+  SUB_CHECK_ARG(d.ffn % 16 == 0 && d.vocab >= 16 && d.vocab <= (1 << 20), "bad ffn/vocab");
+  SUB_CHECK_ARG(d.n_resident >= 0 && d.n_resident <= d.n_layers, "bad n_resident");
+  SUB_CHECK_ARG(d.max_seq >= 2 && d.max_prompt >= 1 && d.max_prompt <= d.max_seq, "bad max_seq");
+  SUB_CHECK_ARG(d.max_depth >= 0 && d.max_depth <= 64 && d.max_width >= 1 &&
+                    d.max_width <= MAX_WIDTH,
+                "tree size out of range (depth <= 64, width <= 16)");
+  SUB_CHECK_ARG(d.embed && d.lm_head && d.final_norm, "null global weights");
+  *out = nullptr;
+  sub_model* m = new sub_model();
+  m->d = d;
+  m->layers.assign(d.layers, d.layers + d.n_layers);
+  m->d.layers = m->layers.data();
+  auto bail = [&](int32_t code) {
+    const std::string msg = sub_last_error();
+    free_model(m);
+    set_error(msg);
+    return code;
+  };
+#define CREATE_TRY(expr) do { int32_t _s = (expr); if (_s != SUB_OK) return bail(_s); } while (0)
+#define CREATE_CUDA(expr) do { cudaError_t _e = (expr); if (_e != cudaSuccess) { \
+    fail(SUB_ECUDA, std::string(#expr) + ": " + cudaGetErrorString(_e)); return bail(SUB_ECUDA); } } while (0)
+
+  for (int l = 0; l < d.n_layers; ++l) {
+    const sub_layer_desc& L = d.layers[l];
+    if (!(L.wq && L.wk && L.wv && L.wo && L.wg && L.wu && L.wd && L.attn_norm && L.ffn_norm)) {
+      fail(SUB_EINVAL, "layer " + std::to_string(l) + ": null weight");
+      return bail(SUB_EINVAL);
+    }
+    if (l >= d.n_resident) {
+      const sub_w4* w4[7] = {&L.q4, &L.k4, &L.v4, &L.o4, &L.g4, &L.u4, &L.d4};
+      for (auto* w : w4)
+        if (!(w->q && w->scale && w->zero)) {
+          fail(SUB_EINVAL, "layer " + std::to_string(l) + ": null int4 substitute");
+          return bail(SUB_EINVAL);
+        }
+    }
+  }
+  CREATE_TRY(gemm_init());
+  CREATE_TRY(attn_init());
+  CREATE_CUDA(cudaStreamCreateWithFlags(&m->s_main, cudaStreamNonBlocking));
+  CREATE_CUDA(cudaStreamCreateWithFlags(&m->s_copy, cudaStreamNonBlocking));
+  for (cudaEvent_t* e : {&m->ev_fork, &m->ev_join})
+    CREATE_CUDA(cudaEventCreateWithFlags(e, cudaEventDisableTiming));
+  CREATE_CUDA(cudaEventCreate(&m->ev_t0));
+  CREATE_CUDA(cudaEventCreate(&m->ev_t1));
+  CREATE_CUDA(cudaHostAlloc(reinterpret_cast<void**>(&m->host_state), 64, cudaHostAllocDefault));
+
+  const int H = d.hidden, D = d.head_dim, F = d.ffn;
+  m->q_dim = d.n_heads_q * D;
+  m->kv_dim = d.n_heads_kv * D;
+  m->qkv_dim = m->q_dim + 2 * m->kv_dim;
+  const int n_tree = 1 + d.max_depth * d.max_width;
+  m->rows_max = std::max({n_tree, d.max_prompt, d.max_width});
+  m->logit_rows = std::max(n_tree, d.max_width);
+
+  // cache: committed tokens + one tree region + a page of slack
+  m->capacity = (int64_t)d.max_seq + n_tree + m->page_size;
+  m->n_pages = (int)cdiv(m->capacity, m->page_size);
+  m->capacity = (int64_t)m->n_pages * m->page_size;
+  const size_t kv_elems = (size_t)d.n_layers * m->n_pages * d.n_heads_kv * m->page_size * D;
+  CREATE_TRY(dalloc_t(m, &m->kpool, kv_elems));
+  CREATE_TRY(dalloc_t(m, &m->vpool, kv_elems));
+  CREATE_CUDA(cudaMemset(m->kpool, 0, kv_elems * 2));
+  CREATE_CUDA(cudaMemset(m->vpool, 0, kv_elems * 2));
+  {
+    std::vector<int32_t> pt(m->n_pages);
+    for (int i = 0; i < m->n_pages; ++i) pt[i] = i;
+    CREATE_TRY(dalloc_t(m, &m->page_table, pt.size()));
+    CREATE_CUDA(cudaMemcpy(m->page_table, pt.data(), pt.size() * 4, cudaMemcpyHostToDevice));
+  }
+  // RoPE table in double, stored fp32: angle = pos * theta^(-2i/D)
+  {
+    m->max_pos = (int)m->capacity;
+    std::vector<float2> tab((size_t)m->max_pos * (D / 2));
+    for (int p = 0; p < m->max_pos; ++p)
+      for (int i = 0; i < D / 2; ++i) {
+        const double ang = (double)p * std::pow((double)d.rope_theta, -2.0 * i / D);
+        tab[(size_t)p * (D / 2) + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+      }
+    CREATE_TRY(dalloc_t(m, &m->rope, tab.size()));
+    CREATE_CUDA(cudaMemcpy(m->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice));
+  }
+  const size_t R = m->rows_max;
+  CREATE_TRY(dalloc_t(m, &m->x, R * H));
+  CREATE_TRY(dalloc_t(m, &m->xn, R * H));
+  CREATE_TRY(dalloc_t(m, &m->qkv, R * m->qkv_dim));
+  CREATE_TRY(dalloc_t(m, &m->q, R * m->q_dim));
+  CREATE_TRY(dalloc_t(m, &m->attn, R * m->q_dim));
+  CREATE_TRY(dalloc_t(m, &m->act, R * F));
+  CREATE_TRY(dalloc_t(m, &m->logits, (size_t)m->logit_rows * d.vocab));
+  CREATE_TRY(dalloc_t(m, &m->rows_tok, R));
+  m->attn_part_floats = (size_t)std::max(d.max_width, 8) * d.n_heads_q * (D + 2) * 32;
+  CREATE_TRY(dalloc_t(m, &m->attn_part, m->attn_part_floats));
+
+  // tree (slot 0 = root: parent -1, depth 0, score 0, anc [0, -1...])
+  {
+    const int A = d.max_depth + 1;
+    m->tree.width = d.max_width;
+    m->tree.max_depth = d.max_depth;
+    CREATE_TRY(dalloc_t(m, &m->tree.token, n_tree));
+    CREATE_TRY(dalloc_t(m, &m->tree.parent, n_tree));
+    CREATE_TRY(dalloc_t(m, &m->tree.depth, n_tree));
+    CREATE_TRY(dalloc_t(m, &m->tree.score, n_tree));
+    CREATE_TRY(dalloc_t(m, &m->tree.anc, (size_t)n_tree * A));
+    std::vector<int32_t> anc((size_t)n_tree * A, -1), par(n_tree, -1), dep(n_tree, 0);
+    anc[0] = 0;
+    CREATE_CUDA(cudaMemcpy(m->tree.anc, anc.data(), anc.size() * 4, cudaMemcpyHostToDevice));
+    CREATE_CUDA(cudaMemcpy(m->tree.parent, par.data(), par.size() * 4, cudaMemcpyHostToDevice));
+    CREATE_CUDA(cudaMemcpy(m->tree.depth, dep.data(), dep.size() * 4, cudaMemcpyHostToDevice));
+    CREATE_CUDA(cudaMemset(m->tree.score, 0, n_tree * 4));
+    CREATE_CUDA(cudaMemset(m->tree.token, 0, n_tree * 4));
+  }
+  CREATE_TRY(dalloc_t(m, &m->state, ST_COUNT));
+  CREATE_TRY(dalloc_t(m, &m->accepted, std::max(d.max_depth, 1)));
+  CREATE_TRY(dalloc_t(m, &m->choice, n_tree));
+  CREATE_TRY(dalloc_t(m, &m->hist, d.max_depth + 1));
+  m->out_cap = d.max_seq + d.max_depth + 2;
+  CREATE_TRY(dalloc_t(m, &m->out_tokens, m->out_cap));
+  {
+    const int ec = expand_pick_chunks(d.max_width, d.vocab);
+    const int ac = std::max(accept_pick_chunks(n_tree, d.vocab), accept_pick_chunks(1, d.vocab));
+    m->part_keys = std::max((size_t)d.max_width * 64 * MAX_WIDTH, (size_t)n_tree * 64);
+    (void)ec;
+    (void)ac;
+    m->part_floats = (size_t)d.max_width * 64 * 2;
+    CREATE_TRY(dalloc_t(m, &m->part_key, m->part_keys));
+    CREATE_TRY(dalloc_t(m, &m->part_f, m->part_floats));
+    CREATE_TRY(dalloc_t(m, &m->counters, 4));
+    CREATE_CUDA(cudaMemset(m->counters, 0, 16));
+  }
+
+  // staging ring for the offloaded originals
+  m->n_off = d.n_layers - d.n_resident;
+  if (m->n_off > 0) {
+    const size_t rows[7] = {(size_t)m->q_dim, (size_t)m->kv_dim, (size_t)m->kv_dim, (size_t)H,
+                            (size_t)F, (size_t)F, (size_t)H};
+    const size_t cols[7] = {(size_t)H, (size_t)H, (size_t)H, (size_t)m->q_dim,
+                            (size_t)H, (size_t)H, (size_t)F};
+    size_t off = 0;
+    for (int i = 0; i < 7; ++i) {
+      m->mat_off[i] = off;
+      m->mat_bytes[i] = rows[i] * cols[i] * 2;
+      off += (m->mat_bytes[i] + 255) / 256 * 256;
+    }
+    m->layer_bytes = off;
+    m->ring = d.staging_layers <= 0 ? m->n_off : std::min(d.staging_layers, m->n_off);
+    for (int i = 0; i < m->ring; ++i) {
+      void* p = nullptr;
+      CREATE_TRY(dalloc(m, &p, m->layer_bytes));
+      m->slots.push_back(reinterpret_cast<uint16_t*>(p));
+    }
+    m->ev_staged.resize(m->n_off, nullptr);
+    m->ev_free.resize(m->n_off, nullptr);
+    for (int j = 0; j < m->n_off; ++j) {
+      CREATE_CUDA(cudaEventCreateWithFlags(&m->ev_staged[j], cudaEventDisableTiming));
+      CREATE_CUDA(cudaEventCreateWithFlags(&m->ev_free[j], cudaEventDisableTiming));
+    }
+  }
+  CREATE_CUDA(cudaDeviceSynchronize());
+  *out = m;
+  return SUB_OK;
+#undef CREATE_TRY
+#undef CREATE_CUDA
+}
+
+extern "C" int32_t sub_model_destroy(sub_model* m) {
+  free_model(m);
+  return SUB_OK;
+}
+
+extern "C" int32_t sub_model_memory(const sub_model* m, int64_t* device_bytes) {
+  SUB_CHECK_ARG(m && device_bytes, "null pointer");
+  *device_bytes = m->dev_bytes;
+  return SUB_OK;
+}
+
+extern "C" int32_t sub_model_kv(sub_model* m, sub_kv_cache* out) {
+  SUB_CHECK_ARG(m && out, "null pointer");
+  out->k = m->kpool;
+  out->v = m->vpool;
+  out->page_table = m->page_table;
+  out->n_layers = m->d.n_layers;
+  out->n_heads_kv = m->d.n_heads_kv;
+  out->head_dim = m->d.head_dim;
+  out->page_size = m->page_size;
+  out->n_pages = m->n_pages;
+  out->capacity = m->capacity;
+  return SUB_OK;
+}
+
+// ------------------------------------------------------------ forward (API) --
+extern "C" int32_t sub_model_forward(sub_model* m, int32_t which, const int32_t* tokens,
+                                     int32_t n_rows, int32_t slot0, const int32_t* depth,
+                                     const int32_t* anc, int32_t anc_stride, int64_t n_prefix,
+                                     float* logits, void* stream) {
+  SUB_CHECK_ARG(m && tokens, "null pointer");
+  SUB_CHECK_ARG(which == 0 || which == 1, "which must be 0 (target) or 1 (draft)");
+  SUB_CHECK_ARG(n_rows >= 1 && n_rows <= m->rows_max, "n_rows out of range");
+  SUB_CHECK_ARG(slot0 >= 0 && n_prefix >= 0, "negative slot or prefix");
+  SUB_CHECK_ARG(n_prefix + slot0 + n_rows <= m->capacity, "beyond the cache capacity");
+  SUB_CHECK_ARG(!anc || (depth && anc_stride >= 1), "anc needs depth and anc_stride");
+  SUB_CHECK_ARG(n_prefix + slot0 + n_rows <= m->max_pos, "positions beyond the RoPE table");
+  const cudaStream_t user = as_stream(stream);
+  // order after the caller's stream, run on the model's streams, order back
+  SUB_CUDA_TRY(cudaEventRecord(m->ev_t0, user));
+  SUB_CUDA_TRY(cudaStreamWaitEvent(m->s_main, m->ev_t0, 0));
+  FwdRows r{};
+  r.tokens = tokens;
+  r.n = n_rows;
+  r.slot0 = slot0;
+  r.depth = depth;
+  r.anc = anc;
+  r.anc_stride = anc_stride;
+  r.n_slots = slot0 + n_rows;
+  r.base = n_prefix;
+  r.keys_hint = n_prefix + slot0 + n_rows;
+  const bool target = which == 0;
+  if (target) SUB_TRY(begin_target_pass(m));
+  SUB_TRY(forward(m, !target, r, logits, false));
+  if (target) SUB_TRY(end_target_pass(m));
+  SUB_CUDA_TRY(cudaEventRecord(m->ev_t1, m->s_main));
+  SUB_CUDA_TRY(cudaStreamWaitEvent(user, m->ev_t1, 0));
+  return SUB_OK;
+}
+
+// ----------------------------------------------------------------- generate --
+static int32_t accept_args(sub_model* m, const sub_decode_cfg& c, int n_nodes, AcceptArgs& a) {
+  a = AcceptArgs{};
+  a.logits = m->logits;
+  a.V = m->d.vocab;
+  a.tree = m->tree;
+  a.tree.width = c.width;
+  a.tree.max_depth = m->d.max_depth;
+  a.n_nodes = n_nodes;
+  a.mode = c.mode;
+  a.temp = c.target_temp;
+  a.seed = c.seed;
+  a.root_pos_dev = m->state + ST_N;
+  a.n_chunks = accept_pick_chunks(n_nodes, m->d.vocab);
+  if ((size_t)n_nodes * a.n_chunks > m->part_keys) return fail(SUB_EINVAL, "accept scratch too small");
+  a.part_key = m->part_key;
+  a.counter = m->counters + 1;
+  a.accepted = m->accepted;
+  a.n_accepted = m->state + ST_NACC;
+  a.bonus = m->state + ST_BONUS;
+  a.choice = m->choice;
+  a.out_tokens = m->out_tokens;
+  a.state_emitted = m->state + ST_EMITTED;
+  a.hist = m->hist;
+  return SUB_OK;
+}
+
+// One decode cycle on the compute stream (capturable): draft D levels,
+// verify the tree, accept, compact, advance.
+static int32_t enqueue_cycle(sub_model* m, const sub_decode_cfg& c) {
+  const sub_model_desc& d = m->d;
+  const int k = c.width, D = c.depth;
+  const int n_tree = 1 + D * k;
+  const int A = d.max_depth + 1;
+  sub_tree tr = m->tree;
+  tr.width = k;
+  tr.max_depth = d.max_depth;
+  SUB_TRY(begin_target_pass(m));
+  // ---- draft ----
+  for (int lvl = 0; lvl < D; ++lvl) {
+    const int s0 = lvl == 0 ? 0 : 1 + (lvl - 1) * k;
+    const int M = lvl == 0 ? 1 : k;
+    FwdRows r{};
+    r.tokens = tr.token + s0;
+    r.n = M;
+    r.slot0 = s0;
+    r.depth = tr.depth + s0;
+    r.anc = tr.anc + (size_t)s0 * A;
+    r.anc_stride = A;
+    r.n_slots = s0 + M;
+    r.base_dev = m->state + ST_N;
+    r.keys_hint = d.max_seq;
+    SUB_TRY(forward(m, true, r, m->logits, false));
+    ExpandArgs e{};
+    e.logits = m->logits;
+    e.V = d.vocab;
+    e.temp = c.draft_temp;
+    e.tree = tr;
+    e.level = lvl;
+    e.k_prev = M;
+    e.n_chunks = expand_pick_chunks(M, d.vocab);
+    const size_t parts = (size_t)M * e.n_chunks;
+    if (parts * MAX_WIDTH > m->part_keys || parts * 2 > m->part_floats)
+      return fail(SUB_EINVAL, "expand scratch too small");
+    e.part_key = m->part_key;
+    e.part_max = m->part_f;
+    e.part_sum = m->part_f + parts;
+    e.counter = m->counters;
+    SUB_TRY(launch_expand(e, m->s_main));
+  }
+  // ---- verify ----
+  FwdRows v{};
+  v.tokens = tr.token;
+  v.n = n_tree;
+  v.slot0 = 0;
+  v.depth = tr.depth;
+  v.anc = tr.anc;
+  v.anc_stride = A;
+  v.n_slots = n_tree;
+  v.base_dev = m->state + ST_N;
+  v.keys_hint = d.max_seq;
+  SUB_TRY(forward(m, false, v, m->logits, false));
+  SUB_TRY(end_target_pass(m));
+  // ---- accept, compact, advance ----
+  AcceptArgs a;
+  SUB_TRY(accept_args(m, c, n_tree, a));
+  SUB_TRY(launch_accept(a, m->s_main));
+  CompactArgs cp{};
+  cp.k = m->kpool;
+  cp.v = m->vpool;
+  cp.page_table = m->page_table;
+  cp.n_layers = d.n_layers;
+  cp.n_heads_kv = d.n_heads_kv;
+  cp.head_dim = d.head_dim;
+  cp.page_size = m->page_size;
+  cp.n_pages = m->n_pages;
+  cp.root_pos_dev = m->state + ST_N;
+  cp.accepted = m->accepted;
+  cp.n_accepted = m->state + ST_NACC;
+  cp.max_accept = D;
+  SUB_TRY(launch_compact(cp, m->s_main));
+  advance_kernel<<<1, 1, 0, m->s_main>>>(m->state, tr.token);
+  return check_launch("advance");
+}
+
+static bool same_cfg(const sub_decode_cfg& a, const sub_decode_cfg& b) {
+  return a.depth == b.depth && a.width == b.width && a.draft_temp == b.draft_temp &&
+         a.mode == b.mode && a.target_temp == b.target_temp && a.seed == b.seed;
+}
+
+extern "C" int32_t sub_generate(sub_model* m, const int32_t* prompt_host, int32_t n_prompt,
+                                int32_t n_new, const sub_decode_cfg* cfg, int32_t* out_tokens_host,
+                                sub_stats* stats) {
+  SUB_CHECK_ARG(m && prompt_host && cfg && out_tokens_host, "null pointer");
+  const sub_model_desc& d = m->d;
+  const sub_decode_cfg c = *cfg;
+  SUB_CHECK_ARG(n_prompt >= 1 && n_prompt <= d.max_prompt, "n_prompt out of range");
+  SUB_CHECK_ARG(n_new >= 1 && (int64_t)n_prompt + n_new <= d.max_seq, "n_prompt + n_new > max_seq");
+  SUB_CHECK_ARG(c.depth >= 0 && c.depth <= d.max_depth, "depth beyond the model's max_depth");
+  SUB_CHECK_ARG(c.width >= 1 && c.width <= d.max_width, "width beyond the model's max_width");
+  SUB_CHECK_ARG(c.depth == 0 || c.draft_temp > 0.f, "draft_temp must be positive");
+  SUB_CHECK_ARG(c.mode == 0 || c.mode == 1, "mode must be 0 or 1");
+  SUB_CHECK_ARG(c.mode == 0 || c.target_temp > 0.f, "target_temp must be positive");
+  for (int i = 0; i < n_prompt; ++i)
+    SUB_CHECK_ARG(prompt_host[i] >= 0 && prompt_host[i] < d.vocab, "prompt token out of range");
+  const cudaStream_t st = m->s_main;
+
+  // ---- prefill: chain forward of the prompt, first token from its last row ----
+  SUB_CUDA_TRY(cudaEventRecord(m->ev_t0, st));
+  SUB_CUDA_TRY(cudaMemcpyAsync(m->rows_tok, prompt_host, (size_t)n_prompt * 4,
+                               cudaMemcpyHostToDevice, st));
+  {
+    int32_t init[ST_COUNT] = {0};
+    init[ST_N] = n_prompt - 1;   // the prefill's last row predicts position n_prompt
+    std::memcpy(m->host_state, init, sizeof(init));
+    SUB_CUDA_TRY(cudaMemcpyAsync(m->state, m->host_state, sizeof(init), cudaMemcpyHostToDevice, st));
+    SUB_CUDA_TRY(cudaMemsetAsync(m->hist, 0, (d.max_depth + 1) * 4, st));
+  }
+  FwdRows p{};
+  p.tokens = m->rows_tok;
+  p.n = n_prompt;
+  p.slot0 = 0;
+  p.n_slots = n_prompt;
+  p.base = 0;
+  p.keys_hint = n_prompt;
+  SUB_TRY(begin_target_pass(m));
+  SUB_TRY(forward(m, false, p, m->logits, true));
+  SUB_TRY(end_target_pass(m));
+  {
+    AcceptArgs a;
+    SUB_TRY(accept_args(m, c, 1, a));
+    a.hist = nullptr;
+    SUB_TRY(launch_accept(a, st));
+    advance_kernel<<<1, 1, 0, st>>>(m->state, m->tree.token);
+    SUB_TRY(check_launch("advance"));
+    SUB_CUDA_TRY(cudaMemsetAsync(m->hist, 0, (d.max_depth + 1) * 4, st));
+  }
+  SUB_CUDA_TRY(cudaEventRecord(m->ev_t1, st));
+  SUB_CUDA_TRY(cudaStreamSynchronize(st));
+  float t_prefill = 0.f;
+  SUB_CUDA_TRY(cudaEventElapsedTime(&t_prefill, m->ev_t0, m->ev_t1));
+
+  // ---- decode cycles ----
+  if (c.use_graph && !(m->graph && same_cfg(m->graph_cfg, c))) {
+    if (m->graph) {
+      cudaGraphExecDestroy(m->graph);
+      m->graph = nullptr;
+    }
+    cudaGraph_t g = nullptr;
+    SUB_CUDA_TRY(cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal));
+    const int32_t s = enqueue_cycle(m, c);
+    const cudaError_t e = cudaStreamEndCapture(st, &g);
+    if (s != SUB_OK) {
+      if (g) cudaGraphDestroy(g);
+      return s;
+    }
+    if (e != cudaSuccess) return fail(SUB_ECUDA, std::string("end capture: ") + cudaGetErrorString(e));
+    const cudaError_t ie = cudaGraphInstantiate(&m->graph, g, 0);
+    cudaGraphDestroy(g);
+    if (ie != cudaSuccess) {
+      m->graph = nullptr;
+      return fail(SUB_ECUDA, std::string("graph instantiate: ") + cudaGetErrorString(ie));
+    }
+    m->graph_cfg = c;
+  }
+  SUB_CUDA_TRY(cudaEventRecord(m->ev_t0, st));
+  int64_t cycles = 0;
+  int emitted = 1;
+  while (emitted < n_new) {
+    if (c.use_graph) SUB_CUDA_TRY(cudaGraphLaunch(m->graph, st));
+    else SUB_TRY(enqueue_cycle(m, c));
+    ++cycles;
+    SUB_CUDA_TRY(cudaMemcpyAsync(m->host_state, m->state, ST_COUNT * 4, cudaMemcpyDeviceToHost, st));
+    SUB_CUDA_TRY(cudaStreamSynchronize(st));
+    emitted = m->host_state[ST_EMITTED];
+    if (emitted > m->out_cap) return fail(SUB_ECUDA, "decode state corrupted (emitted overflow)");
+  }
+  SUB_CUDA_TRY(cudaEventRecord(m->ev_t1, st));
+  SUB_CUDA_TRY(cudaMemcpyAsync(out_tokens_host, m->out_tokens, (size_t)n_new * 4,
+                               cudaMemcpyDeviceToHost, st));
+  SUB_CUDA_TRY(cudaStreamSynchronize(st));
+  float t_decode = 0.f;
+  SUB_CUDA_TRY(cudaEventElapsedTime(&t_decode, m->ev_t0, m->ev_t1));
+  if (stats) {
+    std::memset(stats, 0, sizeof(*stats));
+    stats->cycles = cycles;
+    stats->emitted = n_new;
+    stats->tau = cycles ? (double)(emitted - 1) / (double)cycles : 0.0;
+    stats->t_prefill_ms = t_prefill;
+    stats->t_decode_ms = t_decode;
+    std::vector<int32_t> h(d.max_depth + 1);
+    SUB_CUDA_TRY(cudaMemcpy(h.data(), m->hist, h.size() * 4, cudaMemcpyDeviceToHost));
+    for (int i = 0; i <= std::min(d.max_depth, 64); ++i) stats->accept_hist[i] = h[i];
+  }
+  return SUB_OK;
+}
