@@ -1,0 +1,506 @@
+#!/usr/bin/env python
+"""SubSpec decode benchmark on GB300.
+
+One step = one SubSpec decode cycle over the Qwen2.5-7B-shaped decoder:
+48 draft levels (shared resident bf16 layers + int4 substitutes, width 8,
+draft temperature 0.2) -> one target pass verifying all 385 tree nodes (the
+offloaded layers' bf16 originals streamed from pinned host memory on a copy
+stream under the draft) -> greedy accept -> KV compaction.  `value` is the
+generated tokens/s of K device-timed cycles with every input resident;
+`e2e` is sub_generate (host prompt in, host tokens out, prefill included).
+
+Flags: --gpus N (replicas; one process per GPU under torchrun), --steps K,
+--warmup W, --impl reference (the CPU oracle arm), --quick (skip the kernel
+sweep, e2e and the CPU baseline: for profiler launch lists).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import synthetic  # noqa: E402
+
+METRIC = "generated tokens/s and τ (1 GB300); W4 GEMM + tree-attn GB/s vs 8 TB/s"
+CONFIG = "qwen7b"
+DEPTH, WIDTH, DRAFT_T = 48, 8, 0.2
+E2E_NEW = 256
+
+
+# ------------------------------------------------------------------ setup --
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce(world, value, op):
+    if world == 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return dict(hbm=p["hbm_gbs"], bf16=p["bf16_tflops"], bf16_sus=p["bf16_tflops_sustained"],
+                    src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+class Clocks:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.rows = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([c.strip() for c in line.split(",")])
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm = [float(r[1]) for r in self.rows if len(r) >= 9 and r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if len(r) >= 9 and r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in self.rows:
+            if len(r) < 9:
+                continue
+            for i, n in enumerate(names):
+                if r[5 + i].lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_index(local):
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        return int(vis.split(",")[local])
+    return local
+
+
+# ------------------------------------------------------------ workload --
+def layer_bytes_bf16(cfg):
+    return cfg.params_per_layer() * 2
+
+
+def layer_bytes_w4(cfg):
+    h, f = cfg.hidden, cfg.ffn
+    rows_k = [(cfg.q_dim, h), (cfg.kv_dim, h), (cfg.kv_dim, h), (h, cfg.q_dim), (f, h), (f, h),
+              (h, f)]
+    return sum(n * ((k + 63) // 64) * (32 + 4) for n, k in rows_k)
+
+
+def cycle_bound(cfg, pk, tau, n_ctx, link_gbs):
+    """Roofline-derived lower bound on one cycle (ms) and the tokens/s it allows."""
+    lm = cfg.vocab * cfg.hidden * 2
+    kv = cfg.n_layers * n_ctx * cfg.kv_dim * 2 * 2
+    level_bytes = (cfg.n_resident * layer_bytes_bf16(cfg)
+                   + (cfg.n_layers - cfg.n_resident) * layer_bytes_w4(cfg) + lm + kv)
+    t_draft = DEPTH * level_bytes / (pk["hbm"] * 1e9) * 1e3
+    n_tree = 1 + DEPTH * WIDTH
+    flops = 2 * n_tree * (cfg.n_layers * cfg.params_per_layer() + lm // 2)
+    t_verify = flops / (pk["bf16_sus"] * 1e12) * 1e3
+    h2d = (cfg.n_layers - cfg.n_resident) * layer_bytes_bf16(cfg)
+    t_link = h2d / (link_gbs * 1e9) * 1e3 if link_gbs else 0.0
+    t = t_draft + t_verify + max(0.0, t_link - t_draft)
+    return dict(cycle_ms=t, draft_ms=t_draft, verify_ms=t_verify, link_ms=t_link,
+                level_bytes=level_bytes, tokens_per_s=tau / t * 1e3 if t else None)
+
+
+def measure_link(dev):
+    """Pinned host -> device copy bandwidth (GB/s), 1 GiB, best of 3."""
+    n = 1 << 30
+    h = torch.empty(n, dtype=torch.uint8).pin_memory()
+    d = torch.empty(n, dtype=torch.uint8, device=dev)
+    best = 0.0
+    for _ in range(3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        d.copy_(h, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        best = max(best, n / (e0.elapsed_time(e1) / 1e3) / 1e9)
+    del h, d
+    return best
+
+
+def time_launches(fn, iters, stream):
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(iters):
+        fn(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / iters
+
+
+def kernel_measurements(sub, cfg, weights, model, pk, dev, quick):
+    """Dominant-kernel roofline and the kernel sweep (CUDA events on the
+    launching stream; every operand set is larger than L2 or rotated)."""
+    st = torch.cuda.current_stream()
+    out = {}
+    # --- dominant kernel: bf16 GEMV of the resident layers at draft width M=8
+    mats = []
+    for i in range(cfg.n_resident):
+        for n in ("wo", "wg", "wu", "wd"):
+            mats.append(weights["layers"][i][n])
+    x = {m.shape[1]: torch.randn(WIDTH, m.shape[1], device=dev).to(torch.bfloat16) for m in mats}
+    y = {m.shape[0]: torch.empty(WIDTH, m.shape[0], device=dev, dtype=torch.bfloat16) for m in mats}
+    for m in mats[:4]:
+        sub.bf16_gemm(x[m.shape[1]], m, out=y[m.shape[0]])
+    ms = time_launches(lambda i: sub.bf16_gemm(x[mats[i % len(mats)].shape[1]], mats[i % len(mats)],
+                                               out=y[mats[i % len(mats)].shape[0]]),
+                       len(mats) * 3, st)
+    nbytes = sum(m.numel() * 2 + WIDTH * (m.shape[0] + m.shape[1]) * 2 for m in mats) / len(mats)
+    out["gemv_bf16_m8"] = dict(ms_per_launch=ms, bytes_per_launch=nbytes,
+                               gbs=nbytes / (ms / 1e3) / 1e9)
+    # --- int4 GEMV of the substitutes at M=8
+    subs = model.w4_mats
+    if subs:
+        xs = {s[4]: torch.randn(WIDTH, s[4], device=dev).to(torch.bfloat16) for s in subs}
+        ys = {s[3]: torch.empty(WIDTH, s[3], device=dev, dtype=torch.bfloat16) for s in subs}
+
+        def run_w4(i):
+            q, s_, z, n, k = subs[i % len(subs)]
+            sub.w4_gemm(xs[k], q, s_, z, n, k, out=ys[n])
+        ms4 = time_launches(run_w4, len(subs) * 3, st)
+        b4 = sum(q.numel() + s_.numel() * 2 + z.numel() * 2 + WIDTH * (n + k) * 2
+                 for q, s_, z, n, k in subs) / len(subs)
+        out["w4_gemv_m8"] = dict(ms_per_launch=ms4, bytes_per_launch=b4,
+                                 gbs=b4 / (ms4 / 1e3) / 1e9)
+    if quick:
+        return out
+    # --- int4 sweep on Qwen2.5-32B layer shapes
+    shapes = {"qkv": (7168, 5120), "o": (5120, 5120), "gate_up": (55296, 5120),
+              "down": (5120, 27648)}
+    sweep = {}
+    packs = {k: [synthetic.random_w4(n, kk, seed, device=dev) for seed in (1, 2)]
+             for k, (n, kk) in shapes.items()}
+    for mrows in (1, 8, 48, 128, 384):
+        row = {}
+        for name, (n, k) in shapes.items():
+            xx = torch.randn(mrows, k, device=dev).to(torch.bfloat16)
+            yy = torch.empty(mrows, n, device=dev, dtype=torch.bfloat16)
+            pp = packs[name]
+            sub.w4_gemm(xx, *pp[0], n, k, out=yy)
+            msx = time_launches(lambda i: sub.w4_gemm(xx, *pp[i % 2], n, k, out=yy), 20, st)
+            byt = n * ((k + 63) // 64) * 36 + 2 * mrows * (n + k)
+            row[name] = dict(ms=round(msx, 5), gbs=round(byt / (msx / 1e3) / 1e9, 1),
+                             tflops=round(2 * mrows * n * k / (msx / 1e3) / 1e12, 2))
+        sweep[f"M{mrows}"] = row
+    out["w4_sweep_qwen32b"] = sweep
+    # --- tree attention, Qwen2.5-32B heads (40 q / 8 kv, d 128)
+    attn = {}
+    hq, hkv, d = 40, 8, 128
+    tok, par, dep = synthetic.random_tree(DEPTH, WIDTH, 3, 1000)
+    anc = synthetic.ancestors(par, dep, DEPTH).to(dev)
+    depd = dep.to(dev)
+    n_tree = len(par)
+    for lkv in (1024, 4096, 16384):
+        cap = lkv + n_tree + 64
+        kv, keep = sub.make_kv(1, hkv, d, cap, page_size=64)
+        keep[0].normal_()
+        keep[1].normal_()
+        for nq, tag in ((n_tree, "verify385"), (WIDTH, "draft8")):
+            q = torch.randn(nq, hq, d, device=dev).to(torch.bfloat16)
+            a_ = anc[-nq:].contiguous()
+            dd = depd[-nq:].contiguous()
+            sub.tree_attn(q, kv, 0, lkv, lkv, n_tree, anc=a_, depth=dd)
+            msa = time_launches(lambda i: sub.tree_attn(q, kv, 0, lkv, lkv, n_tree, anc=a_,
+                                                        depth=dd), 20, st)
+            byt = (lkv + n_tree) * hkv * d * 2 * 2 + 2 * nq * hq * d * 2
+            fl = 4 * nq * hq * (lkv + DEPTH) * d
+            attn[f"{tag}_kv{lkv}"] = dict(ms=round(msa, 5), gbs=round(byt / (msa / 1e3) / 1e9, 1),
+                                          tflops=round(fl / (msa / 1e3) / 1e12, 2))
+        del kv, keep
+    out["tree_attn_qwen32b_heads"] = attn
+    return out
+
+
+# ------------------------------------------------------------ CPU oracle --
+class LazyLayers:
+    """Oracle-format (float32 NumPy) layer weights, converted on access."""
+
+    def __init__(self, layers, idx):
+        self.layers, self.idx = layers, idx
+
+    def __len__(self):
+        return len(self.idx)
+
+    def __iter__(self):
+        for i in self.idx:
+            yield {k: v.float().cpu().numpy() for k, v in self.layers[i].items()}
+
+
+def oracle_token_sample(cfg, weights, n_layers_sample, n_ctx=None):
+    """Time the oracle's plain target decoding of one token at the prompt's
+    context length (random bf16 KV stands in for the prefix) over a subset of
+    layers; returns (seconds for those layers, seconds for the lm_head)."""
+    import numpy as np
+    from oracle.bf16 import round_bf16
+    from oracle.model import forward_rows
+    n_ctx = cfg.prompt_len if n_ctx is None else n_ctx
+    rng = np.random.default_rng(0)
+    ks = [round_bf16(rng.standard_normal((n_ctx, cfg.n_heads_kv, cfg.head_dim)).astype(np.float32))
+          for _ in range(n_layers_sample)]
+    glob = {"embed": weights["embed"].float().cpu().numpy(),
+            "lm_head": weights["lm_head"].float().cpu().numpy(),
+            "final_norm": weights["final_norm"].float().cpu().numpy()}
+    layers = LazyLayers(weights["layers"], list(range(n_layers_sample)))
+    t0 = time.perf_counter()
+    forward_rows(cfg, glob, layers, [7], [n_ctx], ks, ks, np.ones((1, n_ctx), bool),
+                 np.ones((1, 1), bool))
+    t1 = time.perf_counter()
+    # the lm_head share: one more call with no layers at all
+    forward_rows(cfg, glob, LazyLayers(weights["layers"], []), [7], [n_ctx], [], [],
+                 np.ones((1, 0), bool), np.ones((1, 1), bool))
+    t2 = time.perf_counter()
+    return t1 - t0 - (t2 - t1), t2 - t1
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the CPU oracle, as it stands, on the host cores."""
+    if rank != 0:
+        return
+    cfg = synthetic.CONFIGS[CONFIG]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    weights = synthetic.make_model(cfg, device=dev)
+    n_sample = 2
+    times = []
+    for i in range(args.warmup + args.steps):
+        tl, th = oracle_token_sample(cfg, weights, n_sample)
+        t_tok = tl * cfg.n_layers / n_sample + th
+        if i >= args.warmup:
+            times.append(t_tok)
+    t = statistics.mean(times)
+    value = 1.0 / t
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": workload_name(), "prompt": cfg.prompt_len},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(),
+                         "kind": "oracle",
+                         "sample": f"per step: oracle plain target decoding of one token at "
+                                   f"context {cfg.prompt_len} over {n_sample} of "
+                                   f"{cfg.n_layers} layers, scaled to all layers, plus the "
+                                   f"lm_head"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def workload_name():
+    return ("Qwen2.5-7B-shaped decoder (28 layers, hidden 3584, 28/4 heads, FFN 18944, vocab "
+            "152064), random bf16 init; 11 resident layers + 17 int4 g64 substitutes with "
+            "pinned-host bf16 originals streamed per verify; prompt 512; SubSpec tree depth 48, "
+            "width 8, draft T 0.2, greedy; step = one draft/verify/accept cycle")
+
+
+# ------------------------------------------------------------------ main --
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--quick", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    import substitute_speculative_decoding_gb300 as sub
+
+    assert args.warmup >= 0 and args.steps >= 1
+    cfg = synthetic.CONFIGS[CONFIG]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    pk = peaks()
+    t_setup = time.perf_counter()
+    weights = synthetic.make_model(cfg, device=dev)
+    max_seq = cfg.prompt_len + max(E2E_NEW, (args.warmup + args.steps + 2) * (DEPTH + 1)) + 64
+    model = sub.Model(cfg, weights, max_seq=max_seq, max_depth=DEPTH, max_width=WIDTH,
+                      max_prompt=cfg.prompt_len)
+    # the substitutes' device tensors, for the kernel measurement
+    model.w4_mats = []
+    for i in range(cfg.n_resident, cfg.n_layers):
+        for name in ("wo", "wg", "wu", "wd"):
+            q, s_, z = model.w4[(i, name)]
+            n, k = weights["layers"][i][name].shape
+            model.w4_mats.append((q, s_, z, n, k))
+    # offloaded originals now live pinned on the host; free their device copies
+    for i in range(cfg.n_resident, cfg.n_layers):
+        for name in synthetic.LAYER_TENSORS:
+            weights["layers"][i][name] = weights["layers"][i][name].to("cpu")
+    torch.cuda.empty_cache()
+    t_setup = time.perf_counter() - t_setup
+
+    prompt = synthetic.make_prompt(cfg)
+    dcfg = sub.Model.decode_cfg(DEPTH, WIDTH, DRAFT_T)
+    kernels_per_cycle, h2d_per_cycle = model.cycle_info(dcfg)
+    stream = torch.cuda.current_stream()
+    model.prefill(prompt, dcfg, stream)
+    model.decode_cycles(dcfg, args.warmup, stream)
+    _, e0, c0 = model.decode_read()
+
+    clocks = Clocks(gpu_index(local))
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    model.decode_cycles(dcfg, args.steps, stream)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = ev0.elapsed_time(ev1)
+    clk = clocks.stop()
+    _, e1, c1 = model.decode_read()
+    tokens = e1 - e0
+    tau = tokens / args.steps
+    ms_max = reduce(world, ms, "max")
+    tokens_all = reduce(world, tokens, "sum")
+    value = tokens_all / (ms_max / 1e3)
+
+    link = measure_link(dev)
+    bound = cycle_bound(cfg, pk, tau, cfg.prompt_len + tokens, link)
+    kern = kernel_measurements(sub, cfg, weights, model, pk, dev, args.quick)
+
+    # e2e: the public call with host buffers, prefill included
+    e2e = None
+    if not args.quick:
+        t0 = time.perf_counter()
+        out, st = model.generate(prompt, E2E_NEW, DEPTH, WIDTH, DRAFT_T)
+        t_e2e = time.perf_counter() - t0
+        e2e = {"value": E2E_NEW / t_e2e, "unit": "tokens/s",
+               "h2d_bytes_per_step": int(prompt.numel() * 4 + h2d_per_cycle * (st.cycles + 1)),
+               "d2h_bytes_per_step": int(E2E_NEW * 4 + 32 * st.cycles),
+               "tokens": E2E_NEW, "seconds": t_e2e, "prefill_ms": st.t_prefill_ms,
+               "decode_ms": st.t_decode_ms, "tau": st.tau, "cycles": st.cycles,
+               "note": "h2d counts the prompt and the offloaded originals streamed for the "
+                       "prefill and every verify pass"}
+
+    g = kern["gemv_bf16_m8"]
+    traffic = profile_traffic("gemv_bf16")
+    roof = {"kernel": "gemv_kernel (bf16 weights, M=8: resident layers of the draft)",
+            "bound": "hbm", "achieved": round(g["gbs"], 1), "peak": pk["hbm"],
+            "unit": "GB/s", "frac": round(g["gbs"] / pk["hbm"], 4),
+            "traffic": traffic, "peak_source": pk["src"] + " (burst copy)",
+            "bytes_per_launch": int(g["bytes_per_launch"])}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.quick:
+        n_sample = 4
+        tl, th = oracle_token_sample(cfg, weights, n_sample)
+        t_tok = tl * cfg.n_layers / n_sample + th
+        cpu = {"value": 1.0 / t_tok, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"oracle plain target decoding of one token at context "
+                         f"{cfg.prompt_len} over {n_sample} of {cfg.n_layers} layers (random "
+                         f"bf16 KV prefix), scaled to all layers, plus the lm_head"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": workload_name(), "prompt": cfg.prompt_len, "depth": DEPTH,
+                   "width": WIDTH, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (8.5 GB of weights read per draft level)"},
+        "tau": tau, "tokens_timed": tokens_all,
+        "bound": {k: (round(v, 3) if isinstance(v, float) else v) for k, v in bound.items()},
+        "frac_of_bound": value / world / bound["tokens_per_s"] if bound["tokens_per_s"] else None,
+        "host_link_gbs": round(link, 1),
+        "roofline": roof, "kernels": kern, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": kernels_per_cycle * args.steps, "kernels_per_cycle": kernels_per_cycle,
+        "clocks": clk, "setup_s": round(t_setup, 1),
+        "model_device_bytes": model.device_bytes(),
+    }
+    if rank == 0:
+        print(json.dumps(line))
+    model.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def profile_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, valid only while
+    the kernel's source is unchanged; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    d = json.load(open(path)).get(kernel)
+    if not d:
+        return None
+    src = os.path.join(ROOT, "substitute_speculative_decoding_gb300", "csrc", d["source"])
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return d["dram_bytes_per_launch"] if sha == d["source_sha"] else None
+
+
+if __name__ == "__main__":
+    main()

@@ -242,6 +242,31 @@ typedef struct {
   int64_t accept_hist[65];/* cycles that accepted a tokens, a <= 64 */
 } sub_stats;
 
+/* Step-wise decoding (the pieces sub_generate is made of).
+ * sub_prefill: reset the decode state, run the target over the prompt
+ *   (streaming offloaded layers), and emit the first token.  Enqueued on
+ *   `stream`; nothing is read back.
+ * sub_decode_cycles: enqueue n_cycles draft/verify/accept/compact cycles on
+ *   `stream` without any host synchronisation (as CUDA-graph replays when
+ *   cfg->use_graph; the graph is captured on first use per configuration).
+ *   Emitted tokens accumulate on the device; the caller must keep
+ *   n_prompt + emitted + depth + 1 <= max_seq.
+ * sub_decode_read: synchronise the model's stream, then copy the emitted
+ *   stream (int32 [min(n, emitted)]) to out_host and return the count of
+ *   emitted tokens and of cycles run since the prefill. */
+int32_t sub_prefill(sub_model* model, const int32_t* prompt_host, int32_t n_prompt,
+                    const sub_decode_cfg* cfg, void* stream);
+int32_t sub_decode_cycles(sub_model* model, const sub_decode_cfg* cfg, int32_t n_cycles,
+                          void* stream);
+int32_t sub_decode_read(sub_model* model, int32_t* out_host, int32_t n, int32_t* emitted,
+                        int64_t* cycles);
+
+/* Per-cycle facts of the captured graph for configuration cfg (captures it
+ * if needed): kernels launched per cycle and host->device bytes streamed per
+ * cycle (the offloaded originals). */
+int32_t sub_cycle_info(sub_model* model, const sub_decode_cfg* cfg, int64_t* kernels_per_cycle,
+                       int64_t* h2d_bytes_per_cycle);
+
 /* Generate n_new tokens after prompt_host (int32 [n_prompt], host) into
  * out_tokens_host (int32 [n_new], host): prefill, then draft/verify/accept
  * cycles until n_new tokens are emitted (the first comes from the prefill;

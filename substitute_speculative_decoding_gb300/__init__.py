@@ -106,11 +106,17 @@ _model_forward = _decl("sub_model_forward", [_vp, _i32, _vp, _i32, _i32, _vp, _v
 _model_kv = _decl("sub_model_kv", [_vp, C.POINTER(KVCache)])
 _generate = _decl("sub_generate", [_vp, _vp, _i32, _i32, C.POINTER(DecodeCfg), _vp,
                                    C.POINTER(Stats)])
+_prefill = _decl("sub_prefill", [_vp, _vp, _i32, C.POINTER(DecodeCfg), _vp])
+_decode_cycles = _decl("sub_decode_cycles", [_vp, C.POINTER(DecodeCfg), _i32, _vp])
+_decode_read = _decl("sub_decode_read", [_vp, _vp, _i32, C.POINTER(_i32), C.POINTER(_i64)])
+_cycle_info = _decl("sub_cycle_info", [_vp, C.POINTER(DecodeCfg), C.POINTER(_i64),
+                                       C.POINTER(_i64)])
 
 EXPORTED = ["sub_last_error", "sub_version", "sub_w4_pack", "sub_w4_dequant", "sub_w4_gemm",
             "sub_bf16_gemm", "sub_tree_attn", "sub_draft_expand", "sub_verify_accept",
             "sub_kv_compact", "sub_model_create", "sub_model_destroy", "sub_model_memory",
-            "sub_model_forward", "sub_model_kv", "sub_generate"]
+            "sub_model_forward", "sub_model_kv", "sub_generate", "sub_prefill",
+            "sub_decode_cycles", "sub_decode_read", "sub_cycle_info"]
 
 
 def _check(code):
@@ -252,6 +258,7 @@ class Model:
                  max_prompt: int | None = None, staging_layers: int = 0, device="cuda"):
         self.cfg = cfg
         self.keep = []          # tensors the library points into
+        self.w4 = {}            # (layer, name) -> (q, scale, zero) device substitutes
         dev = torch.device(device)
 
         def dev_t(t):
@@ -273,8 +280,7 @@ class Model:
                 else:
                     wd = w.to(dev).contiguous()
                     q, s, z = w4_pack(wd)
-                    for t in (q, s, z):
-                        self.keep.append(t)
+                    self.w4[(i, name)] = (q, s, z)
                     setattr(L, qn, W4(q.data_ptr(), s.data_ptr(), z.data_ptr()))
                     host = w.to("cpu").contiguous().pin_memory()
                     self.keep.append(host)
@@ -329,6 +335,31 @@ class Model:
                               0 if anc is None else anc.shape[1], n_prefix, _p(logits),
                               _stream(stream)))
         return logits
+
+    @staticmethod
+    def decode_cfg(depth, width, draft_temp=0.2, mode=0, target_temp=1.0, seed=0,
+                   use_graph=True) -> DecodeCfg:
+        return DecodeCfg(depth, width, draft_temp, mode, target_temp, seed, int(use_graph))
+
+    def prefill(self, prompt, cfg: DecodeCfg, stream=None):
+        self._prompt = prompt.to(torch.int32).contiguous()
+        _check(_prefill(self.handle, C.c_void_p(self._prompt.data_ptr()), self._prompt.numel(),
+                        C.byref(cfg), _stream(stream)))
+
+    def decode_cycles(self, cfg: DecodeCfg, n_cycles: int, stream=None):
+        _check(_decode_cycles(self.handle, C.byref(cfg), n_cycles, _stream(stream)))
+
+    def decode_read(self, n: int = 0):
+        """-> (emitted tokens int32 CPU tensor [min(n, emitted)], emitted, cycles)."""
+        out = torch.zeros(max(n, 1), dtype=torch.int32)
+        e, c = _i32(), _i64()
+        _check(_decode_read(self.handle, C.c_void_p(out.data_ptr()), n, C.byref(e), C.byref(c)))
+        return out[:min(n, e.value)], e.value, c.value
+
+    def cycle_info(self, cfg: DecodeCfg):
+        k, b = _i64(), _i64()
+        _check(_cycle_info(self.handle, C.byref(cfg), C.byref(k), C.byref(b)))
+        return k.value, b.value
 
     def generate(self, prompt, n_new: int, depth: int, width: int, draft_temp=0.2, mode=0,
                  target_temp=1.0, seed=0, use_graph=True):

@@ -84,6 +84,13 @@ struct sub_model {
   std::vector<cudaEvent_t> ev_staged, ev_free;
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr, ev_t0 = nullptr, ev_t1 = nullptr;
   int32_t* host_state = nullptr;   // pinned
+  int32_t* host_prompt = nullptr;  // pinned [max_prompt]
+  int32_t* host_out = nullptr;     // pinned [out_cap]
+  cudaEvent_t ev_g0 = nullptr, ev_g1 = nullptr, ev_g2 = nullptr;
+  int n_prompt = 0;
+  int64_t cycles = 0;
+  int64_t max_emit = 0;
+  int64_t graph_kernels = 0;
   // graph of one decode cycle
   cudaGraphExec_t graph = nullptr;
   sub_decode_cfg graph_cfg{};
@@ -121,6 +128,10 @@ static void free_model(sub_model* m) {
   if (m->s_main) cudaStreamDestroy(m->s_main);
   if (m->s_copy) cudaStreamDestroy(m->s_copy);
   if (m->host_state) cudaFreeHost(m->host_state);
+  if (m->host_prompt) cudaFreeHost(m->host_prompt);
+  if (m->host_out) cudaFreeHost(m->host_out);
+  for (cudaEvent_t e : {m->ev_g0, m->ev_g1, m->ev_g2})
+    if (e) cudaEventDestroy(e);
   delete m;
 }
 
@@ -394,8 +405,11 @@ extern "C" int32_t sub_model_create(const sub_model_desc* desc, sub_model** out)
   CREATE_CUDA(cudaStreamCreateWithFlags(&m->s_copy, cudaStreamNonBlocking));
   for (cudaEvent_t* e : {&m->ev_fork, &m->ev_join})
     CREATE_CUDA(cudaEventCreateWithFlags(e, cudaEventDisableTiming));
-  CREATE_CUDA(cudaEventCreate(&m->ev_t0));
-  CREATE_CUDA(cudaEventCreate(&m->ev_t1));
+  CREATE_CUDA(cudaEventCreateWithFlags(&m->ev_t0, cudaEventDisableTiming));
+  CREATE_CUDA(cudaEventCreateWithFlags(&m->ev_t1, cudaEventDisableTiming));
+  CREATE_CUDA(cudaEventCreate(&m->ev_g0));
+  CREATE_CUDA(cudaEventCreate(&m->ev_g1));
+  CREATE_CUDA(cudaEventCreate(&m->ev_g2));
   CREATE_CUDA(cudaHostAlloc(reinterpret_cast<void**>(&m->host_state), 64, cudaHostAllocDefault));
 
   const int H = d.hidden, D = d.head_dim, F = d.ffn;
@@ -469,6 +483,10 @@ extern "C" int32_t sub_model_create(const sub_model_desc* desc, sub_model** out)
   CREATE_TRY(dalloc_t(m, &m->hist, d.max_depth + 1));
   m->out_cap = d.max_seq + d.max_depth + 2;
   CREATE_TRY(dalloc_t(m, &m->out_tokens, m->out_cap));
+  CREATE_CUDA(cudaHostAlloc(reinterpret_cast<void**>(&m->host_prompt), (size_t)d.max_prompt * 4,
+                            cudaHostAllocDefault));
+  CREATE_CUDA(cudaHostAlloc(reinterpret_cast<void**>(&m->host_out), (size_t)m->out_cap * 4,
+                            cudaHostAllocDefault));
   {
     const int ec = expand_pick_chunks(d.max_width, d.vocab);
     const int ac = std::max(accept_pick_chunks(n_tree, d.vocab), accept_pick_chunks(1, d.vocab));
@@ -686,34 +704,84 @@ static bool same_cfg(const sub_decode_cfg& a, const sub_decode_cfg& b) {
          a.mode == b.mode && a.target_temp == b.target_temp && a.seed == b.seed;
 }
 
-extern "C" int32_t sub_generate(sub_model* m, const int32_t* prompt_host, int32_t n_prompt,
-                                int32_t n_new, const sub_decode_cfg* cfg, int32_t* out_tokens_host,
-                                sub_stats* stats) {
-  SUB_CHECK_ARG(m && prompt_host && cfg && out_tokens_host, "null pointer");
+static int32_t check_cfg(const sub_model* m, const sub_decode_cfg& c) {
   const sub_model_desc& d = m->d;
-  const sub_decode_cfg c = *cfg;
-  SUB_CHECK_ARG(n_prompt >= 1 && n_prompt <= d.max_prompt, "n_prompt out of range");
-  SUB_CHECK_ARG(n_new >= 1 && (int64_t)n_prompt + n_new <= d.max_seq, "n_prompt + n_new > max_seq");
   SUB_CHECK_ARG(c.depth >= 0 && c.depth <= d.max_depth, "depth beyond the model's max_depth");
   SUB_CHECK_ARG(c.width >= 1 && c.width <= d.max_width, "width beyond the model's max_width");
   SUB_CHECK_ARG(c.depth == 0 || c.draft_temp > 0.f, "draft_temp must be positive");
   SUB_CHECK_ARG(c.mode == 0 || c.mode == 1, "mode must be 0 or 1");
   SUB_CHECK_ARG(c.mode == 0 || c.target_temp > 0.f, "target_temp must be positive");
+  return SUB_OK;
+}
+
+// Capture one decode cycle for cfg (once per configuration).
+static int32_t ensure_graph(sub_model* m, const sub_decode_cfg& c) {
+  if (m->graph && same_cfg(m->graph_cfg, c)) return SUB_OK;
+  if (m->graph) {
+    cudaGraphExecDestroy(m->graph);
+    m->graph = nullptr;
+  }
+  cudaGraph_t g = nullptr;
+  SUB_CUDA_TRY(cudaStreamBeginCapture(m->s_main, cudaStreamCaptureModeThreadLocal));
+  const int32_t s = enqueue_cycle(m, c);
+  const cudaError_t e = cudaStreamEndCapture(m->s_main, &g);
+  if (s != SUB_OK) {
+    if (g) cudaGraphDestroy(g);
+    return s;
+  }
+  if (e != cudaSuccess) return fail(SUB_ECUDA, std::string("end capture: ") + cudaGetErrorString(e));
+  size_t n_nodes = 0;
+  cudaGraphGetNodes(g, nullptr, &n_nodes);
+  std::vector<cudaGraphNode_t> nodes(n_nodes);
+  int64_t kernels = 0;
+  if (n_nodes) {
+    cudaGraphGetNodes(g, nodes.data(), &n_nodes);
+    for (auto nd : nodes) {
+      cudaGraphNodeType t;
+      if (cudaGraphNodeGetType(nd, &t) == cudaSuccess && t == cudaGraphNodeTypeKernel) ++kernels;
+    }
+  }
+  const cudaError_t ie = cudaGraphInstantiate(&m->graph, g, 0);
+  cudaGraphDestroy(g);
+  if (ie != cudaSuccess) {
+    m->graph = nullptr;
+    return fail(SUB_ECUDA, std::string("graph instantiate: ") + cudaGetErrorString(ie));
+  }
+  m->graph_cfg = c;
+  m->graph_kernels = kernels;
+  return SUB_OK;
+}
+
+// Order the model's compute stream after `user`, and `user` after it.
+static int32_t join_in(sub_model* m, cudaStream_t user) {
+  SUB_CUDA_TRY(cudaEventRecord(m->ev_t0, user));
+  SUB_CUDA_TRY(cudaStreamWaitEvent(m->s_main, m->ev_t0, 0));
+  return SUB_OK;
+}
+static int32_t join_out(sub_model* m, cudaStream_t user) {
+  SUB_CUDA_TRY(cudaEventRecord(m->ev_t1, m->s_main));
+  SUB_CUDA_TRY(cudaStreamWaitEvent(user, m->ev_t1, 0));
+  return SUB_OK;
+}
+
+static int32_t prefill_impl(sub_model* m, const int32_t* prompt_host, int32_t n_prompt,
+                            const sub_decode_cfg& c) {
+  const sub_model_desc& d = m->d;
+  const cudaStream_t st = m->s_main;
+  SUB_CHECK_ARG(n_prompt >= 1 && n_prompt <= d.max_prompt && n_prompt < d.max_seq,
+                "n_prompt out of range");
   for (int i = 0; i < n_prompt; ++i)
     SUB_CHECK_ARG(prompt_host[i] >= 0 && prompt_host[i] < d.vocab, "prompt token out of range");
-  const cudaStream_t st = m->s_main;
-
-  // ---- prefill: chain forward of the prompt, first token from its last row ----
-  SUB_CUDA_TRY(cudaEventRecord(m->ev_t0, st));
-  SUB_CUDA_TRY(cudaMemcpyAsync(m->rows_tok, prompt_host, (size_t)n_prompt * 4,
+  SUB_TRY(check_cfg(m, c));
+  // the prompt goes through pinned staging so the copy is a true async H2D
+  SUB_CUDA_TRY(cudaStreamSynchronize(st));
+  std::memcpy(m->host_prompt, prompt_host, (size_t)n_prompt * 4);
+  SUB_CUDA_TRY(cudaMemcpyAsync(m->rows_tok, m->host_prompt, (size_t)n_prompt * 4,
                                cudaMemcpyHostToDevice, st));
-  {
-    int32_t init[ST_COUNT] = {0};
-    init[ST_N] = n_prompt - 1;   // the prefill's last row predicts position n_prompt
-    std::memcpy(m->host_state, init, sizeof(init));
-    SUB_CUDA_TRY(cudaMemcpyAsync(m->state, m->host_state, sizeof(init), cudaMemcpyHostToDevice, st));
-    SUB_CUDA_TRY(cudaMemsetAsync(m->hist, 0, (d.max_depth + 1) * 4, st));
-  }
+  int32_t init[ST_COUNT] = {0};
+  init[ST_N] = n_prompt - 1;   // the prefill's last row predicts position n_prompt
+  std::memcpy(m->host_state, init, sizeof(init));
+  SUB_CUDA_TRY(cudaMemcpyAsync(m->state, m->host_state, sizeof(init), cudaMemcpyHostToDevice, st));
   FwdRows p{};
   p.tokens = m->rows_tok;
   p.n = n_prompt;
@@ -724,66 +792,123 @@ extern "C" int32_t sub_generate(sub_model* m, const int32_t* prompt_host, int32_
   SUB_TRY(begin_target_pass(m));
   SUB_TRY(forward(m, false, p, m->logits, true));
   SUB_TRY(end_target_pass(m));
-  {
-    AcceptArgs a;
-    SUB_TRY(accept_args(m, c, 1, a));
-    a.hist = nullptr;
-    SUB_TRY(launch_accept(a, st));
-    advance_kernel<<<1, 1, 0, st>>>(m->state, m->tree.token);
-    SUB_TRY(check_launch("advance"));
-    SUB_CUDA_TRY(cudaMemsetAsync(m->hist, 0, (d.max_depth + 1) * 4, st));
-  }
-  SUB_CUDA_TRY(cudaEventRecord(m->ev_t1, st));
-  SUB_CUDA_TRY(cudaStreamSynchronize(st));
-  float t_prefill = 0.f;
-  SUB_CUDA_TRY(cudaEventElapsedTime(&t_prefill, m->ev_t0, m->ev_t1));
+  AcceptArgs a;
+  SUB_TRY(accept_args(m, c, 1, a));
+  a.hist = nullptr;
+  SUB_TRY(launch_accept(a, st));
+  advance_kernel<<<1, 1, 0, st>>>(m->state, m->tree.token);
+  SUB_TRY(check_launch("advance"));
+  SUB_CUDA_TRY(cudaMemsetAsync(m->hist, 0, (d.max_depth + 1) * 4, st));
+  m->n_prompt = n_prompt;
+  m->cycles = 0;
+  m->max_emit = d.max_seq - n_prompt;
+  return SUB_OK;
+}
 
-  // ---- decode cycles ----
-  if (c.use_graph && !(m->graph && same_cfg(m->graph_cfg, c))) {
-    if (m->graph) {
-      cudaGraphExecDestroy(m->graph);
-      m->graph = nullptr;
-    }
-    cudaGraph_t g = nullptr;
-    SUB_CUDA_TRY(cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal));
-    const int32_t s = enqueue_cycle(m, c);
-    const cudaError_t e = cudaStreamEndCapture(st, &g);
-    if (s != SUB_OK) {
-      if (g) cudaGraphDestroy(g);
-      return s;
-    }
-    if (e != cudaSuccess) return fail(SUB_ECUDA, std::string("end capture: ") + cudaGetErrorString(e));
-    const cudaError_t ie = cudaGraphInstantiate(&m->graph, g, 0);
-    cudaGraphDestroy(g);
-    if (ie != cudaSuccess) {
-      m->graph = nullptr;
-      return fail(SUB_ECUDA, std::string("graph instantiate: ") + cudaGetErrorString(ie));
-    }
-    m->graph_cfg = c;
-  }
-  SUB_CUDA_TRY(cudaEventRecord(m->ev_t0, st));
-  int64_t cycles = 0;
-  int emitted = 1;
-  while (emitted < n_new) {
-    if (c.use_graph) SUB_CUDA_TRY(cudaGraphLaunch(m->graph, st));
+static int32_t decode_impl(sub_model* m, const sub_decode_cfg& c, int32_t n_cycles) {
+  SUB_TRY(check_cfg(m, c));
+  SUB_CHECK_ARG(n_cycles >= 0, "n_cycles must be >= 0");
+  SUB_CHECK_ARG(m->n_prompt > 0, "sub_prefill must run first");
+  SUB_CHECK_ARG((int64_t)(m->cycles + n_cycles) * (c.depth + 1) + 1 <= m->max_emit ||
+                    n_cycles <= 1,
+                "n_cycles could overflow max_seq");
+  if (c.use_graph) SUB_TRY(ensure_graph(m, c));
+  for (int i = 0; i < n_cycles; ++i) {
+    if (c.use_graph) SUB_CUDA_TRY(cudaGraphLaunch(m->graph, m->s_main));
     else SUB_TRY(enqueue_cycle(m, c));
-    ++cycles;
-    SUB_CUDA_TRY(cudaMemcpyAsync(m->host_state, m->state, ST_COUNT * 4, cudaMemcpyDeviceToHost, st));
-    SUB_CUDA_TRY(cudaStreamSynchronize(st));
-    emitted = m->host_state[ST_EMITTED];
-    if (emitted > m->out_cap) return fail(SUB_ECUDA, "decode state corrupted (emitted overflow)");
   }
-  SUB_CUDA_TRY(cudaEventRecord(m->ev_t1, st));
-  SUB_CUDA_TRY(cudaMemcpyAsync(out_tokens_host, m->out_tokens, (size_t)n_new * 4,
+  m->cycles += n_cycles;
+  return SUB_OK;
+}
+
+static int32_t read_state(sub_model* m) {
+  SUB_CUDA_TRY(cudaMemcpyAsync(m->host_state, m->state, ST_COUNT * 4, cudaMemcpyDeviceToHost,
+                               m->s_main));
+  SUB_CUDA_TRY(cudaStreamSynchronize(m->s_main));
+  if (m->host_state[ST_EMITTED] > m->out_cap)
+    return fail(SUB_ECUDA, "decode state corrupted (emitted overflow)");
+  return SUB_OK;
+}
+
+extern "C" int32_t sub_prefill(sub_model* m, const int32_t* prompt_host, int32_t n_prompt,
+                               const sub_decode_cfg* cfg, void* stream) {
+  SUB_CHECK_ARG(m && prompt_host && cfg, "null pointer");
+  SUB_TRY(join_in(m, as_stream(stream)));
+  SUB_TRY(prefill_impl(m, prompt_host, n_prompt, *cfg));
+  return join_out(m, as_stream(stream));
+}
+
+extern "C" int32_t sub_decode_cycles(sub_model* m, const sub_decode_cfg* cfg, int32_t n_cycles,
+                                     void* stream) {
+  SUB_CHECK_ARG(m && cfg, "null pointer");
+  SUB_TRY(join_in(m, as_stream(stream)));
+  SUB_TRY(decode_impl(m, *cfg, n_cycles));
+  return join_out(m, as_stream(stream));
+}
+
+extern "C" int32_t sub_decode_read(sub_model* m, int32_t* out_host, int32_t n, int32_t* emitted,
+                                   int64_t* cycles) {
+  SUB_CHECK_ARG(m, "null pointer");
+  SUB_TRY(read_state(m));
+  const int e = m->host_state[ST_EMITTED];
+  if (emitted) *emitted = e;
+  if (cycles) *cycles = m->cycles;
+  if (out_host && n > 0) {
+    const int cnt = std::min(n, e);
+    SUB_CUDA_TRY(cudaMemcpy(out_host, m->out_tokens, (size_t)cnt * 4, cudaMemcpyDeviceToHost));
+  }
+  return SUB_OK;
+}
+
+extern "C" int32_t sub_cycle_info(sub_model* m, const sub_decode_cfg* cfg,
+                                  int64_t* kernels_per_cycle, int64_t* h2d_bytes_per_cycle) {
+  SUB_CHECK_ARG(m && cfg, "null pointer");
+  SUB_TRY(check_cfg(m, *cfg));
+  sub_decode_cfg c = *cfg;
+  c.use_graph = 1;
+  SUB_TRY(ensure_graph(m, c));
+  if (kernels_per_cycle) *kernels_per_cycle = m->graph_kernels;
+  if (h2d_bytes_per_cycle) {
+    int64_t b = 0;
+    for (int i = 0; i < 7; ++i) b += (int64_t)m->mat_bytes[i];
+    *h2d_bytes_per_cycle = b * m->n_off;
+  }
+  return SUB_OK;
+}
+
+extern "C" int32_t sub_generate(sub_model* m, const int32_t* prompt_host, int32_t n_prompt,
+                                int32_t n_new, const sub_decode_cfg* cfg, int32_t* out_tokens_host,
+                                sub_stats* stats) {
+  SUB_CHECK_ARG(m && prompt_host && cfg && out_tokens_host, "null pointer");
+  const sub_model_desc& d = m->d;
+  const sub_decode_cfg c = *cfg;
+  SUB_CHECK_ARG(n_new >= 1 && (int64_t)n_prompt + n_new <= d.max_seq, "n_prompt + n_new > max_seq");
+  const cudaStream_t st = m->s_main;
+  SUB_CUDA_TRY(cudaStreamSynchronize(st));
+  SUB_CUDA_TRY(cudaEventRecord(m->ev_g0, st));
+  SUB_TRY(prefill_impl(m, prompt_host, n_prompt, c));
+  SUB_CUDA_TRY(cudaEventRecord(m->ev_g1, st));
+  if (c.use_graph) SUB_TRY(ensure_graph(m, c));
+  SUB_TRY(read_state(m));
+  int emitted = m->host_state[ST_EMITTED];
+  while (emitted < n_new) {
+    SUB_TRY(decode_impl(m, c, 1));
+    SUB_TRY(read_state(m));
+    emitted = m->host_state[ST_EMITTED];
+  }
+  SUB_CUDA_TRY(cudaEventRecord(m->ev_g2, st));
+  SUB_CUDA_TRY(cudaMemcpyAsync(m->host_out, m->out_tokens, (size_t)n_new * 4,
                                cudaMemcpyDeviceToHost, st));
   SUB_CUDA_TRY(cudaStreamSynchronize(st));
-  float t_decode = 0.f;
-  SUB_CUDA_TRY(cudaEventElapsedTime(&t_decode, m->ev_t0, m->ev_t1));
+  std::memcpy(out_tokens_host, m->host_out, (size_t)n_new * 4);
   if (stats) {
+    float t_prefill = 0.f, t_decode = 0.f;
+    SUB_CUDA_TRY(cudaEventElapsedTime(&t_prefill, m->ev_g0, m->ev_g1));
+    SUB_CUDA_TRY(cudaEventElapsedTime(&t_decode, m->ev_g1, m->ev_g2));
     std::memset(stats, 0, sizeof(*stats));
-    stats->cycles = cycles;
+    stats->cycles = m->cycles;
     stats->emitted = n_new;
-    stats->tau = cycles ? (double)(emitted - 1) / (double)cycles : 0.0;
+    stats->tau = m->cycles ? (double)(emitted - 1) / (double)m->cycles : 0.0;
     stats->t_prefill_ms = t_prefill;
     stats->t_decode_ms = t_decode;
     std::vector<int32_t> h(d.max_depth + 1);
