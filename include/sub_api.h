@@ -112,8 +112,8 @@ typedef struct {
  * anc == NULL means a chain: query i is slot i with path 0..i (a causal block,
  * as in prefill).  n_slots bounds the slot indices (max slot + 1, <= 16384).
  * O [n_q, Hq, d] bf16 = softmax(q K^T * softmax_scale) V, softmax in fp32.
- * Hq % Hkv == 0; head_dim 64 or 128.  Splits over the keys use temporary
- * device memory taken with cudaMallocAsync on `stream`. */
+ * Hq % Hkv == 0; head_dim 64 or 128.  Allocates nothing: key splits merge
+ * inside one thread-block cluster. */
 int32_t sub_tree_attn(const sub_bf16* Q, int32_t n_q, int32_t n_heads_q,
                       const sub_kv_cache* kv, int32_t layer, int64_t n_prefix, int64_t tree_base,
                       int32_t n_slots, const int32_t* anc, int32_t anc_stride,

@@ -1,5 +1,6 @@
 // C ABI entry points for the kernels (the model and generate calls live in
 // model.cu): argument checks, temporary scratch, launch.
+#include <cstdlib>
 #include <mutex>
 #include "attn.cuh"
 #include "gemm.cuh"
@@ -8,6 +9,16 @@
 namespace sub {
 
 static thread_local std::string g_last_error;
+
+bool env_flag(const char* name, bool dflt) {
+  const char* e = getenv(name);
+  if (!e || !e[0]) return dflt;
+  return e[0] != '0';
+}
+bool pdl_enabled() {
+  static const bool on = env_flag("SUB_PDL", true);
+  return on;
+}
 
 void set_error(const std::string& msg) { g_last_error = msg; }
 int32_t fail(int32_t code, const std::string& msg) {
@@ -123,14 +134,6 @@ extern "C" int32_t sub_tree_attn(const sub_bf16* Q, int32_t n_q, int32_t n_heads
                 "Hq must be a multiple of Hkv");
   const cudaStream_t st = as_stream(stream);
   const int splits = attn_pick_splits(a, (int)(n_prefix + n_slots));
-  StreamScratch scratch(st);
-  if (splits > 1) {
-    const size_t rows = (size_t)n_q * n_heads_q;
-    SUB_TRY(scratch.alloc(attn_scratch_floats(a, splits) * sizeof(float)));
-    a.part_o = reinterpret_cast<float*>(scratch.p);
-    a.part_m = a.part_o + (size_t)splits * rows * a.head_dim;
-    a.part_l = a.part_m + (size_t)splits * rows;
-  }
   return launch_tree_attn(a, splits, st);
 }
 

@@ -14,9 +14,11 @@
 // heads that share a KV head read each K/V tile once.  A CTA of four warps
 // owns 64 rows; S = Q K^T and O += P V run on mma.sync m16n8k16 with fp32
 // accumulators and an online softmax in fp32 (FlashAttention-2 style).  Keys
-// may be split over CTAs (grid.z); partial (max, sum, O) are then merged in a
-// fixed order by attn_combine_kernel.
+// may be split over up to 8 CTAs (grid.z) that form one thread-block cluster;
+// their partial (max, sum, O) are merged in split order through distributed
+// shared memory, so no global scratch and no second launch are needed.
 #include <mutex>
+#include <cooperative_groups.h>
 #include "attn.cuh"
 
 namespace sub {
@@ -57,6 +59,7 @@ __global__ void __launch_bounds__(THREADS) tree_attn_kernel(AttnArgs a) {
   uint32_t* sBits = reinterpret_cast<uint32_t*>(sV + 2 * KT * D * 2);
   auto sw = [](int row, int ch) { return row * CH + (ch ^ (row & 7)); };
 
+  pdl_wait();   // Q, K/V and the tree come from earlier kernels
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int kvh = blockIdx.y;
   const int G = a.n_heads_q / a.n_heads_kv;
@@ -252,14 +255,15 @@ __global__ void __launch_bounds__(THREADS) tree_attn_kernel(AttnArgs a) {
     __syncthreads();   // buffer reuse by the next prefetch
   }
 
+  pdl_trigger();
   // ---- write out ----
+  if (gridDim.z == 1) {
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int gr = row0 + wrow + g + 8 * h;
-    if (gr >= n_rows) continue;
-    const int q = gr / G, hh = gr % G;
-    const size_t orow = (size_t)q * a.n_heads_q + kvh * G + hh;   // row of [n_q*Hq]
-    if (gridDim.z == 1) {
+    for (int h = 0; h < 2; ++h) {
+      const int gr = row0 + wrow + g + 8 * h;
+      if (gr >= n_rows) continue;
+      const int q = gr / G, hh = gr % G;
+      const size_t orow = (size_t)q * a.n_heads_q + kvh * G + hh;   // row of [n_q*Hq]
       const float inv = l_run[h] > 0.f ? 1.f / l_run[h] : 0.f;
 #pragma unroll
       for (int i = 0; i < D / 8; ++i) {
@@ -267,50 +271,86 @@ __global__ void __launch_bounds__(THREADS) tree_attn_kernel(AttnArgs a) {
         *reinterpret_cast<uint32_t*>(a.O + orow * D + c) =
             pack_bf16x2(o[i][2 * h] * inv, o[i][2 * h + 1] * inv);
       }
-    } else {
-      const size_t base = ((size_t)blockIdx.z * a.n_q * a.n_heads_q + orow);
-      float* po = a.part_o + base * D;
+    }
+    return;
+  }
+  // Key splits form one thread-block cluster: each CTA parks its partial
+  // (max, sum, unnormalised O) in its own shared memory, and after a cluster
+  // barrier every CTA merges a slice of the rows by reading its peers' shared
+  // memory (distributed shared memory), in split order.
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  constexpr int PLD = D + 4;
+  float* sO = reinterpret_cast<float*>(sK);            // [ROWS][PLD], reuses the K/V tiles
+  float* sM = sO + ROWS * PLD;                          // [ROWS]
+  float* sL = sM + ROWS;                                // [ROWS]
+  float* sW = sL + ROWS;                                // [rows_per][S] merge weights
 #pragma unroll
-      for (int i = 0; i < D / 8; ++i) {
-        const int c = i * 8 + 2 * tig;
-        po[c] = o[i][2 * h];
-        po[c + 1] = o[i][2 * h + 1];
-      }
-      if (tig == 0) {
-        a.part_m[base] = m_run[h];
-        a.part_l[base] = l_run[h];
-      }
+  for (int h = 0; h < 2; ++h) {
+    const int r = wrow + g + 8 * h;
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) {
+      const int c = i * 8 + 2 * tig;
+      sO[r * PLD + c] = o[i][2 * h];
+      sO[r * PLD + c + 1] = o[i][2 * h + 1];
+    }
+    if (tig == 0) {
+      sM[r] = m_run[h];
+      sL[r] = l_run[h];
     }
   }
-}
-
-// Merge split partials in split order: O = sum_s w_s o_s / sum_s w_s l_s,
-// w_s = 2^(m_s - max_s m_s).  One warp per output row.
-template <int D>
-__global__ void attn_combine_kernel(AttnArgs a, int n_split) {
-  const int row = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-  const int lane = threadIdx.x & 31;
-  const int n_out = a.n_q * a.n_heads_q;
-  if (row >= n_out) return;
-  float mx = -INFINITY;
-  for (int s = 0; s < n_split; ++s) mx = fmaxf(mx, a.part_m[(size_t)s * n_out + row]);
-  float den = 0.f;
-  float num[D / 32];
+  cluster.sync();
+  const int S = (int)gridDim.z;
+  const int rank = (int)cluster.block_rank();
+  const int rows_per = (ROWS + S - 1) / S;
+  const int r_lo = rank * rows_per, r_hi = min(ROWS, r_lo + rows_per);
+  for (int i = tid; i < (r_hi - r_lo); i += THREADS) {
+    const int r = r_lo + i;
+    float ms[ATTN_MAX_SPLIT], ls[ATTN_MAX_SPLIT];
 #pragma unroll
-  for (int i = 0; i < D / 32; ++i) num[i] = 0.f;
-  for (int s = 0; s < n_split; ++s) {
-    const float ms = a.part_m[(size_t)s * n_out + row];
-    const float w = (ms == -INFINITY) ? 0.f : exp2f(ms - mx);
-    den += w * a.part_l[(size_t)s * n_out + row];
-    const float* po = a.part_o + ((size_t)s * n_out + row) * D;
+    for (int s2 = 0; s2 < ATTN_MAX_SPLIT; ++s2) {   // all remote loads in flight at once
+      ms[s2] = s2 < S ? cluster.map_shared_rank(sM, s2)[r] : -INFINITY;
+      ls[s2] = s2 < S ? cluster.map_shared_rank(sL, s2)[r] : 0.f;
+    }
+    float mx = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < D / 32; ++i) num[i] += w * po[lane + 32 * i];
+    for (int s2 = 0; s2 < ATTN_MAX_SPLIT; ++s2) mx = fmaxf(mx, ms[s2]);
+    float den = 0.f;
+#pragma unroll
+    for (int s2 = 0; s2 < ATTN_MAX_SPLIT; ++s2) {
+      ms[s2] = (ms[s2] == -INFINITY) ? 0.f : exp2f(ms[s2] - mx);
+      den += ms[s2] * ls[s2];
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+#pragma unroll
+    for (int s2 = 0; s2 < ATTN_MAX_SPLIT; ++s2)
+      if (s2 < S) sW[i * ATTN_MAX_SPLIT + s2] = ms[s2] * inv;
   }
-  const float inv = den > 0.f ? 1.f / den : 0.f;
+  __syncthreads();
+  for (int idx = tid; idx < (r_hi - r_lo) * (D / 2); idx += THREADS) {
+    const int i = idx / (D / 2), c = (idx % (D / 2)) * 2;
+    const int r = r_lo + i;
+    const int gr = row0 + r;
+    if (gr >= n_rows) continue;
+    float2 pv[ATTN_MAX_SPLIT];
 #pragma unroll
-  for (int i = 0; i < D / 32; ++i)
-    reinterpret_cast<__nv_bfloat16*>(a.O)[(size_t)row * D + lane + 32 * i] =
-        __float2bfloat16_rn(num[i] * inv);
+    for (int s2 = 0; s2 < ATTN_MAX_SPLIT; ++s2)
+      pv[s2] = s2 < S ? *reinterpret_cast<const float2*>(cluster.map_shared_rank(sO, s2) + r * PLD + c)
+                      : make_float2(0.f, 0.f);
+    float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+    for (int s2 = 0; s2 < ATTN_MAX_SPLIT; ++s2) {
+      if (s2 < S) {
+        const float w = sW[i * ATTN_MAX_SPLIT + s2];
+        v0 = fmaf(w, pv[s2].x, v0);
+        v1 = fmaf(w, pv[s2].y, v1);
+      }
+    }
+    const int q = gr / G, hh = gr % G;
+    const size_t orow = (size_t)q * a.n_heads_q + kvh * G + hh;
+    *reinterpret_cast<uint32_t*>(a.O + orow * D + c) = pack_bf16x2(v0, v1);
+  }
+  cluster.sync();   // peers may still be reading this CTA's shared memory
 }
 
 int attn_smem_bytes(const AttnArgs& a) {
@@ -320,13 +360,17 @@ int attn_smem_bytes(const AttnArgs& a) {
   const int words = (a.n_slots + 31) / 32;
   return ROWS * d * 2 + 4 * KT * d * 2 + (a.anc ? nq * words * 4 : 0);
 }
+static_assert(ROWS * (128 + 4) * 4 + 2 * ROWS * 4 + ROWS * ATTN_MAX_SPLIT * 4 <= 4 * KT * 128 * 2,
+              "the cluster merge buffers must fit in the K/V tiles (head_dim 128)");
+static_assert(ROWS * (64 + 4) * 4 + 2 * ROWS * 4 + ROWS * ATTN_MAX_SPLIT * 4 <= 4 * KT * 64 * 2,
+              "the cluster merge buffers must fit in the K/V tiles (head_dim 64)");
 
 int attn_pick_splits(const AttnArgs& a, int n_keys_hint) {
   const int G = a.n_heads_q / a.n_heads_kv;
   const int blocks = (a.n_q * G + ROWS - 1) / ROWS * a.n_heads_kv;
   const int tiles = (n_keys_hint + KT - 1) / KT;
   int s = (2 * 152 + blocks - 1) / blocks;
-  s = std::max(1, std::min(s, std::min(tiles, 32)));
+  s = std::max(1, std::min(s, std::min(tiles, ATTN_MAX_SPLIT)));
   return s;
 }
 
@@ -351,25 +395,35 @@ int32_t launch_tree_attn(const AttnArgs& a, int n_split, cudaStream_t st) {
   SUB_CHECK_ARG(a.n_heads_kv >= 1 && a.n_heads_q % a.n_heads_kv == 0, "attn: Hq % Hkv != 0");
   SUB_CHECK_ARG(a.page_size % 16 == 0 && a.page_size > 0, "attn: page_size % 16 != 0");
   SUB_CHECK_ARG(a.n_slots >= 0 && a.n_slots <= 16384, "attn: n_slots out of range");
-  SUB_CHECK_ARG(n_split >= 1 && n_split <= 64, "attn: bad split count");
+  SUB_CHECK_ARG(n_split >= 1 && n_split <= ATTN_MAX_SPLIT, "attn: bad split count");
   if (a.n_q == 0) return SUB_OK;
   const int G = a.n_heads_q / a.n_heads_kv;
   const int smem = attn_smem_bytes(a);
   SUB_CHECK_ARG(smem <= ATTN_MAX_SMEM, "attn: tree too large for the shared-memory bitmap");
   SUB_TRY(attn_init());
-  dim3 grid((a.n_q * G + ROWS - 1) / ROWS, a.n_heads_kv, n_split);
-  if (a.head_dim == 128) tree_attn_kernel<128><<<grid, THREADS, smem, st>>>(a);
-  else tree_attn_kernel<64><<<grid, THREADS, smem, st>>>(a);
-  SUB_TRY(check_launch("tree_attn"));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((a.n_q * G + ROWS - 1) / ROWS, a.n_heads_kv, n_split);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
   if (n_split > 1) {
-    const int rows = a.n_q * a.n_heads_q;
-    const int wpb = 8;
-    if (a.head_dim == 128)
-      attn_combine_kernel<128><<<(rows + wpb - 1) / wpb, wpb * 32, 0, st>>>(a, n_split);
-    else
-      attn_combine_kernel<64><<<(rows + wpb - 1) / wpb, wpb * 32, 0, st>>>(a, n_split);
-    SUB_TRY(check_launch("attn_combine"));
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 1;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = n_split;
+    ++na;
   }
+  if (pdl_enabled()) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  if (a.head_dim == 128) SUB_CUDA_TRY(cudaLaunchKernelEx(&cfg, tree_attn_kernel<128>, a));
+  else SUB_CUDA_TRY(cudaLaunchKernelEx(&cfg, tree_attn_kernel<64>, a));
   return SUB_OK;
 }
 

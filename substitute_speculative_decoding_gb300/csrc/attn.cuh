@@ -25,21 +25,13 @@ struct AttnArgs {
   const int32_t* depth;         // [n_q] path length - 1 (with anc)
   int chain_slot0;              // chain mode: query i is slot chain_slot0 + i
   float scale;
-  // split-K partials (n_split > 1): [n_split, n_q*Hq, D], [n_split, n_q*Hq] x2
-  float* part_o;
-  float* part_m;
-  float* part_l;
 };
 
 constexpr int ATTN_MAX_SMEM = 200 * 1024;
+constexpr int ATTN_MAX_SPLIT = 8;   // key splits = CTAs of one (portable) cluster
 int32_t attn_init();
 int attn_smem_bytes(const AttnArgs& a);
 int attn_pick_splits(const AttnArgs& a, int n_keys_hint);
-// Floats of split scratch needed for n_split splits.
-inline size_t attn_scratch_floats(const AttnArgs& a, int n_split) {
-  const size_t rows = (size_t)a.n_q * a.n_heads_q;
-  return n_split > 1 ? (size_t)n_split * rows * (a.head_dim + 2) : 0;
-}
 int32_t launch_tree_attn(const AttnArgs& a, int n_split, cudaStream_t st);
 
 }  // namespace sub

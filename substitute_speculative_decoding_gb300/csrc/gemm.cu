@@ -53,6 +53,8 @@ template <bool W4, int EPI>
 __global__ void __launch_bounds__(THREADS) gemm_kernel(GemvArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr bool GLU = (EPI == EPI_GLU);
+  pdl_trigger();
+  pdl_wait();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int wm = warp >> 2, wn = warp & 3;
   const int m0 = blockIdx.y * BM;
@@ -301,8 +303,8 @@ static int32_t gemm_launch(const GemvArgs& a, cudaStream_t st) {
   auto kern = gemm_kernel<W4, EPI>;
   const int cols = (EPI == EPI_GLU) ? BN / 2 : BN;
   dim3 grid((a.N + cols - 1) / cols, (a.M + BM - 1) / BM);
-  kern<<<grid, THREADS, SMEM_BYTES, st>>>(a);
-  return check_launch("gemm");
+  SUB_CUDA_TRY(launch_k(kern, grid, dim3(THREADS), SMEM_BYTES, st, a));
+  return SUB_OK;
 }
 
 template <bool W4>

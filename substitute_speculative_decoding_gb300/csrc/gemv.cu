@@ -5,49 +5,96 @@ namespace sub {
 
 __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
 
-template <bool W4, int MT, int RT, int WK, int EPI, int U>
+constexpr int WK = 4;   // warps per CTA, splitting K
+
+// Activations come from the previous kernel, which may still be draining when
+// this one starts (programmatic dependent launch): read them coherently
+// through L2, never through the read-only path.
+__device__ __forceinline__ uint4 ldcg_v4(const uint16_t* p) {
+  uint4 r;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p) : "memory");
+  return r;
+}
+
+// Rows of tile t of this CTA: (segment, local row of fragment row g, local
+// row of fragment row g + 8); the fragment rows are lo + g and hi + g.
+struct TileRows {
+  int seg, lo, hi;
+};
+
+template <int EPI, int RT>
+__device__ __forceinline__ TileRows tile_rows(const GemvArgs& a, int t) {
+  TileRows r;
+  if constexpr (EPI == EPI_GLU) {
+    r.seg = t / RT;
+    r.lo = (blockIdx.x * RT + t % RT) * 16;
+    r.hi = r.lo + 8;
+  } else if constexpr (EPI == EPI_QKV) {
+    const int D = a.qkv.head_dim, per_head = D / 16;
+    const int tq = a.qkv.n_heads_q * per_head, tk = a.qkv.n_heads_kv * per_head;
+    const int vt = blockIdx.x;
+    if (vt < tq + tk) {
+      const int v = vt < tq ? vt : vt - tq;
+      r.seg = vt < tq ? 0 : 1;
+      r.lo = (v / per_head) * D + 8 * (v % per_head);
+      r.hi = r.lo + D / 2;            // RoPE partner rows in the same fragment
+    } else {
+      r.seg = 2;
+      r.lo = (vt - tq - tk) * 16;
+      r.hi = r.lo + 8;
+    }
+  } else {
+    const int vrow = (blockIdx.x * RT + t) * 16;
+    int seg = 0, start = 0;
+#pragma unroll
+    for (int i = 0; i < 3; ++i)
+      if (seg < a.n_seg - 1 && vrow >= a.seg_end[seg]) { start = a.seg_end[seg]; ++seg; }
+    r.seg = seg;
+    r.lo = vrow - start;
+    r.hi = r.lo + 8;
+  }
+  return r;
+}
+
+template <int EPI>
+__device__ __forceinline__ int seg_rows(const GemvArgs& a, int seg) {
+  if constexpr (EPI == EPI_GLU) return a.N;
+  return a.seg_end[seg] - (seg ? a.seg_end[seg - 1] : 0);
+}
+
+template <bool W4, int MT, int RT, int EPI, int U>
 __global__ void __launch_bounds__(WK * 32)
 gemv_kernel(GemvArgs a) {
   constexpr bool GLU = (EPI == EPI_GLU);
   constexpr int NT = GLU ? 2 * RT : RT;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, tig = lane & 3;
-  const int n0 = blockIdx.x * (16 * RT);
   const int K = a.K;
+  const int G = (K + 63) / 64;
 
-  // ---- per-tile row pointers (two rows per lane: g and g+8) ----
+  // ---- per-tile row pointers (two rows per lane: g and g + 8) ----
   const char* rp0[NT];
   const char* rp1[NT];
   const uint16_t* sp0[NT];
   const uint16_t* sp1[NT];
   const uint16_t* zp0[NT];
   const uint16_t* zp1[NT];
-  const int G = (K + 63) / 64;
 #pragma unroll
   for (int t = 0; t < NT; ++t) {
-    const int vrow = n0 + 16 * (t % RT);
-    int seg = GLU ? (t / RT) : 0;
-    int seg_start = 0;
-    if (!GLU) {
-#pragma unroll
-      for (int i = 0; i < 3; ++i)
-        if (seg < a.n_seg - 1 && vrow >= a.seg_end[seg]) { seg_start = a.seg_end[seg]; ++seg; }
-    }
-    const int seg_rows = GLU ? a.N : a.seg_end[seg] - seg_start;
-    int r0 = vrow - (GLU ? 0 : seg_start) + g;
-    int r1 = r0 + 8;
-    r0 = min(r0, seg_rows - 1);
-    r1 = min(r1, seg_rows - 1);
-    if (W4) {
-      const char* base = reinterpret_cast<const char*>(a.W[seg]);
+    const TileRows tr = tile_rows<EPI, RT>(a, t);
+    const int nrows = seg_rows<EPI>(a, tr.seg);
+    const int r0 = min(tr.lo + g, nrows - 1);
+    const int r1 = min(tr.hi + g, nrows - 1);
+    const char* base = reinterpret_cast<const char*>(a.W[tr.seg]);
+    if constexpr (W4) {
       rp0[t] = base + (int64_t)r0 * G * 32 + tig * 8;
       rp1[t] = base + (int64_t)r1 * G * 32 + tig * 8;
-      sp0[t] = a.S[seg] + (int64_t)r0 * G;
-      sp1[t] = a.S[seg] + (int64_t)r1 * G;
-      zp0[t] = a.Z[seg] + (int64_t)r0 * G;
-      zp1[t] = a.Z[seg] + (int64_t)r1 * G;
+      sp0[t] = a.S[tr.seg] + (int64_t)r0 * G;
+      sp1[t] = a.S[tr.seg] + (int64_t)r1 * G;
+      zp0[t] = a.Z[tr.seg] + (int64_t)r0 * G;
+      zp1[t] = a.Z[tr.seg] + (int64_t)r1 * G;
     } else {
-      const char* base = reinterpret_cast<const char*>(a.W[seg]);
       rp0[t] = base + ((int64_t)r0 * K + tig * 8) * 2;
       rp1[t] = base + ((int64_t)r1 * K + tig * 8) * 2;
     }
@@ -72,26 +119,33 @@ gemv_kernel(GemvArgs a) {
   if constexpr (!W4) {
     // ------------------------------------------------ bf16 weights ----
     const int steps = (K + 31) / 32;
-    const int per = (steps + WK - 1) / WK;
+    const int per = ((steps + WK - 1) / WK + U - 1) / U * U;
     const int s_begin = warp * per, s_end = min(steps, s_begin + per);
+    uint4 w0[U][NT], w1[U][NT], xv[U][MT];
+    auto load_w = [&](int u, int s) {
+      const bool ok = s < s_end && s * 32 + tig * 8 < K;   // K % 8 == 0: whole 16-byte chunks
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        w0[u][t] = ok ? ldg_nc_v4(rp0[t] + (int64_t)s * 64) : make_uint4(0, 0, 0, 0);
+        w1[u][t] = ok ? ldg_nc_v4(rp1[t] + (int64_t)s * 64) : make_uint4(0, 0, 0, 0);
+      }
+    };
+    auto load_x = [&](int u, int s) {
+      const int k = s * 32 + tig * 8;
+      const bool ok = s < s_end && k < K;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+        xv[u][mt] = (ok && xok[mt]) ? ldcg_v4(xp[mt] + k)
+                                    : make_uint4(0, 0, 0, 0);
+    };
+#pragma unroll
+    for (int u = 0; u < U; ++u) load_w(u, s_begin + u);   // weights before the wait
+    pdl_wait();
+#pragma unroll
+    for (int u = 0; u < U; ++u) load_x(u, s_begin + u);
     for (int s = s_begin; s < s_end; s += U) {
-      uint4 w0[U][NT], w1[U][NT], xv[U][MT];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int k = (s + u) * 32 + tig * 8;
-        const bool ok = (s + u < s_end) && (k < K);
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          w0[u][t] = ok ? ldg_nc_v4(rp0[t] + (int64_t)(s + u) * 64) : make_uint4(0, 0, 0, 0);
-          w1[u][t] = ok ? ldg_nc_v4(rp1[t] + (int64_t)(s + u) * 64) : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-          xv[u][mt] = (ok && xok[mt]) ? __ldg(reinterpret_cast<const uint4*>(xp[mt] + k))
-                                      : make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u)
 #pragma unroll
         for (int t = 0; t < NT; ++t)
 #pragma unroll
@@ -101,40 +155,69 @@ gemv_kernel(GemvArgs a) {
             mma_bf16_16816(acc[t][mt], A0, xv[u][mt].x, xv[u][mt].y);
             mma_bf16_16816(acc[t][mt], A1, xv[u][mt].z, xv[u][mt].w);
           }
+        load_w(u, s + U + u);
+        load_x(u, s + U + u);
+      }
     }
   } else {
     // ------------------------------------------------ int4 weights ----
-    const int per = (G + WK - 1) / WK;
+    const int per = ((G + WK - 1) / WK + U - 1) / U * U;
     const int g_begin = warp * per, g_end = min(G, g_begin + per);
+    // scales/zeros of U = 4 consecutive groups in one 8-byte load when rows allow
+    const bool sz_vec = (U == 4) && (G % 4 == 0);
     const uint32_t ONES = 0x3f803f80u;
     const uint32_t ONES_A[4] = {ONES, ONES, ONES, ONES};
-    for (int gi0 = g_begin; gi0 < g_end; gi0 += U) {
-      uint2 q0[U][NT], q1[U][NT];
-      uint16_t s0[U][NT], s1[U][NT], z0[U][NT], z1[U][NT];
-      uint4 xa[U][MT], xb[U][MT];
+    uint2 q0[U][NT], q1[U][NT];
+    uint2 sv0[NT], sv1[NT], zv0[NT], zv1[NT];
+    uint16_t ss0[U][NT], ss1[U][NT], zs0[U][NT], zs1[U][NT];
+    uint4 xa[U][MT], xb[U][MT];
+    auto load_q = [&](int u, int gi) {
+      const bool ok = gi < g_end;
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int gi = gi0 + u;
-        const bool ok = gi < g_end;
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          q0[u][t] = ok ? ldg_nc_v2(rp0[t] + (int64_t)gi * 32) : make_uint2(0, 0);
-          q1[u][t] = ok ? ldg_nc_v2(rp1[t] + (int64_t)gi * 32) : make_uint2(0, 0);
-          s0[u][t] = ok ? __ldg(sp0[t] + gi) : 0;
-          s1[u][t] = ok ? __ldg(sp1[t] + gi) : 0;
-          z0[u][t] = ok ? __ldg(zp0[t] + gi) : 0;
-          z1[u][t] = ok ? __ldg(zp1[t] + gi) : 0;
-        }
-        const int k = gi * 64 + tig * 16;
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          xa[u][mt] = (ok && xok[mt] && k < K) ? __ldg(reinterpret_cast<const uint4*>(xp[mt] + k))
-                                               : make_uint4(0, 0, 0, 0);
-          xb[u][mt] = (ok && xok[mt] && k + 8 < K)
-                          ? __ldg(reinterpret_cast<const uint4*>(xp[mt] + k + 8))
-                          : make_uint4(0, 0, 0, 0);
+      for (int t = 0; t < NT; ++t) {
+        q0[u][t] = ok ? ldg_nc_v2(rp0[t] + (int64_t)gi * 32) : make_uint2(0, 0);
+        q1[u][t] = ok ? ldg_nc_v2(rp1[t] + (int64_t)gi * 32) : make_uint2(0, 0);
+        if (!sz_vec) {
+          ss0[u][t] = ok ? __ldg(sp0[t] + gi) : 0;
+          ss1[u][t] = ok ? __ldg(sp1[t] + gi) : 0;
+          zs0[u][t] = ok ? __ldg(zp0[t] + gi) : 0;
+          zs1[u][t] = ok ? __ldg(zp1[t] + gi) : 0;
         }
       }
+    };
+    auto load_sz = [&](int gi0) {   // vector path: groups gi0 .. gi0 + 3 (gi0 % 4 == 0)
+      const bool ok = sz_vec && gi0 < g_end;
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        sv0[t] = ok ? __ldg(reinterpret_cast<const uint2*>(sp0[t] + gi0)) : make_uint2(0, 0);
+        sv1[t] = ok ? __ldg(reinterpret_cast<const uint2*>(sp1[t] + gi0)) : make_uint2(0, 0);
+        zv0[t] = ok ? __ldg(reinterpret_cast<const uint2*>(zp0[t] + gi0)) : make_uint2(0, 0);
+        zv1[t] = ok ? __ldg(reinterpret_cast<const uint2*>(zp1[t] + gi0)) : make_uint2(0, 0);
+      }
+    };
+    auto load_x = [&](int u, int gi) {
+      const bool ok = gi < g_end;
+      const int k = gi * 64 + tig * 16;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        xa[u][mt] = (ok && xok[mt] && k < K) ? ldcg_v4(xp[mt] + k)
+                                             : make_uint4(0, 0, 0, 0);
+        xb[u][mt] = (ok && xok[mt] && k + 8 < K)
+                        ? ldcg_v4(xp[mt] + k + 8)
+                        : make_uint4(0, 0, 0, 0);
+      }
+    };
+#pragma unroll
+    for (int u = 0; u < U; ++u) load_q(u, g_begin + u);    // weights before the wait
+    load_sz(g_begin);
+    pdl_wait();
+#pragma unroll
+    for (int u = 0; u < U; ++u) load_x(u, g_begin + u);
+    for (int gi0 = g_begin; gi0 < g_end; gi0 += U) {
+      uint2 cs0[NT], cs1[NT], cz0[NT], cz1[NT];   // this batch's packed scales/zeros
+#pragma unroll
+      for (int t = 0; t < NT; ++t) { cs0[t] = sv0[t]; cs1[t] = sv1[t]; cz0[t] = zv0[t]; cz1[t] = zv1[t]; }
+      load_sz(gi0 + U);
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         // B fragments: pairs (k, k+4) to match the nibble pairs of one word
@@ -157,14 +240,29 @@ gemv_kernel(GemvArgs a) {
         }
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
-          // nibble pairs (n_i, n_{i+4}) of each word -> bf16x2 (128 + q)
+          // scale and 128 + zero of rows g and g + 8 for group gi0 + u
+          uint32_t a0s, a1s, b0z, b1z;
+          if (sz_vec) {
+            const uint32_t ws0 = u < 2 ? cs0[t].x : cs0[t].y, ws1 = u < 2 ? cs1[t].x : cs1[t].y;
+            const uint32_t wz0 = u < 2 ? cz0[t].x : cz0[t].y, wz1 = u < 2 ? cz1[t].x : cz1[t].y;
+            a0s = (u & 1) ? (ws0 >> 16) : (ws0 & 0xffffu);
+            a1s = (u & 1) ? (ws1 >> 16) : (ws1 & 0xffffu);
+            b0z = (u & 1) ? (wz0 >> 16) : (wz0 & 0xffffu);
+            b1z = (u & 1) ? (wz1 >> 16) : (wz1 & 0xffffu);
+          } else {
+            a0s = ss0[u][t]; a1s = ss1[u][t]; b0z = zs0[u][t]; b1z = zs1[u][t];
+          }
+          const float sr0 = __uint_as_float(a0s << 16), sr1 = __uint_as_float(a1s << 16);
+          const float zr0 = 128.0f + __uint_as_float(b0z << 16);
+          const float zr1 = 128.0f + __uint_as_float(b1z << 16);
+          // nibble pairs (n_i, n_{i+4}) of each word -> bf16x2 (128 + q); mma i
+          // reads word i/2 of each row: pairs (0,4),(1,5) for even i and
+          // (2,6),(3,7) for odd i; the B fragments pair K the same way
           uint32_t A[4][4];
           {
             const uint32_t a0 = q0[u][t].x, a1 = q0[u][t].y;   // row g: words 0, 1
-            const uint32_t c0 = q1[u][t].x, c1 = q1[u][t].y;   // row g+8
+            const uint32_t c0 = q1[u][t].x, c1 = q1[u][t].y;   // row g + 8
             const uint32_t NIB = 0x000f000fu, E = 0x43004300u;
-            // mma i reads word i/2 of each row: nibble pairs (0,4),(1,5) for even
-            // i and (2,6),(3,7) for odd i; the B fragments pair K the same way
             A[0][0] = (a0 & NIB) | E;         A[0][2] = ((a0 >> 4) & NIB) | E;
             A[0][1] = (c0 & NIB) | E;         A[0][3] = ((c0 >> 4) & NIB) | E;
             A[1][0] = ((a0 >> 8) & NIB) | E;  A[1][2] = ((a0 >> 12) & NIB) | E;
@@ -174,9 +272,6 @@ gemv_kernel(GemvArgs a) {
             A[3][0] = ((a1 >> 8) & NIB) | E;  A[3][2] = ((a1 >> 12) & NIB) | E;
             A[3][1] = ((c1 >> 8) & NIB) | E;  A[3][3] = ((c1 >> 12) & NIB) | E;
           }
-          const float sr0 = bf16_bits_to_f32(s0[u][t]), sr1 = bf16_bits_to_f32(s1[u][t]);
-          const float zr0 = 128.0f + bf16_bits_to_f32(z0[u][t]);
-          const float zr1 = 128.0f + bf16_bits_to_f32(z1[u][t]);
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt) {
             float p[4] = {0.f, 0.f, 0.f, 0.f};
@@ -192,12 +287,15 @@ gemv_kernel(GemvArgs a) {
             acc[t][mt][3] = fmaf(sr1, fmaf(-zr1, sx[mt][3], p[3]), acc[t][mt][3]);
           }
         }
+        load_q(u, gi0 + U + u);
+        load_x(u, gi0 + U + u);
       }
     }
   }
 
+  // the next kernel may launch now and stream its weights during this epilogue
+  pdl_trigger();
   // ---- cross-warp reduction in a fixed order, then the epilogue ----
-  static_assert(WK >= 2, "the epilogue reads partial sums through shared memory");
   constexpr int PER_WARP = NT * MT * 4 * 32;
   __shared__ float red[WK * PER_WARP];
 #pragma unroll
@@ -208,6 +306,53 @@ gemv_kernel(GemvArgs a) {
       for (int j = 0; j < 4; ++j)
         red[warp * PER_WARP + ((t * MT + mt) * 4 + j) * 32 + lane] = acc[t][mt][j];
   __syncthreads();
+  auto total = [&](int e) {
+    float v = 0.f;
+#pragma unroll
+    for (int w = 0; w < WK; ++w) v += red[w * PER_WARP + e];
+    return v;
+  };
+
+  if constexpr (EPI == EPI_QKV) {
+    // element e = (mt * 4 + j) * 32 + ln; j in {0,1}: rows g (lo), e + 64: rows g + 8 (hi)
+    const QkvOut& qo = a.qkv;
+    const TileRows tr = tile_rows<EPI, RT>(a, 0);
+    const int D = qo.head_dim, half = D / 2;
+    const int64_t base = qo.base_dev ? (int64_t)*qo.base_dev : qo.base;
+    const size_t head_stride = (size_t)qo.page_size * D;
+    const size_t page_stride = (size_t)qo.n_heads_kv * head_stride;
+    const size_t layer_off = (size_t)qo.layer * qo.n_pages * page_stride;
+    for (int h = threadIdx.x; h < MT * 2 * 32; h += WK * 32) {
+      const int ln = h & 31, j = (h >> 5) & 1, mt = h >> 6;
+      const int e = (mt * 4 + j) * 32 + ln;
+      const float vlo = total(e), vhi = total(e + 64);
+      const int gg = ln >> 2, tg = ln & 3;
+      const int tok = mt * 8 + 2 * tg + j;
+      if (tok >= a.M) continue;
+      const int64_t kvpos = base + qo.slot0 + tok;
+      const size_t slot_off = layer_off + (size_t)qo.page_table[kvpos / qo.page_size] * page_stride +
+                              (size_t)(kvpos % qo.page_size) * D;
+      if (tr.seg < 2) {
+        const int head = tr.lo / D;
+        const int i = tr.lo % D + gg;   // index within the first half
+        const int64_t pos = base + (qo.depth ? qo.depth[tok] : qo.slot0 + tok);
+        const float2 cs = qo.rope[(pos < qo.max_pos ? pos : qo.max_pos - 1) * half + i];
+        const float y1 = vlo * cs.x - vhi * cs.y;
+        const float y2 = vhi * cs.x + vlo * cs.y;
+        uint16_t* dst = tr.seg == 0
+                            ? qo.q_out + ((size_t)tok * qo.n_heads_q + head) * D
+                            : qo.k_cache + slot_off + (size_t)head * head_stride;
+        dst[i] = f32_to_bf16_bits(y1);
+        dst[i + half] = f32_to_bf16_bits(y2);
+      } else {
+        const int rlo = tr.lo + gg, rhi = tr.hi + gg;
+        qo.v_cache[slot_off + (size_t)(rlo / D) * head_stride + rlo % D] = f32_to_bf16_bits(vlo);
+        qo.v_cache[slot_off + (size_t)(rhi / D) * head_stride + rhi % D] = f32_to_bf16_bits(vhi);
+      }
+    }
+    return;
+  }
+
   constexpr int OUT_ELEMS = RT * MT * 4 * 32;
   for (int e = threadIdx.x; e < OUT_ELEMS; e += WK * 32) {
     // e = ((t * MT + mt) * 4 + j) * 32 + ln, t < RT
@@ -215,16 +360,9 @@ gemv_kernel(GemvArgs a) {
     const int j = (e >> 5) & 3;
     const int mt = (e >> 7) % MT;
     const int t = (e >> 7) / MT;
-    float v = 0.f, vu = 0.f;
-#pragma unroll
-    for (int w = 0; w < WK; ++w) v += red[w * PER_WARP + e];
-    if constexpr (GLU) {
-      const int eu = e + RT * MT * 4 * 32;   // same element of the 'up' tile t + RT
-#pragma unroll
-      for (int w = 0; w < WK; ++w) vu += red[w * PER_WARP + eu];
-    }
+    const float v = total(e);
     const int gg = ln >> 2, tg = ln & 3;
-    const int row = n0 + 16 * t + gg + ((j & 2) ? 8 : 0);
+    const int row = (blockIdx.x * RT + t) * 16 + gg + ((j & 2) ? 8 : 0);
     const int tok = mt * 8 + 2 * tg + (j & 1);
     if (row >= a.N || tok >= a.M) continue;
     const int64_t o = (int64_t)tok * a.ldy + row;
@@ -235,30 +373,114 @@ gemv_kernel(GemvArgs a) {
     } else if constexpr (EPI == EPI_RESID) {
       reinterpret_cast<float*>(a.Y)[o] += v;
     } else {
+      const float vu = total(e + RT * MT * 4 * 32);   // same element of the 'up' tile
       reinterpret_cast<__nv_bfloat16*>(a.Y)[o] = __float2bfloat16_rn(silu_f(v) * vu);
     }
   }
+
+  if constexpr (EPI == EPI_RESID) {
+    const NormOut& no = a.norm;
+    if (!no.xn) return;
+    __shared__ float s_r[16];
+    __shared__ unsigned int s_last;
+    float* Y = reinterpret_cast<float*>(a.Y);
+    __syncthreads();   // this CTA's residual rows are written
+    if (warp == 0 && lane < a.M) {
+      float v[16 * RT];
+#pragma unroll
+      for (int r = 0; r < 16 * RT; ++r) {
+        const int row = blockIdx.x * RT * 16 + r;
+        v[r] = row < a.N ? __ldcg(Y + (int64_t)lane * a.ldy + row) : 0.f;
+      }
+      float ss = 0.f;
+#pragma unroll
+      for (int r = 0; r < 16 * RT; ++r) ss = fmaf(v[r], v[r], ss);
+      no.partial[blockIdx.x * 16 + lane] = ss;
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = (atomicAdd(no.counter, 1u) == gridDim.x - 1) ? 1u : 0u;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    // last CTA: r[m] = rsqrt(mean(x^2) + eps) from the partials in CTA order
+    for (int m = warp; m < a.M; m += WK) {
+      float tot = 0.f;
+      for (int b = lane; b < (int)gridDim.x; b += 32) tot += __ldcg(no.partial + b * 16 + m);
+      tot = warp_sum(tot);
+      if (lane == 0) s_r[m] = rsqrtf(tot / (float)a.ldy + no.eps);
+    }
+    __syncthreads();
+    // every thread normalises whole 8-element chunks, 8 chunks in flight at a time
+    const int nc = a.ldy / 8;   // ldy % 8 == 0
+    const int total_chunks = a.M * nc;
+    constexpr int ILP = 8;
+    for (int base = threadIdx.x; base < total_chunks; base += WK * 32 * ILP) {
+      float4 xa[ILP], xb[ILP];
+      uint4 gv[ILP];
+#pragma unroll
+      for (int i = 0; i < ILP; ++i) {
+        const int idx = base + i * WK * 32;
+        if (idx < total_chunks) {
+          const int m = idx / nc, c = (idx % nc) * 8;
+          const float4* src = reinterpret_cast<const float4*>(Y + (int64_t)m * a.ldy + c);
+          xa[i] = __ldcg(src);
+          xb[i] = __ldcg(src + 1);
+          gv[i] = *reinterpret_cast<const uint4*>(no.gain + c);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < ILP; ++i) {
+        const int idx = base + i * WK * 32;
+        if (idx < total_chunks) {
+          const int m = idx / nc, c = (idx % nc) * 8;
+          const float r = s_r[m];
+          uint4 o;
+          o.x = pack_bf16x2(xa[i].x * r * bf16lo(gv[i].x), xa[i].y * r * bf16hi(gv[i].x));
+          o.y = pack_bf16x2(xa[i].z * r * bf16lo(gv[i].y), xa[i].w * r * bf16hi(gv[i].y));
+          o.z = pack_bf16x2(xb[i].x * r * bf16lo(gv[i].z), xb[i].y * r * bf16hi(gv[i].z));
+          o.w = pack_bf16x2(xb[i].z * r * bf16lo(gv[i].w), xb[i].w * r * bf16hi(gv[i].w));
+          *reinterpret_cast<uint4*>(no.xn + (int64_t)m * a.ldy + c) = o;
+        }
+      }
+    }
+    if (threadIdx.x == 0) *no.counter = 0u;
+  }
 }
 
-template <bool W4, int MT, int RT, int WK, int EPI>
-static int32_t launch_cfg(const GemvArgs& a, cudaStream_t st) {
-  constexpr int U = W4 ? 4 : 4;
-  const int blocks = (a.N + 16 * RT - 1) / (16 * RT);
-  gemv_kernel<W4, MT, RT, WK, EPI, U><<<blocks, WK * 32, 0, st>>>(a);
-  return check_launch("gemv");
-}
-
-template <bool W4, int MT, int EPI>
-static int32_t launch_rt(const GemvArgs& a, cudaStream_t st) {
-  // Segments must not straddle a CTA's rows: two row tiles per CTA when every
-  // segment is a multiple of 32 rows and the grid stays wide enough.
-  bool rt2 = (EPI != EPI_GLU) && a.N >= 32 * 152;
+// ------------------------------------------------------------------ launch --
+static int pick_rt(const GemvArgs& a, int epi) {
+  if (epi == EPI_GLU || epi == EPI_QKV) return 1;
+  bool rt2 = a.N >= 32 * 152;
   for (int i = 0; i < a.n_seg; ++i) {
     const int start = i ? a.seg_end[i - 1] : 0;
     if ((a.seg_end[i] - start) % 32) rt2 = false;
   }
-  if (rt2) return launch_cfg<W4, MT, 2, 4, EPI>(a, st);
-  return launch_cfg<W4, MT, 1, 4, EPI>(a, st);
+  return rt2 ? 2 : 1;
+}
+
+int gemv_grid(const GemvArgs& a, int epi) {
+  if (epi == EPI_QKV) return a.N / 16;
+  const int rt = pick_rt(a, epi);
+  return (a.N + 16 * rt - 1) / (16 * rt);
+}
+
+template <bool W4, int MT, int RT, int EPI>
+static int32_t launch_cfg(const GemvArgs& a, cudaStream_t st) {
+  constexpr int U = 4;
+  SUB_CUDA_TRY(launch_k(gemv_kernel<W4, MT, RT, EPI, U>, dim3(gemv_grid(a, EPI)), dim3(WK * 32), 0,
+                        st, a));
+  return SUB_OK;
+}
+
+template <bool W4, int MT, int EPI>
+static int32_t launch_rt(const GemvArgs& a, cudaStream_t st) {
+  if constexpr (EPI == EPI_GLU || EPI == EPI_QKV) {
+    return launch_cfg<W4, MT, 1, EPI>(a, st);
+  } else {
+    if (pick_rt(a, EPI) == 2) return launch_cfg<W4, MT, 2, EPI>(a, st);
+    return launch_cfg<W4, MT, 1, EPI>(a, st);
+  }
 }
 
 template <bool W4, int EPI>
@@ -274,6 +496,7 @@ static int32_t launch_epi(const GemvArgs& a, int epi, cudaStream_t st) {
     case EPI_F32: return launch_mt<W4, EPI_F32>(a, st);
     case EPI_RESID: return launch_mt<W4, EPI_RESID>(a, st);
     case EPI_GLU: return launch_mt<W4, EPI_GLU>(a, st);
+    case EPI_QKV: return launch_mt<W4, EPI_QKV>(a, st);
   }
   return fail(SUB_EINVAL, "bad gemv epilogue");
 }
@@ -287,6 +510,20 @@ int32_t launch_gemv(const GemvArgs& a, bool is_w4, int epi, cudaStream_t st) {
       const int start = i ? a.seg_end[i - 1] : 0;
       SUB_CHECK_ARG((a.seg_end[i] - start) % 16 == 0, "gemv: segments must be multiples of 16 rows");
     }
+  if (epi == EPI_QKV) {
+    const QkvOut& q = a.qkv;
+    SUB_CHECK_ARG(a.n_seg == 3 && q.head_dim % 16 == 0 && q.head_dim >= 16, "gemv: bad q/k/v layout");
+    SUB_CHECK_ARG(a.seg_end[0] == q.n_heads_q * q.head_dim &&
+                      a.seg_end[1] == (q.n_heads_q + q.n_heads_kv) * q.head_dim &&
+                      a.seg_end[2] == (q.n_heads_q + 2 * q.n_heads_kv) * q.head_dim &&
+                      a.N == a.seg_end[2],
+                  "gemv: q/k/v segment sizes");
+  }
+  if (epi == EPI_RESID && a.norm.xn)
+    SUB_CHECK_ARG(a.norm.partial && a.norm.counter && a.norm.gain && a.ldy == a.N &&
+                      a.N % 8 == 0 && aligned16(a.norm.gain) && aligned16(a.norm.xn) &&
+                      aligned16(a.Y),
+                  "gemv: norm epilogue needs partial, counter, gain and ldy == N");
   return is_w4 ? launch_epi<true>(a, epi, st) : launch_epi<false>(a, epi, st);
 }
 

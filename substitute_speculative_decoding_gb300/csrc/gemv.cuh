@@ -5,7 +5,11 @@
 // every weight byte is read exactly once, at full 128-bit (bf16) or 64-bit
 // (int4) width, straight from HBM into registers.  The order of the K index
 // inside one mma is free as long as A and B agree, so each lane loads its own
-// contiguous run of K and the B fragment is built from the same run.
+// contiguous run of K and the B fragment is built from the same run.  Each
+// warp keeps U steps of weights in flight (a rolling register prefetch), and
+// the first U steps are requested before the kernel waits on its predecessor
+// (programmatic dependent launch), so weight streaming overlaps the previous
+// kernel's tail.
 //
 // Int4 tiles compute, per 64-group, P = X . (128 + q) with q turned into the
 // bf16 value 128+q by one bit-or (0x4300 | q), the group sum Sx = X . 1 by one
@@ -13,9 +17,13 @@
 // Y += s * (P - (128 + z) * Sx).  This is (q - z) * s without rounding the
 // dequantised weight to bf16 first.
 //
-// A CTA owns NT row tiles (16 rows each) over the whole K; its WK warps split
+// A CTA owns RT row tiles (16 rows each) over the whole K; its 4 warps split
 // K and their partial sums meet in shared memory in a fixed order, so results
-// are deterministic and no global scratch is needed.
+// are deterministic.  Epilogues: bf16 or fp32 store, fp32 residual add (which
+// can also produce the next RMSNorm's bf16 input: per-CTA sums of squares,
+// then the last CTA to finish normalises all M rows), SiLU(gate)*up, and the
+// q/k/v epilogue (RoPE on q and k from rows paired i / i + d/2 inside one tile,
+// bf16 q out, k and v written into the paged KV cache).
 #pragma once
 #include "common.cuh"
 
@@ -24,8 +32,35 @@ namespace sub {
 enum GemvEpi : int {
   EPI_BF16 = 0,    // Y bf16 [M, ldy]
   EPI_F32 = 1,     // Y fp32 [M, ldy]
-  EPI_RESID = 2,   // R fp32 [M, ldy] += acc
+  EPI_RESID = 2,   // Y fp32 [M, ldy] += acc (optionally + next RMSNorm, see NormOut)
   EPI_GLU = 3,     // Y bf16 [M, ldy] = silu(gate) * up; segments 0 (gate) and 1 (up)
+  EPI_QKV = 4,     // segments q, k, v -> RoPE, bf16 q, K/V into the cache (QkvOut)
+};
+
+// Residual epilogue extension: xn[m, :] = bf16(Y[m, :] * rsqrt(mean(Y[m]^2) + eps) * gain)
+struct NormOut {
+  uint16_t* xn;              // [M, ldy] bf16, or null for a plain residual add
+  const uint16_t* gain;      // [ldy]
+  float eps;
+  float* partial;            // [gridDim.x * 16] per-CTA sums of squares
+  unsigned int* counter;     // zero before launch; the last CTA resets it
+};
+
+// q/k/v epilogue: rows are q (Hq*D), k (Hkv*D), v (Hkv*D); token m sits at
+// position base + depth[m] and its K/V go to cache position base + slot0 + m.
+struct QkvOut {
+  int n_heads_q, n_heads_kv, head_dim;
+  const float2* rope;        // [max_pos, D/2] (cos, sin)
+  int max_pos;
+  const int32_t* depth;      // [M] or null (chain: slot0 + m)
+  int slot0;
+  int64_t base;
+  const int32_t* base_dev;   // overrides base when non-null
+  uint16_t* q_out;           // [M, Hq, D]
+  uint16_t* k_cache;
+  uint16_t* v_cache;
+  const int32_t* page_table;
+  int page_size, n_pages, layer;
 };
 
 struct GemvArgs {
@@ -40,9 +75,13 @@ struct GemvArgs {
   int N;                 // rows covered by the grid (for GLU: rows of one segment)
   void* Y;               // output (bf16 or fp32)
   int ldy;
+  NormOut norm;          // EPI_RESID only
+  QkvOut qkv;            // EPI_QKV only
 };
 
 // Launch: int4 (is_w4) or bf16 weights, epilogue, M <= 16.
 int32_t launch_gemv(const GemvArgs& a, bool is_w4, int epi, cudaStream_t stream);
+// CTAs a launch will use (the size of NormOut::partial is 16 floats per CTA).
+int gemv_grid(const GemvArgs& a, int epi);
 
 }  // namespace sub

@@ -11,26 +11,48 @@ __device__ __forceinline__ int64_t row_base(const RowSet& rs) {
   return rs.base_dev ? (int64_t)*rs.base_dev : rs.base;
 }
 
+// x[r] = embed[token[r]] (fp32 residual) and xn[r] = bf16(RMSNorm(x[r]) * gain),
+// the first layer's matmul input; one CTA per row.
 __global__ void embed_kernel(const uint16_t* __restrict__ embed, int hidden, RowSet rs,
-                             float* __restrict__ x) {
+                             float* __restrict__ x, const uint16_t* __restrict__ gain, float eps,
+                             uint16_t* __restrict__ xn) {
+  __shared__ float s_part[32];
+  pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x;
   const int64_t tok = rs.tokens[r];
   const uint16_t* src = embed + tok * hidden;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < hidden; i += blockDim.x) {
+    const float v = bf16_bits_to_f32(src[i]);
+    x[(int64_t)r * hidden + i] = v;
+    ss = fmaf(v, v, ss);
+  }
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) s_part[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += s_part[w];
+  const float inv = rsqrtf(tot / (float)hidden + eps);
   for (int i = threadIdx.x; i < hidden; i += blockDim.x)
-    x[(int64_t)r * hidden + i] = bf16_bits_to_f32(src[i]);
+    reinterpret_cast<__nv_bfloat16*>(xn)[(int64_t)r * hidden + i] =
+        __float2bfloat16_rn(bf16_bits_to_f32(src[i]) * inv * bf16_bits_to_f32(gain[i]));
 }
 
 int32_t launch_embed(const uint16_t* embed, int hidden, const RowSet& rs, int rows, float* x,
-                     cudaStream_t st) {
+                     const uint16_t* gain, float eps, uint16_t* xn, cudaStream_t st) {
   if (rows <= 0) return SUB_OK;
-  embed_kernel<<<rows, 256, 0, st>>>(embed, hidden, rs, x);
-  return check_launch("embed");
+  SUB_CUDA_TRY(launch_k(embed_kernel, dim3(rows), dim3(256), 0, st, embed, hidden, rs, x, gain,
+                        eps, xn));
+  return SUB_OK;
 }
 
 // y = bf16(x * rsqrt(mean(x^2) + eps) * gain); one CTA per row, fixed-order sum.
 __global__ void rmsnorm_kernel(const float* __restrict__ x, const uint16_t* __restrict__ gain,
                                int hidden, float eps, uint16_t* __restrict__ out) {
   __shared__ float s_part[32];
+  pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x;
   const float* xr = x + (int64_t)r * hidden;
   float ss = 0.f;
@@ -49,13 +71,15 @@ __global__ void rmsnorm_kernel(const float* __restrict__ x, const uint16_t* __re
 int32_t launch_rmsnorm(const float* x, const uint16_t* gain, int rows, int hidden, float eps,
                        uint16_t* out, cudaStream_t st) {
   if (rows <= 0) return SUB_OK;
-  rmsnorm_kernel<<<rows, 256, 0, st>>>(x, gain, hidden, eps, out);
-  return check_launch("rmsnorm");
+  SUB_CUDA_TRY(launch_k(rmsnorm_kernel, dim3(rows), dim3(256), 0, st, x, gain, hidden, eps, out));
+  return SUB_OK;
 }
 
 // One CTA per row: q heads get RoPE -> bf16 q_out; k heads RoPE -> cache;
 // v heads -> cache.  Rotate-half pairing: element i with i + D/2.
 __global__ void qkv_post_kernel(QkvPostArgs a) {
+  pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x;
   const int D = a.head_dim, half = D / 2;
   const int nh = a.n_heads_q + 2 * a.n_heads_kv;
@@ -95,8 +119,8 @@ __global__ void qkv_post_kernel(QkvPostArgs a) {
 
 int32_t launch_qkv_post(const QkvPostArgs& a, cudaStream_t st) {
   if (a.rows <= 0) return SUB_OK;
-  qkv_post_kernel<<<a.rows, 256, 0, st>>>(a);
-  return check_launch("qkv_post");
+  SUB_CUDA_TRY(launch_k(qkv_post_kernel, dim3(a.rows), dim3(256), 0, st, a));
+  return SUB_OK;
 }
 
 }  // namespace sub

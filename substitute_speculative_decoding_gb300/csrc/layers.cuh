@@ -17,7 +17,7 @@ struct RowSet {
 };
 
 int32_t launch_embed(const uint16_t* embed, int hidden, const RowSet& rs, int rows, float* x,
-                     cudaStream_t st);
+                     const uint16_t* gain, float eps, uint16_t* xn, cudaStream_t st);
 int32_t launch_rmsnorm(const float* x, const uint16_t* gain, int rows, int hidden, float eps,
                        uint16_t* out, cudaStream_t st);
 

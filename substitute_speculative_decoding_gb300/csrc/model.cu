@@ -60,8 +60,9 @@ struct sub_model {
   uint16_t* act = nullptr;   // [rows, F]
   float* logits = nullptr;   // [logit_rows, V]
   int32_t* rows_tok = nullptr;  // [rows] token ids staged for a forward
-  float* attn_part = nullptr;
-  size_t attn_part_floats = 0;
+  float* norm_partial = nullptr;     // [norm_parts] per-CTA sums of squares
+  int norm_parts = 0;
+  unsigned int* norm_counters = nullptr;
   // tree + decode state
   sub_tree tree{};
   int32_t* state = nullptr;
@@ -232,13 +233,22 @@ static int32_t forward(sub_model* m, bool draft, const FwdRows& r, float* logits
   const cudaStream_t st = m->s_main;
   const int H = d.hidden, F = d.ffn, D = d.head_dim;
   const int M = r.n;
+  // Draft-shaped passes (M <= 16) run the GEMV kernels with fused epilogues:
+  // RoPE + KV store after q/k/v, the next RMSNorm after each residual add.
+  // Tree-shaped passes run the tiled GEMM with separate row kernels.
+  const bool fused = M <= 16;
+  // SUB_FUSE_NORM=0 runs the RMSNorms as their own kernels on this path too
+  static const bool fuse_norm_env = env_flag("SUB_FUSE_NORM", true);
+  static const bool fuse_qkv_env = env_flag("SUB_FUSE_QKV", true);
+  const bool fuse_norm = fused && fuse_norm_env;
+  const bool fuse_qkv = fused && fuse_qkv_env;
   RowSet rs{};
   rs.tokens = r.tokens;
   rs.depth = r.depth;
   rs.slot0 = r.slot0;
   rs.base = r.base;
   rs.base_dev = r.base_dev;
-  SUB_TRY(launch_embed(d.embed, H, rs, M, m->x, st));
+  SUB_TRY(launch_embed(d.embed, H, rs, M, m->x, m->layers[0].attn_norm, d.rms_eps, m->xn, st));
 
   AttnArgs at{};
   at.Q = m->q;
@@ -262,14 +272,7 @@ static int32_t forward(sub_model* m, bool draft, const FwdRows& r, float* logits
   at.depth = r.depth;
   at.chain_slot0 = r.slot0;
   at.scale = 1.0f / sqrtf((float)D);
-  int splits = attn_pick_splits(at, (int)std::min<int64_t>(r.keys_hint, 1 << 30));
-  while (splits > 1 && attn_scratch_floats(at, splits) > m->attn_part_floats) --splits;
-  if (splits > 1) {
-    const size_t rows = (size_t)M * d.n_heads_q;
-    at.part_o = m->attn_part;
-    at.part_m = at.part_o + (size_t)splits * rows * D;
-    at.part_l = at.part_m + (size_t)splits * rows;
-  }
+  const int splits = attn_pick_splits(at, (int)std::min<int64_t>(r.keys_hint, 1 << 30));
 
   QkvPostArgs qp{};
   qp.qkv = m->qkv;
@@ -287,6 +290,33 @@ static int32_t forward(sub_model* m, bool draft, const FwdRows& r, float* logits
   qp.page_size = m->page_size;
   qp.n_pages = m->n_pages;
 
+  QkvOut qo{};
+  qo.n_heads_q = d.n_heads_q;
+  qo.n_heads_kv = d.n_heads_kv;
+  qo.head_dim = D;
+  qo.rope = m->rope;
+  qo.max_pos = m->max_pos;
+  qo.depth = r.depth;
+  qo.slot0 = r.slot0;
+  qo.base = r.base;
+  qo.base_dev = r.base_dev;
+  qo.q_out = m->q;
+  qo.k_cache = m->kpool;
+  qo.v_cache = m->vpool;
+  qo.page_table = m->page_table;
+  qo.page_size = m->page_size;
+  qo.n_pages = m->n_pages;
+
+  auto norm_out = [&](const uint16_t* gain, int which) {
+    NormOut no{};
+    no.xn = m->xn;
+    no.gain = gain;
+    no.eps = d.rms_eps;
+    no.partial = m->norm_partial;
+    no.counter = m->norm_counters + which;
+    return no;
+  };
+
   const int qkv_rows[3] = {m->q_dim, m->kv_dim, m->kv_dim};
   const int qkv_idx[3] = {0, 1, 2};
   const int o_rows[1] = {H};
@@ -302,23 +332,47 @@ static int32_t forward(sub_model* m, bool draft, const FwdRows& r, float* logits
     const int j = l - d.n_resident;
     if (off && !draft) SUB_CUDA_TRY(cudaStreamWaitEvent(st, m->ev_staged[j], 0));
     const Matrices W = layer_mats(m, l, draft);
+    const uint16_t* next_gain = l + 1 < d.n_layers ? m->layers[l + 1].attn_norm : d.final_norm;
 
-    SUB_TRY(launch_rmsnorm(m->x, L.attn_norm, M, H, d.rms_eps, m->xn, st));
-    SUB_TRY(launch_matmul(mm_args(m->xn, M, H, W, qkv_idx, 3, qkv_rows, m->qkv, m->qkv_dim), w4,
-                          EPI_F32, st));
-    qp.layer = l;
-    SUB_TRY(launch_qkv_post(qp, st));
+    if (fuse_qkv) {
+      if (!fuse_norm && l > 0) SUB_TRY(launch_rmsnorm(m->x, L.attn_norm, M, H, d.rms_eps, m->xn, st));
+      GemvArgs qa = mm_args(m->xn, M, H, W, qkv_idx, 3, qkv_rows, nullptr, 0);
+      qo.layer = l;
+      qa.qkv = qo;
+      SUB_TRY(launch_gemv(qa, w4, EPI_QKV, st));
+    } else {
+      if (l > 0 && !fuse_norm) SUB_TRY(launch_rmsnorm(m->x, L.attn_norm, M, H, d.rms_eps, m->xn, st));
+      SUB_TRY(launch_matmul(mm_args(m->xn, M, H, W, qkv_idx, 3, qkv_rows, m->qkv, m->qkv_dim), w4,
+                            EPI_F32, st));
+      qp.layer = l;
+      SUB_TRY(launch_qkv_post(qp, st));
+    }
     at.layer = l;
     SUB_TRY(launch_tree_attn(at, splits, st));
-    SUB_TRY(launch_matmul(mm_args(m->attn, M, m->q_dim, W, o_idx, 1, o_rows, m->x, H), w4,
-                          EPI_RESID, st));
-    SUB_TRY(launch_rmsnorm(m->x, L.ffn_norm, M, H, d.rms_eps, m->xn, st));
+    {
+      GemvArgs oa = mm_args(m->attn, M, m->q_dim, W, o_idx, 1, o_rows, m->x, H);
+      if (fuse_norm) {
+        oa.norm = norm_out(L.ffn_norm, 0);
+        SUB_TRY(launch_gemv(oa, w4, EPI_RESID, st));
+      } else {
+        SUB_TRY(launch_matmul(oa, w4, EPI_RESID, st));
+        SUB_TRY(launch_rmsnorm(m->x, L.ffn_norm, M, H, d.rms_eps, m->xn, st));
+      }
+    }
     {
       GemvArgs ga = mm_args(m->xn, M, H, W, gu_idx, 2, gu_rows, m->act, F);
       ga.N = F;   // GLU: grid covers one segment's rows
       SUB_TRY(launch_matmul(ga, w4, EPI_GLU, st));
     }
-    SUB_TRY(launch_matmul(mm_args(m->act, M, F, W, dn_idx, 1, o_rows, m->x, H), w4, EPI_RESID, st));
+    {
+      GemvArgs da = mm_args(m->act, M, F, W, dn_idx, 1, o_rows, m->x, H);
+      if (fuse_norm) {
+        da.norm = norm_out(next_gain, 1);
+        SUB_TRY(launch_gemv(da, w4, EPI_RESID, st));
+      } else {
+        SUB_TRY(launch_matmul(da, w4, EPI_RESID, st));
+      }
+    }
 
     if (off && !draft) {
       // slot j % ring is free once this layer's kernels are done: stage layer j + ring
@@ -329,16 +383,21 @@ static int32_t forward(sub_model* m, bool draft, const FwdRows& r, float* logits
       }
     }
   }
-  // final norm + lm_head
+  // final norm (already in xn on the fused path) + lm_head
   const int first = last_only ? M - 1 : 0;
   const int nrow = last_only ? 1 : M;
-  SUB_TRY(launch_rmsnorm(m->x + (size_t)first * H, d.final_norm, nrow, H, d.rms_eps, m->xn, st));
+  const uint16_t* xin = m->xn;
+  if (fuse_norm) {
+    xin = m->xn + (size_t)first * H;
+  } else {
+    SUB_TRY(launch_rmsnorm(m->x + (size_t)first * H, d.final_norm, nrow, H, d.rms_eps, m->xn, st));
+  }
   if (logits) {
     Matrices lm{};
     lm.w[0] = d.lm_head;
     const int idx0[1] = {0};
     const int vrows[1] = {d.vocab};
-    SUB_TRY(launch_matmul(mm_args(m->xn, nrow, H, lm, idx0, 1, vrows, logits, d.vocab), false,
+    SUB_TRY(launch_matmul(mm_args(xin, nrow, H, lm, idx0, 1, vrows, logits, d.vocab), false,
                           EPI_F32, st));
   }
   return SUB_OK;
@@ -347,6 +406,8 @@ static int32_t forward(sub_model* m, bool draft, const FwdRows& r, float* logits
 // ------------------------------------------------------------ tiny kernels --
 // After accept: committed length += accepted + 1, the bonus becomes the root.
 __global__ void advance_kernel(int32_t* state, int32_t* root_token) {
+  pdl_trigger();
+  pdl_wait();
   state[ST_N] += state[ST_NACC] + 1;
   *root_token = state[ST_BONUS];
 }
@@ -456,8 +517,10 @@ extern "C" int32_t sub_model_create(const sub_model_desc* desc, sub_model** out)
   CREATE_TRY(dalloc_t(m, &m->act, R * F));
   CREATE_TRY(dalloc_t(m, &m->logits, (size_t)m->logit_rows * d.vocab));
   CREATE_TRY(dalloc_t(m, &m->rows_tok, R));
-  m->attn_part_floats = (size_t)std::max(d.max_width, 8) * d.n_heads_q * (D + 2) * 32;
-  CREATE_TRY(dalloc_t(m, &m->attn_part, m->attn_part_floats));
+  m->norm_parts = (H / 16 + 1) * 16;
+  CREATE_TRY(dalloc_t(m, &m->norm_partial, m->norm_parts));
+  CREATE_TRY(dalloc_t(m, &m->norm_counters, 4));
+  CREATE_CUDA(cudaMemset(m->norm_counters, 0, 16));
 
   // tree (slot 0 = root: parent -1, depth 0, score 0, anc [0, -1...])
   {
@@ -695,8 +758,8 @@ static int32_t enqueue_cycle(sub_model* m, const sub_decode_cfg& c) {
   cp.n_accepted = m->state + ST_NACC;
   cp.max_accept = D;
   SUB_TRY(launch_compact(cp, m->s_main));
-  advance_kernel<<<1, 1, 0, m->s_main>>>(m->state, tr.token);
-  return check_launch("advance");
+  SUB_CUDA_TRY(launch_k(advance_kernel, dim3(1), dim3(1), 0, m->s_main, m->state, tr.token));
+  return SUB_OK;
 }
 
 static bool same_cfg(const sub_decode_cfg& a, const sub_decode_cfg& b) {
@@ -796,8 +859,7 @@ static int32_t prefill_impl(sub_model* m, const int32_t* prompt_host, int32_t n_
   SUB_TRY(accept_args(m, c, 1, a));
   a.hist = nullptr;
   SUB_TRY(launch_accept(a, st));
-  advance_kernel<<<1, 1, 0, st>>>(m->state, m->tree.token);
-  SUB_TRY(check_launch("advance"));
+  SUB_CUDA_TRY(launch_k(advance_kernel, dim3(1), dim3(1), 0, st, m->state, m->tree.token));
   SUB_CUDA_TRY(cudaMemsetAsync(m->hist, 0, (d.max_depth + 1) * 4, st));
   m->n_prompt = n_prompt;
   m->cycles = 0;

@@ -95,6 +95,8 @@ __global__ void __launch_bounds__(EXP_THREADS) expand_kernel(ExpandArgs a) {
   __shared__ unsigned long long s_red[EXP_THREADS / 32];
   __shared__ float s_m[EXP_THREADS / 32], s_s[EXP_THREADS / 32];
   __shared__ unsigned int s_last;
+  pdl_trigger();
+  pdl_wait();
   const int k = a.tree.width;
   const int j = blockIdx.y, c = blockIdx.x;
   const int64_t V = a.V;
@@ -243,9 +245,9 @@ int32_t launch_expand(const ExpandArgs& a, cudaStream_t st) {
   SUB_CHECK_ARG(1 + (int64_t)a.tree.max_depth * k < 4096, "expand: tree too large");
   SUB_CHECK_ARG(a.temp > 0.f, "expand: temperature must be positive");
   dim3 grid(a.n_chunks, a.k_prev);
-  if (k <= 8) expand_kernel<8><<<grid, EXP_THREADS, 0, st>>>(a);
-  else expand_kernel<16><<<grid, EXP_THREADS, 0, st>>>(a);
-  return check_launch("draft_expand");
+  if (k <= 8) SUB_CUDA_TRY(launch_k(expand_kernel<8>, grid, dim3(EXP_THREADS), 0, st, a));
+  else SUB_CUDA_TRY(launch_k(expand_kernel<16>, grid, dim3(EXP_THREADS), 0, st, a));
+  return SUB_OK;
 }
 
 // ------------------------------------------------------------- accept --
@@ -263,6 +265,8 @@ int accept_pick_chunks(int n_nodes, int64_t V) {
 __global__ void __launch_bounds__(ACC_THREADS) accept_kernel(AcceptArgs a) {
   __shared__ unsigned long long s_red[ACC_THREADS / 32];
   __shared__ unsigned int s_last;
+  pdl_trigger();
+  pdl_wait();
   const int u = blockIdx.y, c = blockIdx.x;
   const int64_t V = a.V;
   // chunks of whole 4-token Philox blocks
@@ -341,8 +345,8 @@ int32_t launch_accept(const AcceptArgs& a, cudaStream_t st) {
   SUB_CHECK_ARG(a.V < (1ll << 32), "accept: V too large");
   SUB_CHECK_ARG(a.choice != nullptr, "accept: choice buffer required");
   dim3 grid(a.n_chunks, a.n_nodes);
-  accept_kernel<<<grid, ACC_THREADS, 0, st>>>(a);
-  return check_launch("verify_accept");
+  SUB_CUDA_TRY(launch_k(accept_kernel, grid, dim3(ACC_THREADS), 0, st, a));
+  return SUB_OK;
 }
 
 // ------------------------------------------------------------ compact --
@@ -350,6 +354,8 @@ int32_t launch_accept(const AcceptArgs& a, cudaStream_t st) {
 // a destination that is also a later source cannot be clobbered.
 __global__ void compact_kernel(CompactArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
+  pdl_trigger();
+  pdl_wait();
   const int layer = blockIdx.x, h = blockIdx.y;
   const int n = min(*a.n_accepted, a.max_accept);
   if (n <= 0) return;
@@ -385,8 +391,8 @@ int32_t launch_compact(const CompactArgs& a, cudaStream_t st) {
   if (a.max_accept == 0) return SUB_OK;
   const int smem = 2 * a.max_accept * a.head_dim * 2;
   dim3 grid(a.n_layers, a.n_heads_kv);
-  compact_kernel<<<grid, 128, smem, st>>>(a);
-  return check_launch("kv_compact");
+  SUB_CUDA_TRY(launch_k(compact_kernel, grid, dim3(128), smem, st, a));
+  return SUB_OK;
 }
 
 }  // namespace sub

@@ -1,0 +1,95 @@
+"""Kernel micro-benchmarks on single shapes of the decode path (for timing and
+for profiler captures on a small case).
+
+    python -m substitute_speculative_decoding_gb300.kernel_bench <case> [--iters N]
+
+Cases (Qwen2.5-7B draft/verify shapes; operand sets rotate over more memory
+than the 129 MB L2):
+  gemv_bf16   bf16 weights 18944x3584, M = 8 (a resident FFN matrix)
+  gemv_w4     int4 weights 37888x3584, M = 8 (a substitute gate+up pair)
+  attn_draft  8 tree queries, 28/4 heads, d 128, 640 committed keys
+  attn_verify 385 tree queries, same heads and keys
+  gemm_bf16   bf16 weights 18944x3584, M = 385 (a verify FFN matrix)
+Prints one JSON line: milliseconds per launch and algorithmic GB/s, TFLOP/s.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import sys
+
+import torch
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+
+import synthetic  # noqa: E402
+import substitute_speculative_decoding_gb300 as sub  # noqa: E402
+
+
+def _time(fn, iters):
+    """Milliseconds per call, device-side: the calls are captured once in a
+    CUDA graph and the graph is replayed, so host launch cost drops out."""
+    for i in range(3):
+        fn(i)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(iters):
+            fn(i)
+    g.replay()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(3):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / (3 * iters)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("case")
+    ap.add_argument("--iters", type=int, default=20)
+    a = ap.parse_args()
+    dev = "cuda"
+    res = {"case": a.case}
+    if a.case in ("gemv_bf16", "gemm_bf16"):
+        m = 8 if a.case == "gemv_bf16" else 385
+        ws = [synthetic.randn_bf16((18944, 3584), s, 0.02, dev) for s in range(4)]
+        x = torch.randn(m, 3584, device=dev).to(torch.bfloat16)
+        y = torch.empty(m, 18944, device=dev, dtype=torch.bfloat16)
+        ms = _time(lambda i: sub.bf16_gemm(x, ws[i % 4], out=y), a.iters)
+        byt = 18944 * 3584 * 2 + m * (3584 + 18944) * 2
+        res.update(ms=ms, gbs=byt / ms / 1e6, tflops=2 * m * 18944 * 3584 / ms / 1e9)
+    elif a.case == "gemv_w4":
+        packs = [synthetic.random_w4(37888, 3584, s, dev) for s in range(4)]
+        x = torch.randn(8, 3584, device=dev).to(torch.bfloat16)
+        y = torch.empty(8, 37888, device=dev, dtype=torch.bfloat16)
+        ms = _time(lambda i: sub.w4_gemm(x, *packs[i % 4], 37888, 3584, out=y), a.iters)
+        byt = 37888 * 56 * 36 + 8 * (3584 + 37888) * 2
+        res.update(ms=ms, gbs=byt / ms / 1e6)
+    elif a.case in ("attn_draft", "attn_verify"):
+        depth, width, hq, hkv, d, n_prefix = 48, 8, 28, 4, 128, 640
+        tok, par, dep = synthetic.random_tree(depth, width, 1, 1000)
+        anc = synthetic.ancestors(par, dep, depth).to(dev)
+        dep = dep.to(dev)
+        n_tree = len(par)
+        kv, keep = sub.make_kv(1, hkv, d, n_prefix + n_tree + 64)
+        keep[0].normal_()
+        keep[1].normal_()
+        nq = width if a.case == "attn_draft" else n_tree
+        q = torch.randn(nq, hq, d, device=dev).to(torch.bfloat16)
+        an, dp = anc[-nq:].contiguous(), dep[-nq:].contiguous()
+        ms = _time(lambda i: sub.tree_attn(q, kv, 0, n_prefix, n_prefix, n_tree, anc=an,
+                                           depth=dp), a.iters)
+        byt = (n_prefix + n_tree) * hkv * d * 4 + 2 * nq * hq * d * 2
+        res.update(ms=ms, gbs=byt / ms / 1e6)
+    else:
+        raise SystemExit(f"unknown case {a.case}")
+    print(json.dumps(res))
+
+
+if __name__ == "__main__":
+    main()
