@@ -10,6 +10,11 @@ than the 129 MB L2):
   attn_draft  8 tree queries, 28/4 heads, d 128, 640 committed keys
   attn_verify 385 tree queries, same heads and keys
   gemm_bf16   bf16 weights 18944x3584, M = 385 (a verify FFN matrix)
+  draft_level one draft forward of 8 tree nodes through the whole Qwen2.5-7B-shaped
+              model (11 resident + 17 int4 layers, lm_head), inside the NVTX range
+              "draft_level" (the second of two runs)
+  verify_pass one target forward over a 385-node tree (offloaded layers streamed),
+              inside the NVTX range "verify_pass"
 Prints one JSON line: milliseconds per launch and algorithmic GB/s, TFLOP/s.
 """
 from __future__ import annotations
@@ -46,6 +51,45 @@ def _time(fn, iters):
     e1.record()
     torch.cuda.synchronize()
     return e0.elapsed_time(e1) / (3 * iters)
+
+
+def _model_pass(case):
+    """One draft level (8 rows at the deepest level) or one verify pass of the
+    Qwen2.5-7B-shaped model after a 512-token prefill."""
+    cfg = synthetic.CONFIGS["qwen7b"]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = synthetic.make_model(cfg, device=dev)
+    m = sub.Model(cfg, w, max_seq=2048, max_depth=48, max_width=8, max_prompt=512)
+    for i in range(cfg.n_resident, cfg.n_layers):
+        for n in synthetic.LAYER_TENSORS:
+            w["layers"][i][n] = w["layers"][i][n].to("cpu")
+    torch.cuda.empty_cache()
+    dcfg = sub.Model.decode_cfg(48, 8, 0.2)
+    m.prefill(synthetic.make_prompt(cfg), dcfg)
+    tok, par, dep = synthetic.random_tree(48, 8, 1, cfg.vocab)
+    anc = synthetic.ancestors(par, dep, 48).to(dev)
+    tok, dep = tok.to(dev), dep.to(dev)
+    logits = torch.empty(385, cfg.vocab, device=dev)
+    s0 = 1 + 46 * 8
+    out = {}
+    for it in range(2):
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if it == 1:
+            torch.cuda.nvtx.range_push(case)
+        e0.record()
+        if case == "draft_level":
+            m.forward(1, tok[s0:s0 + 8], s0, 600, depth=dep[s0:s0 + 8], anc=anc[s0:s0 + 8],
+                      logits=logits)
+        else:
+            m.forward(0, tok, 0, 600, depth=dep, anc=anc, logits=logits)
+        e1.record()
+        torch.cuda.synchronize()
+        if it == 1:
+            torch.cuda.nvtx.range_pop()
+        out["ms"] = e0.elapsed_time(e1)
+    m.close()
+    return out
 
 
 def main():
@@ -86,6 +130,8 @@ def main():
                                            depth=dp), a.iters)
         byt = (n_prefix + n_tree) * hkv * d * 4 + 2 * nq * hq * d * 2
         res.update(ms=ms, gbs=byt / ms / 1e6)
+    elif a.case in ("draft_level", "verify_pass"):
+        res.update(_model_pass(a.case))
     else:
         raise SystemExit(f"unknown case {a.case}")
     print(json.dumps(res))
