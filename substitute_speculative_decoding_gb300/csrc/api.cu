@@ -77,7 +77,20 @@ static int32_t matmul_public(const sub_bf16* X, int64_t M, bool w4, const void* 
   a.N = (int)N;
   a.Y = Y;
   a.ldy = (int)N;
-  return launch_matmul(a, w4, EPI_BF16, as_stream(stream));
+  const cudaStream_t st = as_stream(stream);
+  StreamScratch scratch(st);
+  const int ks = M <= 16 ? gemv_ksplit(a, w4, EPI_BF16) : 1;
+  if (ks > 1) {
+    // room for the split of K over CTAs: ks splits of every 16-row unit
+    const int units = (int)((N + 15) / 16);
+    a.split_cap = (size_t)units * ks * 4 * 128;
+    a.split_cnt_cap = units;
+    SUB_TRY(scratch.alloc(a.split_cap * 4 + (size_t)units * 4));
+    a.split_part = reinterpret_cast<float*>(scratch.p);
+    a.split_cnt = reinterpret_cast<unsigned int*>(a.split_part + a.split_cap);
+    SUB_CUDA_TRY(cudaMemsetAsync(a.split_cnt, 0, (size_t)units * 4, st));
+  }
+  return launch_matmul(a, w4, EPI_BF16, st);
 }
 
 extern "C" int32_t sub_w4_gemm(const sub_bf16* X, int64_t M, const uint8_t* q,

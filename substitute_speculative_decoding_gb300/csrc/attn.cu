@@ -79,19 +79,13 @@ __global__ void __launch_bounds__(THREADS) tree_attn_kernel(AttnArgs a) {
   const int words = (a.n_slots + 31) / 32;
 
   // ---- visibility bitmaps of this CTA's queries ----
+  // depths first (one parallel load), then every ancestor entry in parallel
+  __shared__ int sDep[ROWS + 2];
   if (a.anc) {
     const int nq = q_hi - q_lo + 1;
     for (int i = tid; i < nq * words; i += THREADS) sBits[i] = 0;
-    __syncthreads();
-    for (int i = tid; i < nq * a.anc_stride; i += THREADS) {
-      const int qq = i / a.anc_stride, j = i % a.anc_stride;
-      const int q = q_lo + qq;
-      if (j > a.depth[q]) continue;
-      const int s = a.anc[(int64_t)q * a.anc_stride + j];
-      if (s >= 0 && s < a.n_slots) atomicOr(&sBits[qq * words + (s >> 5)], 1u << (s & 31));
-    }
+    if (tid < nq) sDep[tid] = a.depth[q_lo + tid];
   }
-
   // ---- Q tile ----
   const size_t q_row_stride = (size_t)a.n_heads_q * D;
   for (int c = tid; c < ROWS * CH; c += THREADS) {
@@ -110,23 +104,47 @@ __global__ void __launch_bounds__(THREADS) tree_attn_kernel(AttnArgs a) {
   auto key_pos = [&](int j) -> int64_t {
     return j < n_prefix ? (int64_t)j : tree_base + (j - n_prefix);
   };
-  auto load_kv = [&](int buf, int t) {
-    for (int c = tid; c < KT * CH; c += THREADS) {
-      const int r = c / CH, ch = c % CH;
-      const int j = t * KT + r;
-      const bool ok = j < n_keys;
-      size_t off = 0;
-      if (ok) {
+  // element offset of every key row of a tile, resolved once per tile by KT
+  // threads in parallel (page-table lookups), one tile ahead of its copy
+  __shared__ int64_t sOff[2][KT];
+  auto row_offsets = [&](int slot, int t) {
+    if (tid < KT) {
+      const int j = t * KT + tid;
+      int64_t off = -1;
+      if (t < t_end && j < n_keys) {
         const int64_t p = key_pos(j);
         const int page = a.page_table[p / a.page_size];
-        off = layer_off + (size_t)page * page_stride + (size_t)kvh * head_stride +
-              (size_t)(p % a.page_size) * D + ch * 8;
+        off = (int64_t)(layer_off + (size_t)page * page_stride + (size_t)kvh * head_stride +
+                        (size_t)(p % a.page_size) * D);
       }
-      cp_async16(smem_u32(sK + buf * KT * D * 2 + sw(r, ch) * 16), a.k + off, ok);
-      cp_async16(smem_u32(sV + buf * KT * D * 2 + sw(r, ch) * 16), a.v + off, ok);
+      sOff[slot][tid] = off;
+    }
+  };
+  auto load_kv = [&](int buf, int t) {
+    (void)t;
+    for (int c = tid; c < KT * CH; c += THREADS) {
+      const int r = c / CH, ch = c % CH;
+      const int64_t off = sOff[buf][r];
+      const bool ok = off >= 0;
+      const size_t src = ok ? (size_t)off + ch * 8 : 0;
+      cp_async16(smem_u32(sK + buf * KT * D * 2 + sw(r, ch) * 16), a.k + src, ok);
+      cp_async16(smem_u32(sV + buf * KT * D * 2 + sw(r, ch) * 16), a.v + src, ok);
     }
   };
 
+  row_offsets(0, t_begin);
+  row_offsets(1, t_begin + 1);
+  __syncthreads();   // depths, cleared bitmaps and the first row offsets are visible
+  if (a.anc) {
+    const int nq = q_hi - q_lo + 1;
+    for (int i = tid; i < nq * a.anc_stride; i += THREADS) {
+      const int qq = i / a.anc_stride, j = i % a.anc_stride;
+      const int q = q_lo + qq;
+      if (j > sDep[qq]) continue;
+      const int s = a.anc[(int64_t)q * a.anc_stride + j];
+      if (s >= 0 && s < a.n_slots) atomicOr(&sBits[qq * words + (s >> 5)], 1u << (s & 31));
+    }
+  }
   if (t_begin < t_end) load_kv(0, t_begin);
   cp_commit();
 
@@ -252,7 +270,8 @@ __global__ void __launch_bounds__(THREADS) tree_attn_kernel(AttnArgs a) {
         mma_bf16_16816(o[2 * dd], pa[kk], b0, b1);
         mma_bf16_16816(o[2 * dd + 1], pa[kk], b2, b3);
       }
-    __syncthreads();   // buffer reuse by the next prefetch
+    row_offsets(buf, t + 2);
+    __syncthreads();   // buffer reuse by the next prefetch; row offsets of tile t + 2
   }
 
   pdl_trigger();

@@ -1,15 +1,21 @@
 // Warp-level GEMV kernels (bf16 and int4 weights), see gemv.cuh.
+//
+// A CTA owns RT row tiles (16 rows each, two per lane: g and g + 8) over one
+// split of K.  Each warp keeps U steps of weights and activations in flight
+// with a rolling register prefetch; the first U weight steps are requested
+// before the programmatic-launch wait.  Splits of K over CTAs (grid.y) meet in
+// a scratch buffer and the last split of a unit adds them in split order.
+#include <algorithm>
 #include "gemv.cuh"
 
 namespace sub {
 
 __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
 
-constexpr int WK = 4;   // warps per CTA, splitting K
+constexpr int WK = 4;   // warps per CTA, splitting the CTA's K range
 
-// Activations come from the previous kernel, which may still be draining when
-// this one starts (programmatic dependent launch): read them coherently
-// through L2, never through the read-only path.
+// Activations are written by the previous kernel of the stream: L2-coherent
+// loads that the compiler may not hoist above the programmatic-launch wait.
 __device__ __forceinline__ uint4 ldcg_v4(const uint16_t* p) {
   uint4 r;
   asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -63,6 +69,13 @@ __device__ __forceinline__ int seg_rows(const GemvArgs& a, int seg) {
   return a.seg_end[seg] - (seg ? a.seg_end[seg - 1] : 0);
 }
 
+// K columns of each split: bf16 steps of 32, int4 groups of 64, whole U batches.
+template <bool W4, int U>
+__host__ __device__ inline int split_units(int K, int ks) {
+  const int total = W4 ? (K + 63) / 64 : (K + 31) / 32;
+  return ((total + ks - 1) / ks + U - 1) / U * U;
+}
+
 template <bool W4, int MT, int RT, int EPI, int U>
 __global__ void __launch_bounds__(WK * 32)
 gemv_kernel(GemvArgs a) {
@@ -72,6 +85,14 @@ gemv_kernel(GemvArgs a) {
   const int g = lane >> 2, tig = lane & 3;
   const int K = a.K;
   const int G = (K + 63) / 64;
+  const int ks = gridDim.y;
+
+  // this CTA's K range, in steps of 32 (bf16) or groups of 64 (int4)
+  const int total_u = W4 ? G : (K + 31) / 32;
+  const int per_split = split_units<W4, U>(K, ks);
+  const int r_begin = blockIdx.y * per_split, r_end = min(total_u, r_begin + per_split);
+  const int per = ((r_end - r_begin + WK - 1) / WK + U - 1) / U * U;
+  const int u_begin = r_begin + warp * per, u_end = min(r_end, u_begin + per);
 
   // ---- per-tile row pointers (two rows per lane: g and g + 8) ----
   const char* rp0[NT];
@@ -118,12 +139,9 @@ gemv_kernel(GemvArgs a) {
 
   if constexpr (!W4) {
     // ------------------------------------------------ bf16 weights ----
-    const int steps = (K + 31) / 32;
-    const int per = ((steps + WK - 1) / WK + U - 1) / U * U;
-    const int s_begin = warp * per, s_end = min(steps, s_begin + per);
     uint4 w0[U][NT], w1[U][NT], xv[U][MT];
     auto load_w = [&](int u, int s) {
-      const bool ok = s < s_end && s * 32 + tig * 8 < K;   // K % 8 == 0: whole 16-byte chunks
+      const bool ok = s < u_end && s * 32 + tig * 8 < K;   // K % 8 == 0: whole chunks
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
         w0[u][t] = ok ? ldg_nc_v4(rp0[t] + (int64_t)s * 64) : make_uint4(0, 0, 0, 0);
@@ -132,18 +150,17 @@ gemv_kernel(GemvArgs a) {
     };
     auto load_x = [&](int u, int s) {
       const int k = s * 32 + tig * 8;
-      const bool ok = s < s_end && k < K;
+      const bool ok = s < u_end && k < K;
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt)
-        xv[u][mt] = (ok && xok[mt]) ? ldcg_v4(xp[mt] + k)
-                                    : make_uint4(0, 0, 0, 0);
+        xv[u][mt] = (ok && xok[mt]) ? ldcg_v4(xp[mt] + k) : make_uint4(0, 0, 0, 0);
     };
 #pragma unroll
-    for (int u = 0; u < U; ++u) load_w(u, s_begin + u);   // weights before the wait
+    for (int u = 0; u < U; ++u) load_w(u, u_begin + u);   // weights before the wait
     pdl_wait();
 #pragma unroll
-    for (int u = 0; u < U; ++u) load_x(u, s_begin + u);
-    for (int s = s_begin; s < s_end; s += U) {
+    for (int u = 0; u < U; ++u) load_x(u, u_begin + u);
+    for (int s = u_begin; s < u_end; s += U) {
 #pragma unroll
       for (int u = 0; u < U; ++u) {
 #pragma unroll
@@ -161,18 +178,18 @@ gemv_kernel(GemvArgs a) {
     }
   } else {
     // ------------------------------------------------ int4 weights ----
-    const int per = ((G + WK - 1) / WK + U - 1) / U * U;
-    const int g_begin = warp * per, g_end = min(G, g_begin + per);
-    // scales/zeros of U = 4 consecutive groups in one 8-byte load when rows allow
-    const bool sz_vec = (U == 4) && (G % 4 == 0);
+    // scales/zeros of 4 consecutive groups in one 8-byte load when rows allow
+    const bool sz_vec = (G % 4 == 0);
     const uint32_t ONES = 0x3f803f80u;
     const uint32_t ONES_A[4] = {ONES, ONES, ONES, ONES};
+    static_assert(U % 4 == 0, "int4 batches are whole 4-group scale loads");
+    constexpr int UB = U / 4;
     uint2 q0[U][NT], q1[U][NT];
-    uint2 sv0[NT], sv1[NT], zv0[NT], zv1[NT];
+    uint2 sv0[UB][NT], sv1[UB][NT], zv0[UB][NT], zv1[UB][NT];
     uint16_t ss0[U][NT], ss1[U][NT], zs0[U][NT], zs1[U][NT];
     uint4 xa[U][MT], xb[U][MT];
     auto load_q = [&](int u, int gi) {
-      const bool ok = gi < g_end;
+      const bool ok = gi < u_end;
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
         q0[u][t] = ok ? ldg_nc_v2(rp0[t] + (int64_t)gi * 32) : make_uint2(0, 0);
@@ -184,43 +201,39 @@ gemv_kernel(GemvArgs a) {
           zs1[u][t] = ok ? __ldg(zp1[t] + gi) : 0;
         }
       }
-    };
-    auto load_sz = [&](int gi0) {   // vector path: groups gi0 .. gi0 + 3 (gi0 % 4 == 0)
-      const bool ok = sz_vec && gi0 < g_end;
+      // groups gi - 3 .. gi in one 8-byte load (gi - 3 is a multiple of 4), issued
+      // with the last of the four slots that use them, so the rolling reload
+      // never overwrites scales of the batch in progress
+      if (sz_vec && (u & 3) == 3) {
+        const int b = u >> 2, g4 = gi - 3;
+        const bool ok4 = g4 < u_end;
 #pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        sv0[t] = ok ? __ldg(reinterpret_cast<const uint2*>(sp0[t] + gi0)) : make_uint2(0, 0);
-        sv1[t] = ok ? __ldg(reinterpret_cast<const uint2*>(sp1[t] + gi0)) : make_uint2(0, 0);
-        zv0[t] = ok ? __ldg(reinterpret_cast<const uint2*>(zp0[t] + gi0)) : make_uint2(0, 0);
-        zv1[t] = ok ? __ldg(reinterpret_cast<const uint2*>(zp1[t] + gi0)) : make_uint2(0, 0);
+        for (int t = 0; t < NT; ++t) {
+          sv0[b][t] = ok4 ? __ldg(reinterpret_cast<const uint2*>(sp0[t] + g4)) : make_uint2(0, 0);
+          sv1[b][t] = ok4 ? __ldg(reinterpret_cast<const uint2*>(sp1[t] + g4)) : make_uint2(0, 0);
+          zv0[b][t] = ok4 ? __ldg(reinterpret_cast<const uint2*>(zp0[t] + g4)) : make_uint2(0, 0);
+          zv1[b][t] = ok4 ? __ldg(reinterpret_cast<const uint2*>(zp1[t] + g4)) : make_uint2(0, 0);
+        }
       }
     };
     auto load_x = [&](int u, int gi) {
-      const bool ok = gi < g_end;
+      const bool ok = gi < u_end;
       const int k = gi * 64 + tig * 16;
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
-        xa[u][mt] = (ok && xok[mt] && k < K) ? ldcg_v4(xp[mt] + k)
-                                             : make_uint4(0, 0, 0, 0);
-        xb[u][mt] = (ok && xok[mt] && k + 8 < K)
-                        ? ldcg_v4(xp[mt] + k + 8)
-                        : make_uint4(0, 0, 0, 0);
+        xa[u][mt] = (ok && xok[mt] && k < K) ? ldcg_v4(xp[mt] + k) : make_uint4(0, 0, 0, 0);
+        xb[u][mt] = (ok && xok[mt] && k + 8 < K) ? ldcg_v4(xp[mt] + k + 8) : make_uint4(0, 0, 0, 0);
       }
     };
 #pragma unroll
-    for (int u = 0; u < U; ++u) load_q(u, g_begin + u);    // weights before the wait
-    load_sz(g_begin);
+    for (int u = 0; u < U; ++u) load_q(u, u_begin + u);   // weights before the wait
     pdl_wait();
 #pragma unroll
-    for (int u = 0; u < U; ++u) load_x(u, g_begin + u);
-    for (int gi0 = g_begin; gi0 < g_end; gi0 += U) {
-      uint2 cs0[NT], cs1[NT], cz0[NT], cz1[NT];   // this batch's packed scales/zeros
-#pragma unroll
-      for (int t = 0; t < NT; ++t) { cs0[t] = sv0[t]; cs1[t] = sv1[t]; cz0[t] = zv0[t]; cz1[t] = zv1[t]; }
-      load_sz(gi0 + U);
+    for (int u = 0; u < U; ++u) load_x(u, u_begin + u);
+    for (int gi0 = u_begin; gi0 < u_end; gi0 += U) {
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        // B fragments: pairs (k, k+4) to match the nibble pairs of one word
+        // B fragments: pairs (k, k+4) to match the nibble pairs of one packed word
         uint32_t b[MT][4][2];
         float sx[MT][4];
 #pragma unroll
@@ -243,8 +256,11 @@ gemv_kernel(GemvArgs a) {
           // scale and 128 + zero of rows g and g + 8 for group gi0 + u
           uint32_t a0s, a1s, b0z, b1z;
           if (sz_vec) {
-            const uint32_t ws0 = u < 2 ? cs0[t].x : cs0[t].y, ws1 = u < 2 ? cs1[t].x : cs1[t].y;
-            const uint32_t wz0 = u < 2 ? cz0[t].x : cz0[t].y, wz1 = u < 2 ? cz1[t].x : cz1[t].y;
+            const int bb = u >> 2;
+            const uint32_t ws0 = (u & 2) ? sv0[bb][t].y : sv0[bb][t].x;
+            const uint32_t ws1 = (u & 2) ? sv1[bb][t].y : sv1[bb][t].x;
+            const uint32_t wz0 = (u & 2) ? zv0[bb][t].y : zv0[bb][t].x;
+            const uint32_t wz1 = (u & 2) ? zv1[bb][t].y : zv1[bb][t].x;
             a0s = (u & 1) ? (ws0 >> 16) : (ws0 & 0xffffu);
             a1s = (u & 1) ? (ws1 >> 16) : (ws1 & 0xffffu);
             b0z = (u & 1) ? (wz0 >> 16) : (wz0 & 0xffffu);
@@ -306,11 +322,39 @@ gemv_kernel(GemvArgs a) {
       for (int j = 0; j < 4; ++j)
         red[warp * PER_WARP + ((t * MT + mt) * 4 + j) * 32 + lane] = acc[t][mt][j];
   __syncthreads();
-  auto total = [&](int e) {
+  __shared__ float tot_s[PER_WARP];
+  for (int e = threadIdx.x; e < PER_WARP; e += WK * 32) {
     float v = 0.f;
 #pragma unroll
     for (int w = 0; w < WK; ++w) v += red[w * PER_WARP + e];
-    return v;
+    tot_s[e] = v;
+  }
+  if (ks > 1) {
+    // split of K over CTAs: park this split's sums, the last split of the unit adds all
+    __shared__ unsigned int s_split_last;
+    __syncthreads();
+    float* mine = a.split_part + ((size_t)blockIdx.x * ks + blockIdx.y) * PER_WARP;
+    for (int e = threadIdx.x; e < PER_WARP; e += WK * 32) mine[e] = tot_s[e];
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0)
+      s_split_last = (atomicAdd(a.split_cnt + blockIdx.x, 1u) == (unsigned)ks - 1) ? 1u : 0u;
+    __syncthreads();
+    if (!s_split_last) return;
+    __threadfence();
+    const float* all = a.split_part + (size_t)blockIdx.x * ks * PER_WARP;
+    for (int e = threadIdx.x; e < PER_WARP; e += WK * 32) {
+      float v = 0.f;
+      for (int y = 0; y < ks; ++y) v += __ldcg(all + (size_t)y * PER_WARP + e);
+      tot_s[e] = v;
+    }
+    if (threadIdx.x == 0) a.split_cnt[blockIdx.x] = 0u;
+  }
+  __syncthreads();
+  // factored RMSNorm of the input: scale each token's sums by its row scale
+  auto total = [&](int e, int tok) {
+    const float v = tot_s[e];
+    return a.xscale ? v * __ldcg(a.xscale + tok) : v;
   };
 
   if constexpr (EPI == EPI_QKV) {
@@ -325,10 +369,10 @@ gemv_kernel(GemvArgs a) {
     for (int h = threadIdx.x; h < MT * 2 * 32; h += WK * 32) {
       const int ln = h & 31, j = (h >> 5) & 1, mt = h >> 6;
       const int e = (mt * 4 + j) * 32 + ln;
-      const float vlo = total(e), vhi = total(e + 64);
       const int gg = ln >> 2, tg = ln & 3;
       const int tok = mt * 8 + 2 * tg + j;
       if (tok >= a.M) continue;
+      const float vlo = total(e, tok), vhi = total(e + 64, tok);
       const int64_t kvpos = base + qo.slot0 + tok;
       const size_t slot_off = layer_off + (size_t)qo.page_table[kvpos / qo.page_size] * page_stride +
                               (size_t)(kvpos % qo.page_size) * D;
@@ -360,20 +404,24 @@ gemv_kernel(GemvArgs a) {
     const int j = (e >> 5) & 3;
     const int mt = (e >> 7) % MT;
     const int t = (e >> 7) / MT;
-    const float v = total(e);
     const int gg = ln >> 2, tg = ln & 3;
     const int row = (blockIdx.x * RT + t) * 16 + gg + ((j & 2) ? 8 : 0);
     const int tok = mt * 8 + 2 * tg + (j & 1);
     if (row >= a.N || tok >= a.M) continue;
+    const float v = total(e, tok);
     const int64_t o = (int64_t)tok * a.ldy + row;
     if constexpr (EPI == EPI_BF16) {
       reinterpret_cast<__nv_bfloat16*>(a.Y)[o] = __float2bfloat16_rn(v);
     } else if constexpr (EPI == EPI_F32) {
       reinterpret_cast<float*>(a.Y)[o] = v;
     } else if constexpr (EPI == EPI_RESID) {
-      reinterpret_cast<float*>(a.Y)[o] += v;
+      float* yp = reinterpret_cast<float*>(a.Y) + o;
+      const float xn = *yp + v;
+      *yp = xn;
+      if (a.norm.xn)   // next RMSNorm input, factored: bf16(x * gain)
+        a.norm.xn[o] = f32_to_bf16_bits(xn * bf16_bits_to_f32(a.norm.gain[row]));
     } else {
-      const float vu = total(e + RT * MT * 4 * 32);   // same element of the 'up' tile
+      const float vu = total(e + RT * MT * 4 * 32, tok);   // same element of the 'up' tile
       reinterpret_cast<__nv_bfloat16*>(a.Y)[o] = __float2bfloat16_rn(silu_f(v) * vu);
     }
   }
@@ -381,9 +429,8 @@ gemv_kernel(GemvArgs a) {
   if constexpr (EPI == EPI_RESID) {
     const NormOut& no = a.norm;
     if (!no.xn) return;
-    __shared__ float s_r[16];
     __shared__ unsigned int s_last;
-    float* Y = reinterpret_cast<float*>(a.Y);
+    const float* Y = reinterpret_cast<const float*>(a.Y);
     __syncthreads();   // this CTA's residual rows are written
     if (warp == 0 && lane < a.M) {
       float v[16 * RT];
@@ -403,46 +450,12 @@ gemv_kernel(GemvArgs a) {
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    // last CTA: r[m] = rsqrt(mean(x^2) + eps) from the partials in CTA order
+    // last unit: r[m] = rsqrt(mean(x^2) + eps) from the per-unit partials in unit order
     for (int m = warp; m < a.M; m += WK) {
       float tot = 0.f;
       for (int b = lane; b < (int)gridDim.x; b += 32) tot += __ldcg(no.partial + b * 16 + m);
       tot = warp_sum(tot);
-      if (lane == 0) s_r[m] = rsqrtf(tot / (float)a.ldy + no.eps);
-    }
-    __syncthreads();
-    // every thread normalises whole 8-element chunks, 8 chunks in flight at a time
-    const int nc = a.ldy / 8;   // ldy % 8 == 0
-    const int total_chunks = a.M * nc;
-    constexpr int ILP = 8;
-    for (int base = threadIdx.x; base < total_chunks; base += WK * 32 * ILP) {
-      float4 xa[ILP], xb[ILP];
-      uint4 gv[ILP];
-#pragma unroll
-      for (int i = 0; i < ILP; ++i) {
-        const int idx = base + i * WK * 32;
-        if (idx < total_chunks) {
-          const int m = idx / nc, c = (idx % nc) * 8;
-          const float4* src = reinterpret_cast<const float4*>(Y + (int64_t)m * a.ldy + c);
-          xa[i] = __ldcg(src);
-          xb[i] = __ldcg(src + 1);
-          gv[i] = *reinterpret_cast<const uint4*>(no.gain + c);
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < ILP; ++i) {
-        const int idx = base + i * WK * 32;
-        if (idx < total_chunks) {
-          const int m = idx / nc, c = (idx % nc) * 8;
-          const float r = s_r[m];
-          uint4 o;
-          o.x = pack_bf16x2(xa[i].x * r * bf16lo(gv[i].x), xa[i].y * r * bf16hi(gv[i].x));
-          o.y = pack_bf16x2(xa[i].z * r * bf16lo(gv[i].y), xa[i].w * r * bf16hi(gv[i].y));
-          o.z = pack_bf16x2(xb[i].x * r * bf16lo(gv[i].z), xb[i].y * r * bf16hi(gv[i].z));
-          o.w = pack_bf16x2(xb[i].z * r * bf16lo(gv[i].w), xb[i].w * r * bf16hi(gv[i].w));
-          *reinterpret_cast<uint4*>(no.xn + (int64_t)m * a.ldy + c) = o;
-        }
-      }
+      if (lane == 0) no.rvec[m] = rsqrtf(tot / (float)a.ldy + no.eps);
     }
     if (threadIdx.x == 0) *no.counter = 0u;
   }
@@ -465,11 +478,35 @@ int gemv_grid(const GemvArgs& a, int epi) {
   return (a.N + 16 * rt - 1) / (16 * rt);
 }
 
+// Splits of K over CTAs: each warp walks its K range in batches of U loads
+// and pays about one memory latency per batch, so long K with few row units
+// is latency-chained: aim at about 3 batches per warp when the row units
+// alone leave fewer than 8 CTAs per SM.
+static int pick_ksplit(const GemvArgs& a, bool w4, int units) {
+  if (units >= 8 * 152) return 1;
+  const int U = 4;
+  const int batches = w4 ? ((a.K + 63) / 64 + U - 1) / U : ((a.K + 31) / 32 + U - 1) / U;
+  int ks = (batches + 4 * 3 - 1) / (4 * 3);
+  ks = std::max(1, std::min(ks, 8));
+  while (ks > 1 && units * ks > 16 * 152) --ks;
+  return ks;
+}
+
+int gemv_ksplit(const GemvArgs& a, bool is_w4, int epi) {
+  return pick_ksplit(a, is_w4, gemv_grid(a, epi));
+}
+
 template <bool W4, int MT, int RT, int EPI>
-static int32_t launch_cfg(const GemvArgs& a, cudaStream_t st) {
+static int32_t launch_cfg(const GemvArgs& a_in, cudaStream_t st) {
   constexpr int U = 4;
-  SUB_CUDA_TRY(launch_k(gemv_kernel<W4, MT, RT, EPI, U>, dim3(gemv_grid(a, EPI)), dim3(WK * 32), 0,
-                        st, a));
+  constexpr int NT = (EPI == EPI_GLU) ? 2 * RT : RT;
+  constexpr int PER = NT * MT * 4 * 32;
+  GemvArgs a = a_in;
+  const int units = gemv_grid(a, EPI);
+  int ks = (a.split_part && a.split_cnt) ? pick_ksplit(a, W4, units) : 1;
+  while (ks > 1 && ((size_t)units * ks * PER > a.split_cap || units > a.split_cnt_cap)) --ks;
+  a.ksplit = ks;
+  SUB_CUDA_TRY(launch_k(gemv_kernel<W4, MT, RT, EPI, U>, dim3(units, ks), dim3(WK * 32), 0, st, a));
   return SUB_OK;
 }
 
@@ -505,6 +542,7 @@ int32_t launch_gemv(const GemvArgs& a, bool is_w4, int epi, cudaStream_t st) {
   SUB_CHECK_ARG(a.M >= 1 && a.M <= 16, "gemv: M must be in [1, 16]");
   SUB_CHECK_ARG(a.K % 8 == 0 && a.ldx % 8 == 0, "gemv: K and ldx must be multiples of 8");
   SUB_CHECK_ARG(a.n_seg >= 1 && a.n_seg <= 4, "gemv: 1..4 segments");
+  SUB_CHECK_ARG(aligned16(a.X), "gemv: X must be 16-byte aligned");
   if (a.n_seg > 1 || epi == EPI_GLU)
     for (int i = 0; i < a.n_seg; ++i) {
       const int start = i ? a.seg_end[i - 1] : 0;
@@ -520,10 +558,8 @@ int32_t launch_gemv(const GemvArgs& a, bool is_w4, int epi, cudaStream_t st) {
                   "gemv: q/k/v segment sizes");
   }
   if (epi == EPI_RESID && a.norm.xn)
-    SUB_CHECK_ARG(a.norm.partial && a.norm.counter && a.norm.gain && a.ldy == a.N &&
-                      a.N % 8 == 0 && aligned16(a.norm.gain) && aligned16(a.norm.xn) &&
-                      aligned16(a.Y),
-                  "gemv: norm epilogue needs partial, counter, gain and ldy == N");
+    SUB_CHECK_ARG(a.norm.partial && a.norm.counter && a.norm.gain && a.norm.rvec && a.ldy == a.N,
+                  "gemv: norm epilogue needs partial, counter, gain, rvec and ldy == N");
   return is_w4 ? launch_epi<true>(a, epi, st) : launch_epi<false>(a, epi, st);
 }
 

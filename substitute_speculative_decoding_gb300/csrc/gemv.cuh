@@ -17,13 +17,14 @@
 // Y += s * (P - (128 + z) * Sx).  This is (q - z) * s without rounding the
 // dequantised weight to bf16 first.
 //
-// A CTA owns RT row tiles (16 rows each) over the whole K; its 4 warps split
-// K and their partial sums meet in shared memory in a fixed order, so results
-// are deterministic.  Epilogues: bf16 or fp32 store, fp32 residual add (which
-// can also produce the next RMSNorm's bf16 input: per-CTA sums of squares,
-// then the last CTA to finish normalises all M rows), SiLU(gate)*up, and the
-// q/k/v epilogue (RoPE on q and k from rows paired i / i + d/2 inside one tile,
-// bf16 q out, k and v written into the paged KV cache).
+// A CTA owns RT row tiles (16 rows each) over one split of K (grid.y), with
+// its slice of the activations staged once in shared memory; its 4 warps
+// split the slice and their partial sums meet in shared memory in a fixed
+// order, as do the splits, so results are deterministic.  Epilogues: bf16 or
+// fp32 store, fp32 residual add (which can also produce the next RMSNorm's
+// input in factored form, see NormOut), SiLU(gate)*up, and the q/k/v epilogue
+// (RoPE on q and k from rows paired i / i + d/2 inside one tile, bf16 q out,
+// k and v written into the paged KV cache).
 #pragma once
 #include "common.cuh"
 
@@ -37,13 +38,19 @@ enum GemvEpi : int {
   EPI_QKV = 4,     // segments q, k, v -> RoPE, bf16 q, K/V into the cache (QkvOut)
 };
 
-// Residual epilogue extension: xn[m, :] = bf16(Y[m, :] * rsqrt(mean(Y[m]^2) + eps) * gain)
+// Residual epilogue extension (the next RMSNorm, factored): every unit writes
+// xn[m, rows] = bf16(Y[m, rows] * gain[rows]) for its own rows and its partial
+// sum of squares; the last unit writes rvec[m] = rsqrt(mean(Y[m]^2) + eps).
+// The consumer GEMV multiplies its accumulators by rvec[m] (GemvArgs::xscale):
+// RMSNorm is a per-row scalar, so sum_k W[n,k] x[m,k] r[m] g[k] =
+// r[m] sum_k W[n,k] (x[m,k] g[k]), with the bf16 rounding taken before the scale.
 struct NormOut {
   uint16_t* xn;              // [M, ldy] bf16, or null for a plain residual add
   const uint16_t* gain;      // [ldy]
   float eps;
-  float* partial;            // [gridDim.x * 16] per-CTA sums of squares
-  unsigned int* counter;     // zero before launch; the last CTA resets it
+  float* rvec;               // [M] row scales for the consumer
+  float* partial;            // [units * 16] per-unit sums of squares
+  unsigned int* counter;     // zero before launch; the last unit resets it
 };
 
 // q/k/v epilogue: rows are q (Hq*D), k (Hkv*D), v (Hkv*D); token m sits at
@@ -75,13 +82,24 @@ struct GemvArgs {
   int N;                 // rows covered by the grid (for GLU: rows of one segment)
   void* Y;               // output (bf16 or fp32)
   int ldy;
+  const float* xscale;   // [M] per-row scale of the result (a factored RMSNorm), or null
   NormOut norm;          // EPI_RESID only
   QkvOut qkv;            // EPI_QKV only
+  // split of K over CTAs (grid.y): partial sums meet in split_part and the
+  // last CTA of a row unit adds them in split order; counters start at zero
+  // and are left at zero.  split_cap = floats available in split_part.
+  float* split_part;
+  unsigned int* split_cnt;
+  size_t split_cap;
+  int split_cnt_cap;
+  int ksplit;            // set by launch_gemv
 };
 
 // Launch: int4 (is_w4) or bf16 weights, epilogue, M <= 16.
 int32_t launch_gemv(const GemvArgs& a, bool is_w4, int epi, cudaStream_t stream);
-// CTAs a launch will use (the size of NormOut::partial is 16 floats per CTA).
+// Row units (CTAs along grid.x) a launch uses; NormOut::partial holds 16 floats per unit.
 int gemv_grid(const GemvArgs& a, int epi);
+// Splits of K over CTAs the launch would use given room for them (1 = no split).
+int gemv_ksplit(const GemvArgs& a, bool is_w4, int epi);
 
 }  // namespace sub

@@ -14,6 +14,8 @@
 // the copies for the first ring-full of layers are issued at the start of a
 // cycle, so they run under the draft.
 #include <algorithm>
+#include <cstdio>
+#include <cstdlib>
 #include <cmath>
 #include <mutex>
 #include <vector>
@@ -60,6 +62,12 @@ struct sub_model {
   uint16_t* act = nullptr;   // [rows, F]
   float* logits = nullptr;   // [logit_rows, V]
   int32_t* rows_tok = nullptr;  // [rows] token ids staged for a forward
+  float* split_part = nullptr;       // GEMV split-K partial sums
+  size_t split_cap = 0;
+  unsigned int* split_cnt = nullptr;
+  int split_cnt_cap = 0;
+  float* rvec = nullptr;             // [2][16] row scales of the factored RMSNorms:
+                                     // attention input, FFN input
   float* norm_partial = nullptr;     // [norm_parts] per-CTA sums of squares
   int norm_parts = 0;
   unsigned int* norm_counters = nullptr;
@@ -92,6 +100,10 @@ struct sub_model {
   int64_t cycles = 0;
   int64_t max_emit = 0;
   int64_t graph_kernels = 0;
+  // optional per-kernel tracing of eager forwards (SUB_TRACE=<file>)
+  std::vector<std::pair<const char*, cudaEvent_t>> trace;
+  std::vector<cudaEvent_t> trace_pool;
+  size_t trace_used = 0;
   // graph of one decode cycle
   cudaGraphExec_t graph = nullptr;
   sub_decode_cfg graph_cfg{};
@@ -122,6 +134,7 @@ static void free_model(sub_model* m) {
   if (m->s_copy) cudaStreamSynchronize(m->s_copy);
   if (m->graph) cudaGraphExecDestroy(m->graph);
   for (void* p : m->allocs) cudaFree(p);
+  for (cudaEvent_t e : m->trace_pool) cudaEventDestroy(e);
   for (cudaEvent_t e : m->ev_staged) cudaEventDestroy(e);
   for (cudaEvent_t e : m->ev_free) cudaEventDestroy(e);
   for (cudaEvent_t e : {m->ev_fork, m->ev_join, m->ev_t0, m->ev_t1})
@@ -192,6 +205,45 @@ static int32_t end_target_pass(sub_model* m) {
   return SUB_OK;
 }
 
+// ------------------------------------------------------------------ tracing --
+// With SUB_TRACE=<file>, eager forwards record an event before every kernel on
+// the compute stream; sub_model_forward then appends "name,ms" lines (kernel
+// plus launch gap, stream order) to the file.  Off inside graph capture.
+static const char* trace_path() {
+  static const char* p = getenv("SUB_TRACE");
+  return (p && p[0]) ? p : nullptr;
+}
+static void trace_mark(sub_model* m, const char* name) {
+  if (!trace_path()) return;
+  cudaStreamCaptureStatus cs;
+  if (cudaStreamIsCapturing(m->s_main, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return;
+  if (m->trace_used == m->trace_pool.size()) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return;
+    m->trace_pool.push_back(e);
+  }
+  cudaEvent_t e = m->trace_pool[m->trace_used++];
+  cudaEventRecord(e, m->s_main);
+  m->trace.emplace_back(name, e);
+}
+static void trace_flush(sub_model* m) {
+  if (!trace_path() || m->trace.size() < 2) {
+    m->trace.clear();
+    m->trace_used = 0;
+    return;
+  }
+  cudaStreamSynchronize(m->s_main);
+  FILE* f = fopen(trace_path(), "a");
+  for (size_t i = 0; i + 1 < m->trace.size(); ++i) {
+    float ms = 0.f;
+    cudaEventElapsedTime(&ms, m->trace[i].second, m->trace[i + 1].second);
+    if (f) fprintf(f, "%s,%.5f\n", m->trace[i].first, ms);
+  }
+  if (f) fclose(f);
+  m->trace.clear();
+  m->trace_used = 0;
+}
+
 // ------------------------------------------------------------------ forward --
 struct FwdRows {
   const int32_t* tokens;   // [n]
@@ -207,8 +259,14 @@ struct FwdRows {
 };
 
 static GemvArgs mm_args(const void* X, int M, int K, const Matrices& W, const int* idx, int nseg,
-                        const int* rows, void* Y, int ldy) {
+                        const int* rows, void* Y, int ldy, const sub_model* m = nullptr) {
   GemvArgs a{};
+  if (m) {
+    a.split_part = m->split_part;
+    a.split_cap = m->split_cap;
+    a.split_cnt = m->split_cnt;
+    a.split_cnt_cap = m->split_cnt_cap;
+  }
   a.X = reinterpret_cast<const uint16_t*>(X);
   a.M = M;
   a.K = K;
@@ -248,7 +306,13 @@ static int32_t forward(sub_model* m, bool draft, const FwdRows& r, float* logits
   rs.slot0 = r.slot0;
   rs.base = r.base;
   rs.base_dev = r.base_dev;
-  SUB_TRY(launch_embed(d.embed, H, rs, M, m->x, m->layers[0].attn_norm, d.rms_eps, m->xn, st));
+  trace_mark(m, "embed");
+  // Fused path: RMSNorm in factored form.  xn holds bf16(x * gain) and the
+  // consumer GEMV scales its sums by the row's rsqrt(mean(x^2) + eps).
+  float* const r_attn = fuse_norm ? m->rvec : nullptr;
+  float* const r_ffn = fuse_norm ? m->rvec + 16 : nullptr;
+  SUB_TRY(launch_embed(d.embed, H, rs, M, m->x, m->layers[0].attn_norm, d.rms_eps, m->xn, r_attn,
+                       st));
 
   AttnArgs at{};
   at.Q = m->q;
@@ -307,11 +371,12 @@ static int32_t forward(sub_model* m, bool draft, const FwdRows& r, float* logits
   qo.page_size = m->page_size;
   qo.n_pages = m->n_pages;
 
-  auto norm_out = [&](const uint16_t* gain, int which) {
+  auto norm_out = [&](const uint16_t* gain, int which, float* rv) {
     NormOut no{};
     no.xn = m->xn;
     no.gain = gain;
     no.eps = d.rms_eps;
+    no.rvec = rv;
     no.partial = m->norm_partial;
     no.counter = m->norm_counters + which;
     return no;
@@ -334,40 +399,48 @@ static int32_t forward(sub_model* m, bool draft, const FwdRows& r, float* logits
     const Matrices W = layer_mats(m, l, draft);
     const uint16_t* next_gain = l + 1 < d.n_layers ? m->layers[l + 1].attn_norm : d.final_norm;
 
+    trace_mark(m, w4 ? "qkv_w4" : "qkv_bf16");
     if (fuse_qkv) {
       if (!fuse_norm && l > 0) SUB_TRY(launch_rmsnorm(m->x, L.attn_norm, M, H, d.rms_eps, m->xn, st));
-      GemvArgs qa = mm_args(m->xn, M, H, W, qkv_idx, 3, qkv_rows, nullptr, 0);
+      GemvArgs qa = mm_args(m->xn, M, H, W, qkv_idx, 3, qkv_rows, nullptr, 0, m);
+      qa.xscale = r_attn;
       qo.layer = l;
       qa.qkv = qo;
       SUB_TRY(launch_gemv(qa, w4, EPI_QKV, st));
     } else {
       if (l > 0 && !fuse_norm) SUB_TRY(launch_rmsnorm(m->x, L.attn_norm, M, H, d.rms_eps, m->xn, st));
-      SUB_TRY(launch_matmul(mm_args(m->xn, M, H, W, qkv_idx, 3, qkv_rows, m->qkv, m->qkv_dim), w4,
-                            EPI_F32, st));
+      GemvArgs qa = mm_args(m->xn, M, H, W, qkv_idx, 3, qkv_rows, m->qkv, m->qkv_dim, m);
+      qa.xscale = r_attn;
+      SUB_TRY(launch_matmul(qa, w4, EPI_F32, st));
       qp.layer = l;
       SUB_TRY(launch_qkv_post(qp, st));
     }
     at.layer = l;
+    trace_mark(m, "attn");
     SUB_TRY(launch_tree_attn(at, splits, st));
+    trace_mark(m, w4 ? "o_w4" : "o_bf16");
     {
-      GemvArgs oa = mm_args(m->attn, M, m->q_dim, W, o_idx, 1, o_rows, m->x, H);
+      GemvArgs oa = mm_args(m->attn, M, m->q_dim, W, o_idx, 1, o_rows, m->x, H, m);
       if (fuse_norm) {
-        oa.norm = norm_out(L.ffn_norm, 0);
+        oa.norm = norm_out(L.ffn_norm, 0, r_ffn);
         SUB_TRY(launch_gemv(oa, w4, EPI_RESID, st));
       } else {
         SUB_TRY(launch_matmul(oa, w4, EPI_RESID, st));
         SUB_TRY(launch_rmsnorm(m->x, L.ffn_norm, M, H, d.rms_eps, m->xn, st));
       }
     }
+    trace_mark(m, w4 ? "gate_up_w4" : "gate_up_bf16");
     {
-      GemvArgs ga = mm_args(m->xn, M, H, W, gu_idx, 2, gu_rows, m->act, F);
+      GemvArgs ga = mm_args(m->xn, M, H, W, gu_idx, 2, gu_rows, m->act, F, m);
       ga.N = F;   // GLU: grid covers one segment's rows
+      ga.xscale = r_ffn;
       SUB_TRY(launch_matmul(ga, w4, EPI_GLU, st));
     }
+    trace_mark(m, w4 ? "down_w4" : "down_bf16");
     {
-      GemvArgs da = mm_args(m->act, M, F, W, dn_idx, 1, o_rows, m->x, H);
+      GemvArgs da = mm_args(m->act, M, F, W, dn_idx, 1, o_rows, m->x, H, m);
       if (fuse_norm) {
-        da.norm = norm_out(next_gain, 1);
+        da.norm = norm_out(next_gain, 1, r_attn);
         SUB_TRY(launch_gemv(da, w4, EPI_RESID, st));
       } else {
         SUB_TRY(launch_matmul(da, w4, EPI_RESID, st));
@@ -392,14 +465,17 @@ static int32_t forward(sub_model* m, bool draft, const FwdRows& r, float* logits
   } else {
     SUB_TRY(launch_rmsnorm(m->x + (size_t)first * H, d.final_norm, nrow, H, d.rms_eps, m->xn, st));
   }
+  trace_mark(m, "lm_head");
   if (logits) {
     Matrices lm{};
     lm.w[0] = d.lm_head;
     const int idx0[1] = {0};
     const int vrows[1] = {d.vocab};
-    SUB_TRY(launch_matmul(mm_args(xin, nrow, H, lm, idx0, 1, vrows, logits, d.vocab), false,
-                          EPI_F32, st));
+    GemvArgs la = mm_args(xin, nrow, H, lm, idx0, 1, vrows, logits, d.vocab, m);
+    la.xscale = r_attn ? r_attn + first : nullptr;
+    SUB_TRY(launch_matmul(la, false, EPI_F32, st));
   }
+  trace_mark(m, "end");
   return SUB_OK;
 }
 
@@ -517,8 +593,14 @@ extern "C" int32_t sub_model_create(const sub_model_desc* desc, sub_model** out)
   CREATE_TRY(dalloc_t(m, &m->act, R * F));
   CREATE_TRY(dalloc_t(m, &m->logits, (size_t)m->logit_rows * d.vocab));
   CREATE_TRY(dalloc_t(m, &m->rows_tok, R));
+  m->split_cap = (size_t)1 << 21;            // 8 MB of partial sums
+  m->split_cnt_cap = 8192;
+  CREATE_TRY(dalloc_t(m, &m->split_part, m->split_cap));
+  CREATE_TRY(dalloc_t(m, &m->split_cnt, m->split_cnt_cap));
+  CREATE_CUDA(cudaMemset(m->split_cnt, 0, m->split_cnt_cap * 4));
   m->norm_parts = (H / 16 + 1) * 16;
   CREATE_TRY(dalloc_t(m, &m->norm_partial, m->norm_parts));
+  CREATE_TRY(dalloc_t(m, &m->rvec, 32));
   CREATE_TRY(dalloc_t(m, &m->norm_counters, 4));
   CREATE_CUDA(cudaMemset(m->norm_counters, 0, 16));
 
@@ -652,6 +734,7 @@ extern "C" int32_t sub_model_forward(sub_model* m, int32_t which, const int32_t*
   if (target) SUB_TRY(begin_target_pass(m));
   SUB_TRY(forward(m, !target, r, logits, false));
   if (target) SUB_TRY(end_target_pass(m));
+  trace_flush(m);
   SUB_CUDA_TRY(cudaEventRecord(m->ev_t1, m->s_main));
   SUB_CUDA_TRY(cudaStreamWaitEvent(user, m->ev_t1, 0));
   return SUB_OK;

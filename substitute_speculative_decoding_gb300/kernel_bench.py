@@ -10,6 +10,7 @@ than the 129 MB L2):
   attn_draft  8 tree queries, 28/4 heads, d 128, 640 committed keys
   attn_verify 385 tree queries, same heads and keys
   gemm_bf16   bf16 weights 18944x3584, M = 385 (a verify FFN matrix)
+  gemv_{bf16,w4}_{down,o}  down projection 3584x18944 / o projection 3584x3584, M = 8
   draft_level one draft forward of 8 tree nodes through the whole Qwen2.5-7B-shaped
               model (11 resident + 17 int4 layers, lm_head), inside the NVTX range
               "draft_level" (the second of two runs)
@@ -99,7 +100,21 @@ def main():
     a = ap.parse_args()
     dev = "cuda"
     res = {"case": a.case}
-    if a.case in ("gemv_bf16", "gemm_bf16"):
+    if a.case in ("gemv_bf16_down", "gemv_bf16_o", "gemv_w4_down", "gemv_w4_o"):
+        n, k = (3584, 18944) if a.case.endswith("down") else (3584, 3584)
+        reps = 4
+        x = torch.randn(8, k, device=dev).to(torch.bfloat16)
+        y = torch.empty(8, n, device=dev, dtype=torch.bfloat16)
+        if "w4" in a.case:
+            packs = [synthetic.random_w4(n, k, s, dev) for s in range(reps)]
+            ms = _time(lambda i: sub.w4_gemm(x, *packs[i % reps], n, k, out=y), a.iters)
+            byt = n * (k // 64) * 36 + 8 * (n + k) * 2
+        else:
+            ws = [synthetic.randn_bf16((n, k), s, 0.02, dev) for s in range(reps)]
+            ms = _time(lambda i: sub.bf16_gemm(x, ws[i % reps], out=y), a.iters)
+            byt = n * k * 2 + 8 * (n + k) * 2
+        res.update(ms=ms, gbs=byt / ms / 1e6)
+    elif a.case in ("gemv_bf16", "gemm_bf16"):
         m = 8 if a.case == "gemv_bf16" else 385
         ws = [synthetic.randn_bf16((18944, 3584), s, 0.02, dev) for s in range(4)]
         x = torch.randn(m, 3584, device=dev).to(torch.bfloat16)

@@ -128,10 +128,13 @@ def test_graph_and_eager_agree(tiny):
 def test_spec_matches_plain_on_gpu(tiny):
     plain, _ = tiny["model"].generate(tiny["prompt"], 64, 0, 1)
     spec, st = tiny["model"].generate(tiny["prompt"], 64, 8, 2)
-    # both are the target's choices; they agree up to near-ties of the logits
-    r = _check_lossless(tiny, spec)
-    if not r["near_tie"]:
-        assert torch.equal(plain, spec)
+    # both are the target's choices: each passes the teacher-forced check, and
+    # the two agree token for token up to the first near-tie that either took
+    # the other way (past it the contexts differ)
+    rp = _check_lossless(tiny, plain)
+    rs = _check_lossless(tiny, spec)
+    cut = min(rp["near_tie"][:1] + rs["near_tie"][:1] + [len(plain)])
+    assert torch.equal(plain[:cut], spec[:cut]), (cut, rp, rs)
 
 
 def test_all_resident_chain_accepts_nearly_everything(sub):
