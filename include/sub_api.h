@@ -158,6 +158,25 @@ int32_t sub_verify_accept(const float* logits, const sub_tree* tree, int32_t n_n
                           int32_t* accepted_slots, int32_t* n_accepted, int32_t* bonus_token,
                           int32_t* choice, void* stream);
 
+/* sub_verify_accept without any device allocation: the same operation and
+ * arguments, with its per-call scratch (partial argmax keys, the ticket
+ * counter and, when choice == NULL, the choice array) taken from one fixed
+ * array of device memory that the library holds for each device
+ * (SUB_ACCEPT_STATIC_BYTES).  The pages have no counterpart: this is a
+ * library convenience for callers that must not allocate inside the decode
+ * loop.  Requirement: n_nodes * chunks * 8 + 64 (+ n_nodes * 4 without
+ * choice) <= SUB_ACCEPT_STATIC_BYTES, where chunks = the vocabulary chunks
+ * per node (at most ceil(304 / n_nodes)); larger calls return SUB_EINVAL.
+ * The first call on a device looks the array up (cudaGetSymbolAddress) and
+ * must come before any stream capture on that device.  The array is shared:
+ * calls on one device must be ordered (one stream, or joined by events);
+ * two calls in flight at once race on it. */
+#define SUB_ACCEPT_STATIC_BYTES (256 * 1024)
+int32_t sub_verify_accept_static(const float* logits, const sub_tree* tree, int32_t n_nodes,
+                                 int64_t V, int32_t mode, float temperature, uint64_t seed,
+                                 int64_t root_pos, int32_t* accepted_slots, int32_t* n_accepted,
+                                 int32_t* bonus_token, int32_t* choice, void* stream);
+
 /* Commit the accepted path: for every layer and KV head, copy K,V of tree
  * slot accepted_slots[j-1] (at position root_pos + slot) to position
  * root_pos + j, j = 1..*n_accepted (read on the device).  The root stays at

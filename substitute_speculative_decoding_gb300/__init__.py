@@ -97,6 +97,9 @@ _tree_attn = _decl("sub_tree_attn", [_vp, _i32, _i32, C.POINTER(KVCache), _i32, 
 _draft_expand = _decl("sub_draft_expand", [_vp, _i64, _f32, C.POINTER(Tree), _i32, _vp])
 _verify_accept = _decl("sub_verify_accept", [_vp, C.POINTER(Tree), _i32, _i64, _i32, _f32, _u64,
                                              _i64, _vp, _vp, _vp, _vp, _vp])
+_verify_accept_static = _decl("sub_verify_accept_static",
+                              [_vp, C.POINTER(Tree), _i32, _i64, _i32, _f32, _u64, _i64, _vp, _vp,
+                               _vp, _vp, _vp])
 _kv_compact = _decl("sub_kv_compact", [C.POINTER(KVCache), _i64, _vp, _vp, _i32, _vp])
 _model_create = _decl("sub_model_create", [C.POINTER(ModelDesc), C.POINTER(_vp)])
 _model_destroy = _decl("sub_model_destroy", [_vp])
@@ -114,6 +117,7 @@ _cycle_info = _decl("sub_cycle_info", [_vp, C.POINTER(DecodeCfg), C.POINTER(_i64
 
 EXPORTED = ["sub_last_error", "sub_version", "sub_w4_pack", "sub_w4_dequant", "sub_w4_gemm",
             "sub_bf16_gemm", "sub_tree_attn", "sub_draft_expand", "sub_verify_accept",
+            "sub_verify_accept_static",
             "sub_kv_compact", "sub_model_create", "sub_model_destroy", "sub_model_memory",
             "sub_model_forward", "sub_model_kv", "sub_generate", "sub_prefill",
             "sub_decode_cycles", "sub_decode_read", "sub_cycle_info"]
@@ -212,16 +216,34 @@ def draft_expand(logits, temperature: float, tree: DeviceTree, level: int, strea
 
 
 def verify_accept(logits, tree: DeviceTree, n_nodes: int, mode=0, temperature=1.0, seed=0,
-                  root_pos=0, stream=None):
-    """Returns device tensors (accepted slots [D], n_accepted [1], bonus [1], choice [n])."""
+                  root_pos=0, stream=None, out=None, with_choice=True):
+    """Returns device tensors (accepted slots [D], n_accepted [1], bonus [1],
+    choice [n] or None).  `out` reuses those four tensors."""
+    return _accept(_verify_accept, logits, tree, n_nodes, mode, temperature, seed, root_pos,
+                   stream, out, with_choice)
+
+
+def verify_accept_static(logits, tree: DeviceTree, n_nodes: int, mode=0, temperature=1.0,
+                         seed=0, root_pos=0, stream=None, out=None, with_choice=True):
+    """verify_accept on the library's fixed per-device scratch (no device
+    allocation inside the call; calls on one device must be ordered)."""
+    return _accept(_verify_accept_static, logits, tree, n_nodes, mode, temperature, seed,
+                   root_pos, stream, out, with_choice)
+
+
+def _accept(fn, logits, tree, n_nodes, mode, temperature, seed, root_pos, stream, out,
+            with_choice):
     dev = logits.device
-    acc = torch.zeros(max(tree.depth_max, 1), dtype=torch.int32, device=dev)
-    na = torch.zeros(1, dtype=torch.int32, device=dev)
-    bonus = torch.zeros(1, dtype=torch.int32, device=dev)
-    choice = torch.zeros(n_nodes, dtype=torch.int32, device=dev)
+    if out is None:
+        out = (torch.zeros(max(tree.depth_max, 1), dtype=torch.int32, device=dev),
+               torch.zeros(1, dtype=torch.int32, device=dev),
+               torch.zeros(1, dtype=torch.int32, device=dev),
+               torch.zeros(n_nodes, dtype=torch.int32, device=dev) if with_choice else None)
+    acc, na, bonus, choice = out
     t = tree.struct()
-    _check(_verify_accept(_p(logits), C.byref(t), n_nodes, logits.shape[1], mode, temperature,
-                          seed, root_pos, _p(acc), _p(na), _p(bonus), _p(choice), _stream(stream)))
+    _check(fn(_p(logits), C.byref(t), n_nodes, logits.shape[1], mode, temperature, seed, root_pos,
+              _p(acc), _p(na), _p(bonus), _p(choice),
+              _stream(stream)))
     return acc, na, bonus, choice
 
 

@@ -176,38 +176,89 @@ extern "C" int32_t sub_draft_expand(const float* logits, int64_t V, float temper
   return launch_expand(a, st);
 }
 
+static int32_t accept_args(const float* logits, const sub_tree* tree, int32_t n_nodes, int64_t V,
+                           int32_t mode, float temperature, uint64_t seed, int64_t root_pos,
+                           int32_t* accepted_slots, int32_t* n_accepted, int32_t* bonus_token,
+                           AcceptArgs* a) {
+  SUB_CHECK_ARG(logits && tree && accepted_slots && n_accepted && bonus_token, "null pointer");
+  SUB_CHECK_ARG(n_nodes >= 1 && n_nodes <= 1 + tree->max_depth * tree->width,
+                "n_nodes out of range");
+  SUB_CHECK_ARG(root_pos >= 0, "root_pos must be >= 0");
+  *a = AcceptArgs{};
+  a->logits = logits;
+  a->V = V;
+  a->tree = *tree;
+  a->n_nodes = n_nodes;
+  a->mode = mode;
+  a->temp = temperature;
+  a->seed = seed;
+  a->root_pos = root_pos;
+  a->n_chunks = accept_pick_chunks(n_nodes, V);
+  a->accepted = accepted_slots;
+  a->n_accepted = n_accepted;
+  a->bonus = bonus_token;
+  return SUB_OK;
+}
+
+// Scratch layout of one accept call: part keys, then the counter (64 bytes),
+// then the choice array when the caller gives none.
+static size_t accept_scratch_bytes(const AcceptArgs& a, bool own_choice) {
+  return (size_t)a.n_nodes * a.n_chunks * 8 + 64 + (own_choice ? (size_t)a.n_nodes * 4 : 0);
+}
+static int32_t accept_on(AcceptArgs& a, void* scratch, int32_t* choice, cudaStream_t st) {
+  const size_t key_bytes = (size_t)a.n_nodes * a.n_chunks * 8;
+  a.part_key = reinterpret_cast<unsigned long long*>(scratch);
+  a.counter = reinterpret_cast<unsigned int*>(reinterpret_cast<char*>(scratch) + key_bytes);
+  a.choice = choice ? choice
+                    : reinterpret_cast<int32_t*>(reinterpret_cast<char*>(scratch) + key_bytes + 64);
+  SUB_CUDA_TRY(cudaMemsetAsync(a.counter, 0, sizeof(unsigned int), st));
+  return launch_accept(a, st);
+}
+
 extern "C" int32_t sub_verify_accept(const float* logits, const sub_tree* tree, int32_t n_nodes,
                                      int64_t V, int32_t mode, float temperature, uint64_t seed,
                                      int64_t root_pos, int32_t* accepted_slots,
                                      int32_t* n_accepted, int32_t* bonus_token, int32_t* choice,
                                      void* stream) {
-  SUB_CHECK_ARG(logits && tree && accepted_slots && n_accepted && bonus_token, "null pointer");
-  SUB_CHECK_ARG(n_nodes >= 1 && n_nodes <= 1 + tree->max_depth * tree->width,
-                "n_nodes out of range");
-  SUB_CHECK_ARG(root_pos >= 0, "root_pos must be >= 0");
-  AcceptArgs a{};
-  a.logits = logits;
-  a.V = V;
-  a.tree = *tree;
-  a.n_nodes = n_nodes;
-  a.mode = mode;
-  a.temp = temperature;
-  a.seed = seed;
-  a.root_pos = root_pos;
-  a.n_chunks = accept_pick_chunks(n_nodes, V);
-  a.accepted = accepted_slots;
-  a.n_accepted = n_accepted;
-  a.bonus = bonus_token;
+  AcceptArgs a;
+  SUB_TRY(accept_args(logits, tree, n_nodes, V, mode, temperature, seed, root_pos, accepted_slots,
+                      n_accepted, bonus_token, &a));
   const cudaStream_t st = as_stream(stream);
   StreamScratch scratch(st);
-  const size_t key_bytes = (size_t)n_nodes * a.n_chunks * 8;
-  SUB_TRY(scratch.alloc(key_bytes + 64 + (choice ? 0 : (size_t)n_nodes * 4)));
-  a.part_key = reinterpret_cast<unsigned long long*>(scratch.p);
-  a.counter = reinterpret_cast<unsigned int*>(reinterpret_cast<char*>(scratch.p) + key_bytes);
-  a.choice = choice ? choice
-                    : reinterpret_cast<int32_t*>(reinterpret_cast<char*>(scratch.p) + key_bytes + 64);
-  SUB_CUDA_TRY(cudaMemsetAsync(a.counter, 0, sizeof(unsigned int), st));
-  return launch_accept(a, st);
+  SUB_TRY(scratch.alloc(accept_scratch_bytes(a, !choice)));
+  return accept_on(a, scratch.p, choice, st);
+}
+
+// The fixed scratch of sub_verify_accept_static: one array per device (each
+// device's copy of the module has its own), looked up once per device.
+static __device__ __align__(256) unsigned char g_accept_scratch[SUB_ACCEPT_STATIC_BYTES];
+
+static int32_t accept_static_base(void** out) {
+  constexpr int MAX_DEV = 64;
+  static std::mutex mu;
+  static void* base[MAX_DEV] = {};
+  int dev = 0;
+  SUB_CUDA_TRY(cudaGetDevice(&dev));
+  SUB_CHECK_ARG(dev >= 0 && dev < MAX_DEV, "device ordinal beyond the static scratch table");
+  std::lock_guard<std::mutex> lock(mu);
+  if (!base[dev]) SUB_CUDA_TRY(cudaGetSymbolAddress(&base[dev], g_accept_scratch));
+  *out = base[dev];
+  return SUB_OK;
+}
+
+extern "C" int32_t sub_verify_accept_static(const float* logits, const sub_tree* tree,
+                                            int32_t n_nodes, int64_t V, int32_t mode,
+                                            float temperature, uint64_t seed, int64_t root_pos,
+                                            int32_t* accepted_slots, int32_t* n_accepted,
+                                            int32_t* bonus_token, int32_t* choice, void* stream) {
+  AcceptArgs a;
+  SUB_TRY(accept_args(logits, tree, n_nodes, V, mode, temperature, seed, root_pos, accepted_slots,
+                      n_accepted, bonus_token, &a));
+  SUB_CHECK_ARG(accept_scratch_bytes(a, !choice) <= (size_t)SUB_ACCEPT_STATIC_BYTES,
+                "n_nodes too large for the static accept scratch");
+  void* base = nullptr;
+  SUB_TRY(accept_static_base(&base));
+  return accept_on(a, base, choice, as_stream(stream));
 }
 
 extern "C" int32_t sub_kv_compact(const sub_kv_cache* kv, int64_t root_pos,
