@@ -1,5 +1,6 @@
 // C ABI entry points for the kernels (the model and generate calls live in
 // model.cu): argument checks, temporary scratch, launch.
+#include <algorithm>
 #include <cstdlib>
 #include <mutex>
 #include "attn.cuh"
@@ -79,11 +80,13 @@ static int32_t matmul_public(const sub_bf16* X, int64_t M, bool w4, const void* 
   a.ldy = (int)N;
   const cudaStream_t st = as_stream(stream);
   StreamScratch scratch(st);
+  // split scratch: partial sums of K splits (register-streamed kernel) or of
+  // blocks shared by several CTAs (TMA kernel), and one counter per row unit
   const int ks = M <= 16 ? gemv_ksplit(a, w4, EPI_BF16) : 1;
-  if (ks > 1) {
-    // room for the split of K over CTAs: ks splits of every 16-row unit
+  const size_t tma_floats = M <= 16 ? gemv_tma_scratch_floats(a, w4, EPI_BF16) : 0;
+  if (ks > 1 || tma_floats > 0) {
     const int units = (int)((N + 15) / 16);
-    a.split_cap = (size_t)units * ks * 4 * 128;
+    a.split_cap = std::max((size_t)units * ks * 4 * 128, tma_floats);
     a.split_cnt_cap = units;
     SUB_TRY(scratch.alloc(a.split_cap * 4 + (size_t)units * 4));
     a.split_part = reinterpret_cast<float*>(scratch.p);

@@ -560,6 +560,9 @@ int32_t launch_gemv(const GemvArgs& a, bool is_w4, int epi, cudaStream_t st) {
   if (epi == EPI_RESID && a.norm.xn)
     SUB_CHECK_ARG(a.norm.partial && a.norm.counter && a.norm.gain && a.norm.rvec && a.ldy == a.N,
                   "gemv: norm epilogue needs partial, counter, gain, rvec and ldy == N");
+  bool done = false;
+  SUB_TRY(launch_gemv_tma(a, is_w4, epi, st, &done));
+  if (done) return SUB_OK;
   return is_w4 ? launch_epi<true>(a, epi, st) : launch_epi<false>(a, epi, st);
 }
 

@@ -102,4 +102,18 @@ int gemv_grid(const GemvArgs& a, int epi);
 // Splits of K over CTAs the launch would use given room for them (1 = no split).
 int gemv_ksplit(const GemvArgs& a, bool is_w4, int epi);
 
+// TMA-streamed variant (gemv_tma.cu): one producer warp fills a shared-memory
+// ring by TMA, eight consumer warps (one 16-row tile each) multiply from it,
+// one CTA per SM with the (block, K-stage) units split evenly.  Launches and
+// sets *done when the shape and the split scratch allow it; otherwise leaves
+// *done false and launches nothing.  launch_gemv tries it first
+// (SUB_GEMV_TMA=0 turns it off).
+int32_t launch_gemv_tma(const GemvArgs& a, bool is_w4, int epi, cudaStream_t stream, bool* done);
+// Partial-sum floats the TMA variant needs in split_part (0: it would not run).
+size_t gemv_tma_scratch_floats(const GemvArgs& a, bool is_w4, int epi);
+// Kernel attributes of the TMA variant; call before any stream capture.
+int32_t gemv_init();
+// Pipeline waits that ran out since load (each one is a bug; never expected).
+int32_t gemv_tma_timeouts(unsigned int* out);
+
 }  // namespace sub
