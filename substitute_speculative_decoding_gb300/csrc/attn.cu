@@ -384,26 +384,49 @@ static_assert(ROWS * (128 + 4) * 4 + 2 * ROWS * 4 + ROWS * ATTN_MAX_SPLIT * 4 <=
 static_assert(ROWS * (64 + 4) * 4 + 2 * ROWS * 4 + ROWS * ATTN_MAX_SPLIT * 4 <= 4 * KT * 64 * 2,
               "the cluster merge buffers must fit in the K/V tiles (head_dim 64)");
 
+static int g_max_split = 8;   // largest cluster the device runs (set by attn_init)
+
 int attn_pick_splits(const AttnArgs& a, int n_keys_hint) {
+  if (attn_init() != SUB_OK) return 1;
   const int G = a.n_heads_q / a.n_heads_kv;
   const int blocks = (a.n_q * G + ROWS - 1) / ROWS * a.n_heads_kv;
   const int tiles = (n_keys_hint + KT - 1) / KT;
   int s = (2 * 152 + blocks - 1) / blocks;
-  s = std::max(1, std::min(s, std::min(tiles, ATTN_MAX_SPLIT)));
+  s = std::max(1, std::min(s, std::min(tiles, g_max_split)));
   return s;
 }
 
-// Opt the kernels into the largest dynamic shared memory once per process
-// (before any stream capture: model creation calls this).
+// Opt the kernels into the largest dynamic shared memory and into 16-CTA
+// clusters once per process (before any stream capture: model creation
+// calls this), and find whether the device runs clusters of 16.
 int32_t attn_init() {
   static std::once_flag once;
   static cudaError_t err = cudaSuccess;
   std::call_once(once, [] {
-    err = cudaFuncSetAttribute(tree_attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               ATTN_MAX_SMEM);
-    if (err == cudaSuccess)
-      err = cudaFuncSetAttribute(tree_attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 ATTN_MAX_SMEM);
+    const void* ks[2] = {(const void*)tree_attn_kernel<128>, (const void*)tree_attn_kernel<64>};
+    for (const void* k : ks) {
+      if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, ATTN_MAX_SMEM);
+      if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    }
+    if (err != cudaSuccess) return;
+    // can a 16-CTA cluster of the largest draft-shaped launch be resident?
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, 16);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = ROWS * 128 * 2 + 4 * KT * 128 * 2 + 4096;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 1;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 16;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, tree_attn_kernel<128>, &cfg) == cudaSuccess && n > 0)
+      g_max_split = 16;
+    cudaGetLastError();   // a refused query leaves the portable size
   });
   if (err != cudaSuccess) return fail(SUB_ECUDA, std::string("attn_init: ") + cudaGetErrorString(err));
   return SUB_OK;
@@ -414,7 +437,8 @@ int32_t launch_tree_attn(const AttnArgs& a, int n_split, cudaStream_t st) {
   SUB_CHECK_ARG(a.n_heads_kv >= 1 && a.n_heads_q % a.n_heads_kv == 0, "attn: Hq % Hkv != 0");
   SUB_CHECK_ARG(a.page_size % 16 == 0 && a.page_size > 0, "attn: page_size % 16 != 0");
   SUB_CHECK_ARG(a.n_slots >= 0 && a.n_slots <= 16384, "attn: n_slots out of range");
-  SUB_CHECK_ARG(n_split >= 1 && n_split <= ATTN_MAX_SPLIT, "attn: bad split count");
+  SUB_TRY(attn_init());
+  SUB_CHECK_ARG(n_split >= 1 && n_split <= g_max_split, "attn: bad split count");
   if (a.n_q == 0) return SUB_OK;
   const int G = a.n_heads_q / a.n_heads_kv;
   const int smem = attn_smem_bytes(a);

@@ -28,7 +28,9 @@ struct AttnArgs {
 };
 
 constexpr int ATTN_MAX_SMEM = 200 * 1024;
-constexpr int ATTN_MAX_SPLIT = 8;   // key splits = CTAs of one (portable) cluster
+// Key splits = CTAs of one thread-block cluster: up to 16 where the device
+// runs 16-CTA clusters (a non-portable size), else the portable 8.
+constexpr int ATTN_MAX_SPLIT = 16;
 int32_t attn_init();
 int attn_smem_bytes(const AttnArgs& a);
 int attn_pick_splits(const AttnArgs& a, int n_keys_hint);
