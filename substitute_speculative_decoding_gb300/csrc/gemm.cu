@@ -325,6 +325,9 @@ int32_t launch_gemm(const GemvArgs& a, bool is_w4, int epi, cudaStream_t st) {
   SUB_CHECK_ARG((int64_t)a.M < (1ll << 20), "gemm: M too large");
   SUB_CHECK_ARG(!a.xscale && !(epi == EPI_RESID && a.norm.xn),
                 "gemm: factored-norm inputs and outputs are GEMV-only");
+  bool done = false;
+  SUB_TRY(launch_gemm_tc(a, is_w4, epi, st, &done));
+  if (done) return SUB_OK;
   return is_w4 ? gemm_epi<true>(a, epi, st) : gemm_epi<false>(a, epi, st);
 }
 

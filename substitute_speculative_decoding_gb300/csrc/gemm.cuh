@@ -12,6 +12,15 @@ int32_t gemm_init();
 // Same argument block and epilogues as the GEMV (GemvArgs); M is unbounded.
 int32_t launch_gemm(const GemvArgs& a, bool is_w4, int epi, cudaStream_t stream);
 
+// Tensor-core (tcgen05, TMEM accumulator, TMA-fed) variant for bf16 weights
+// and the bf16/f32/residual/SiLU-GLU epilogues (gemm_tc.cu).  Launches and sets
+// *done when the product suits it; launch_gemm tries it first (SUB_GEMM_TC=0
+// turns it off).  Split-K partials use split_part / split_cnt.
+int32_t launch_gemm_tc(const GemvArgs& a, bool is_w4, int epi, cudaStream_t stream, bool* done);
+int32_t gemm_tc_init();
+size_t gemm_tc_scratch_floats(const GemvArgs& a, bool is_w4, int epi);
+int32_t gemm_tc_timeouts(unsigned int* out);
+
 // Dispatch on M: GEMV for M <= 16, tiled GEMM otherwise.
 inline int32_t launch_matmul(const GemvArgs& a, bool is_w4, int epi, cudaStream_t stream) {
   return a.M <= 16 ? launch_gemv(a, is_w4, epi, stream) : launch_gemm(a, is_w4, epi, stream);

@@ -1,0 +1,513 @@
+// Tree-shaped products (M > 16 activation rows: the verify pass over all tree
+// nodes, the prompt prefill) on the 5th-generation tensor cores.
+//
+// Y[m, n] = sum_k X[m, k] W[n, k] with bf16 operands and fp32 accumulation,
+// computed transposed (swap-AB): the MMA's A operand is a 128-row tile of W
+// and its B operand a tile of up to 256 activation rows, so the accumulator
+// D[n, m] sits in tensor memory with one weight row per TMEM lane and the
+// tokens along the columns.  In the epilogue a warp reads 32 lanes (32
+// consecutive weight rows) of a token column, so its global stores of Y[m, n]
+// are coalesced.
+//
+// One CTA: 128 threads.  Warp 0 lane 0 streams K chunks of 64 columns (128
+// bytes per row, the TMA 128-byte swizzle atom) of both operands into an
+// S-stage shared-memory ring by TMA; warp 1 lane 0 issues tcgen05.mma
+// (kind::f16, M = 128, N = token tile, K = 16 per instruction) from the
+// stages and hands each stage back with tcgen05.commit to its empty
+// mbarrier; after the last chunk a final commit releases the four warps into
+// the epilogue, which reads TMEM with tcgen05.ld.  Long K with few weight
+// tiles splits over CTAs (grid.z); the last split of a tile adds the fp32
+// partials in split order.  Weight tiles never straddle a segment (q/k/v
+// stacked, or gate/up for SiLU-GLU: 64 gate rows + 64 up rows per tile).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <algorithm>
+#include <mutex>
+#include "gemm.cuh"
+
+namespace sub {
+
+namespace {
+
+constexpr int TC_THREADS = 128;
+constexpr int TC_BM = 128;                 // weight rows per tile (TMEM lanes)
+constexpr int TC_BK = 64;                  // K columns per stage (128 B per row)
+constexpr int TC_TN = 256;                 // token rows per tile (max MMA N)
+constexpr int A_BYTES = TC_BM * TC_BK * 2;     // 16 KB
+constexpr int B_BYTES = TC_TN * TC_BK * 2;     // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int TC_STAGES = 4;
+constexpr int TC_SMEM = 1024 + TC_STAGES * STAGE_BYTES + 256;   // + barriers, TMEM address
+constexpr int TMEM_COLS = 256;
+
+__device__ unsigned int g_tc_timeouts;   // waits that ran out (never expected)
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: a wait that runs out records itself and returns (wrong
+// numbers and a host-visible count rather than a hang).
+__device__ __forceinline__ void mbar_wait(uint32_t bar, uint32_t parity) {
+  for (uint32_t i = 0; i < (1u << 22); ++i)
+    if (mbar_try_wait(bar, parity)) return;
+  atomicAdd(&g_tc_timeouts, 1u);
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+// ---------------------------------------------------------------- tcgen05 --
+// Shared-memory matrix descriptor of a K-major operand in the 128-byte
+// swizzled layout TMA writes (8-row groups of 1024 bytes): start address,
+// leading byte offset (unused by swizzled K-major: 16), stride byte offset
+// 1024 between 8-row groups, the descriptor version bit, swizzle mode 2.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(16u >> 4) << 16;
+  d |= (uint64_t)(1024u >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, M = 128, N = n.
+__device__ __forceinline__ uint32_t idesc_bf16(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(TC_BM >> 4) << 24);
+}
+__device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// 32 lanes x 16 consecutive columns of fp32 from TMEM, one lane per thread.
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+}  // namespace
+
+struct alignas(64) TcMaps {
+  CUtensorMap w[3];   // weight segments [rows, K] bf16, box 64 x (128 or 64 rows)
+  CUtensorMap x;      // activations [M, K] bf16, box 64 x token-tile rows
+};
+
+struct TcPlan {
+  int blk_end[3];     // cumulative weight tiles per segment
+  int n_maps;
+  int chunks;         // K chunks of 64 columns
+  int per_split;      // chunks per split of K
+  int xrows;          // token rows of the activation box
+};
+
+template <int EPI>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+gemm_tc_kernel(const __grid_constant__ TcMaps maps, const GemvArgs a, const TcPlan pl) {
+  constexpr bool GLU = EPI == EPI_GLU;
+  constexpr int HALF = GLU ? TC_BM / 2 : TC_BM;   // rows of one segment in a tile
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t* const base_ptr = smem_raw + (base - smem_u32(smem_raw));
+  const uint32_t bars = base + TC_STAGES * STAGE_BYTES;   // full[S], empty[S], done
+  auto full_bar = [&](int s) { return bars + 8u * s; };
+  auto empty_bar = [&](int s) { return bars + 8u * (TC_STAGES + s); };
+  const uint32_t done_bar = bars + 8u * (2 * TC_STAGES);
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + TC_STAGES * STAGE_BYTES + 128);
+  float* const xch = reinterpret_cast<float*>(base_ptr);   // epilogue exchange (reuses stage 0)
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tok0 = blockIdx.x * TC_TN;
+  const int tn = min(TC_TN, ((a.M - tok0) + 15) / 16 * 16);   // MMA N (multiple of 16)
+  const int tile = blockIdx.y;
+  int seg = 0;
+  while (seg < 2 && tile >= pl.blk_end[seg]) ++seg;
+  const int r0 = (tile - (seg ? pl.blk_end[seg - 1] : 0)) * HALF;   // first row in the segment
+  const int ks = gridDim.z, kz = blockIdx.z;
+  const int c0 = kz * pl.per_split, c1 = min(pl.chunks, c0 + pl.per_split);
+  const int nck = max(0, c1 - c0);
+
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (threadIdx.x == 32) {
+    for (int s = 0; s < TC_STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    mbar_init(done_bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // Warps 0 and 1 lend lane 0 to the producer and the MMA issuer; their other
+  // lanes wait at the warp barrier (not on the done barrier) so they never
+  // compete with the working lane's instruction stream.
+  if (warp == 0 && lane == 0) {
+    // ---------------------------------------------------------- producer
+    auto issue = [&](int i, bool weights, bool acts) {
+      const int s = i % TC_STAGES, kx = (c0 + i) * TC_BK;
+      const uint32_t st = base + s * STAGE_BYTES, fb = full_bar(s);
+      if (weights) {
+        mbar_expect_tx(fb, STAGE_BYTES);
+        for (int h = 0; h < (GLU ? 2 : 1); ++h)
+          tma_load_2d(st + h * HALF * 128, &maps.w[GLU ? h : seg], kx, r0, fb);
+      }
+      if (acts) {
+        // the activation box always moves TC_TN rows' worth of bytes: rows past
+        // the tensor (and past the box) arrive as zeros
+        for (int y = 0; y < TC_TN; y += pl.xrows)
+          tma_load_2d(st + A_BYTES + y * 128, &maps.x, kx, tok0 + y, fb);
+      }
+    };
+    const int npre = min(TC_STAGES, nck);
+    for (int i = 0; i < npre; ++i) issue(i, true, false);   // weights before the wait
+    pdl_wait();
+    for (int i = 0; i < npre; ++i) issue(i, false, true);
+    for (int i = npre; i < nck; ++i) {
+      mbar_wait(empty_bar(i % TC_STAGES), ((i / TC_STAGES) - 1) & 1);
+      issue(i, true, true);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------------------------------------------------- MMA issuer
+    const uint32_t idesc = idesc_bf16(tn);
+    for (int i = 0; i < nck; ++i) {
+      const int s = i % TC_STAGES;
+      mbar_wait(full_bar(s), (i / TC_STAGES) & 1);
+      tc_fence_after();
+      const uint32_t st = base + s * STAGE_BYTES;
+#pragma unroll
+      for (int kk = 0; kk < TC_BK / 16; ++kk)
+        tc_mma(tmem, smem_desc_sw128(st + kk * 32), smem_desc_sw128(st + A_BYTES + kk * 32), idesc,
+               (i > 0 || kk > 0) ? 1u : 0u);
+      tc_commit(empty_bar(s));   // the stage is free once these MMAs have read it
+    }
+    tc_commit(done_bar);
+  }
+  __syncwarp();
+  pdl_wait();   // every thread: the epilogue reads what earlier kernels wrote
+  pdl_trigger();
+
+  // ------------------------------------------------------------ epilogue
+  if (nck > 0) mbar_wait(done_bar, 0);
+  __syncwarp();
+  tc_fence_after();
+  const int lrow = warp * 32 + lane;                          // TMEM lane = row of the tile
+  const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
+  const int seg_rows = GLU ? a.N : a.seg_end[seg] - (seg ? a.seg_end[seg - 1] : 0);
+  const int seg_start = GLU ? 0 : (seg ? a.seg_end[seg - 1] : 0);
+  const int rs = r0 + (GLU ? (lrow & (HALF - 1)) : lrow);     // row within the segment
+  const bool row_ok = rs < seg_rows;
+  const int n_glob = seg_start + rs;
+
+  // split of K: park fp32 partials [tile][split][token][row], the last split sums
+  bool last = true;
+  float* part = nullptr;
+  if (ks > 1) {
+    const size_t tile_lin = (size_t)blockIdx.y * gridDim.x + blockIdx.x;
+    part = a.split_part + tile_lin * ks * (size_t)(TC_TN * TC_BM);
+    float* mine = part + (size_t)kz * (TC_TN * TC_BM);
+    for (int cb = 0; cb < tn; cb += 16) {
+      float v[16];
+      if (nck > 0) tc_ld16(taddr + cb, v);
+      else
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = 0.f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) __stcg(mine + (size_t)(cb + j) * TC_BM + lrow, v[j]);
+    }
+    __shared__ unsigned int s_last;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      s_last = (atomicAdd(a.split_cnt + tile_lin, 1u) == (unsigned)ks - 1) ? 1u : 0u;
+      __threadfence();
+    }
+    __syncthreads();
+    last = s_last != 0;
+    if (last && threadIdx.x == 0) a.split_cnt[tile_lin] = 0u;
+  }
+
+  if (last) {
+    for (int cb = 0; cb < tn; cb += 16) {
+      float v[16];
+      if (ks > 1) {
+        // splits in order; the 16 loads of one split are in flight together
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = 0.f;
+        for (int z = 0; z < ks; ++z) {
+          float p[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) p[j] = __ldcg(part + ((size_t)z * TC_TN + cb + j) * TC_BM + lrow);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] += p[j];
+        }
+      } else {
+        tc_ld16(taddr + cb, v);
+      }
+      if constexpr (GLU) {
+        // up rows (lanes 64..127) hand their values to the gate rows (lanes 0..63)
+        __syncthreads();
+        if (lrow >= HALF)
+#pragma unroll
+          for (int j = 0; j < 16; ++j) xch[j * HALF + (lrow - HALF)] = v[j];
+        __syncthreads();
+        if (lrow < HALF && row_ok) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int m = tok0 + cb + j;
+            if (m < a.M)
+              reinterpret_cast<__nv_bfloat16*>(a.Y)[(int64_t)m * a.ldy + rs] =
+                  __float2bfloat16_rn(silu_f(v[j]) * xch[j * HALF + lrow]);
+          }
+        }
+      } else if (row_ok) {
+        if constexpr (EPI == EPI_RESID) {
+          // all 16 old values first: a load after a store to Y would wait for it
+          float* const Y = reinterpret_cast<float*>(a.Y);
+          float y[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int m = tok0 + cb + j;
+            y[j] = m < a.M ? __ldcg(Y + (int64_t)m * a.ldy + n_glob) : 0.f;
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int m = tok0 + cb + j;
+            if (m < a.M) Y[(int64_t)m * a.ldy + n_glob] = y[j] + v[j];
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int m = tok0 + cb + j;
+            if (m >= a.M) continue;
+            const int64_t o = (int64_t)m * a.ldy + n_glob;
+            if constexpr (EPI == EPI_BF16) {
+              reinterpret_cast<__nv_bfloat16*>(a.Y)[o] = __float2bfloat16_rn(v[j]);
+            } else {
+              reinterpret_cast<float*>(a.Y)[o] = v[j];
+            }
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS)
+                 : "memory");
+}
+
+// ------------------------------------------------------------------- host --
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 tc_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 map over a row-major [rows, cols] array, 64-column (128-byte) boxes
+// with the 128-byte swizzle.
+bool tc_map(CUtensorMap* m, const void* ptr, int64_t cols, int64_t rows, int64_t stride_bytes,
+            int box_rows) {
+  auto fn = tc_encode_fn();
+  if (!fn || !aligned16(ptr) || stride_bytes % 16 || box_rows < 1 || box_rows > 256) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)stride_bytes};
+  const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int tc_sm_count() {
+  static int n = 0;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 152;
+  });
+  return n;
+}
+
+template <int EPI>
+int32_t tc_launch(const GemvArgs& a, const TcMaps& maps, const TcPlan& pl, dim3 grid,
+                  cudaStream_t st) {
+  SUB_TRY(gemm_tc_init());
+  SUB_CUDA_TRY(launch_k(gemm_tc_kernel<EPI>, grid, dim3(TC_THREADS), TC_SMEM, st, maps, a, pl));
+  return SUB_OK;
+}
+
+}  // namespace
+
+int32_t gemm_tc_init() {
+  static std::once_flag once;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    const void* ks[4] = {(const void*)gemm_tc_kernel<EPI_BF16>, (const void*)gemm_tc_kernel<EPI_F32>,
+                         (const void*)gemm_tc_kernel<EPI_RESID>, (const void*)gemm_tc_kernel<EPI_GLU>};
+    for (const void* k : ks)
+      if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+  });
+  if (err != cudaSuccess) return fail(SUB_ECUDA, std::string("gemm_tc_init: ") + cudaGetErrorString(err));
+  return SUB_OK;
+}
+
+// Tile plan: weight tiles per segment, token tiles, splits of K.  False when
+// the product is not for this kernel (int4 weights, the q/k/v epilogue,
+// fused-norm outputs, a segment count or alignment it does not handle).
+static bool tc_plan(const GemvArgs& a, bool w4, int epi, TcPlan* pl, dim3* grid, size_t* scratch) {
+  static const bool on = env_flag("SUB_GEMM_TC", true);
+  if (!on || w4 || epi == EPI_QKV || a.M <= 16 || a.xscale) return false;
+  if (epi == EPI_RESID && a.norm.xn) return false;
+  const bool glu = epi == EPI_GLU;
+  if (a.n_seg < 1 || a.n_seg > 3 || (glu && a.n_seg != 2)) return false;
+  if (a.K % 8 || a.ldx % 8) return false;
+  const int half = glu ? TC_BM / 2 : TC_BM;
+  int nb = 0;
+  for (int s = 0; s < 3; ++s) {
+    if (s < (glu ? 1 : a.n_seg)) {
+      const int rows = glu ? a.N : a.seg_end[s] - (s ? a.seg_end[s - 1] : 0);
+      nb += (rows + half - 1) / half;
+    }
+    pl->blk_end[s] = nb;
+  }
+  pl->n_maps = glu ? 2 : a.n_seg;
+  pl->chunks = (a.K + TC_BK - 1) / TC_BK;
+  // activation box height: a power of two from 16 to TC_TN, so whole boxes
+  // tile the TC_TN rows of a stage exactly
+  pl->xrows = 16;
+  while (pl->xrows < TC_TN && pl->xrows < a.M) pl->xrows *= 2;
+  const int tok_tiles = (a.M + TC_TN - 1) / TC_TN;
+  // split K only when the tiles alone would leave most SMs idle (the tensor
+  // cores finish a tile's K quickly; splits cost a round of fp32 partials)
+  const int ctas = nb * tok_tiles;
+  int ks = 1;
+  if (4 * ctas < tc_sm_count())
+    ks = std::max(1, std::min((tc_sm_count() + ctas - 1) / ctas, std::min(8, pl->chunks / 16)));
+  size_t need = ks > 1 ? (size_t)ctas * ks * TC_TN * TC_BM : 0;
+  while (ks > 1 && (need > a.split_cap || ctas > a.split_cnt_cap || !a.split_part || !a.split_cnt)) {
+    --ks;
+    need = ks > 1 ? (size_t)ctas * ks * TC_TN * TC_BM : 0;
+  }
+  pl->per_split = (pl->chunks + ks - 1) / ks;
+  ks = (pl->chunks + pl->per_split - 1) / pl->per_split;
+  need = ks > 1 ? (size_t)ctas * ks * TC_TN * TC_BM : 0;
+  *grid = dim3(tok_tiles, nb, ks);
+  *scratch = need;
+  return true;
+}
+
+size_t gemm_tc_scratch_floats(const GemvArgs& a, bool w4, int epi) {
+  GemvArgs t = a;
+  t.split_part = reinterpret_cast<float*>(16);
+  t.split_cnt = reinterpret_cast<unsigned int*>(16);
+  t.split_cap = ~(size_t)0 >> 1;
+  t.split_cnt_cap = 1 << 30;
+  TcPlan pl{};
+  dim3 grid;
+  size_t need = 0;
+  return tc_plan(t, w4, epi, &pl, &grid, &need) ? need : 0;
+}
+
+int32_t launch_gemm_tc(const GemvArgs& a, bool w4, int epi, cudaStream_t st, bool* done) {
+  *done = false;
+  TcPlan pl{};
+  dim3 grid;
+  size_t need = 0;
+  if (!tc_plan(a, w4, epi, &pl, &grid, &need)) return SUB_OK;
+  const bool glu = epi == EPI_GLU;
+  TcMaps maps;
+  memset(&maps, 0, sizeof(maps));
+  for (int s = 0; s < pl.n_maps; ++s) {
+    const int64_t rows = glu ? a.N : a.seg_end[s] - (s ? a.seg_end[s - 1] : 0);
+    if (!tc_map(&maps.w[s], a.W[s], a.K, rows, (int64_t)a.K * 2, glu ? TC_BM / 2 : TC_BM))
+      return SUB_OK;
+  }
+  if (!tc_map(&maps.x, a.X, a.K, a.M, (int64_t)a.ldx * 2, pl.xrows)) return SUB_OK;
+  *done = true;
+  switch (epi) {
+    case EPI_BF16: return tc_launch<EPI_BF16>(a, maps, pl, grid, st);
+    case EPI_F32: return tc_launch<EPI_F32>(a, maps, pl, grid, st);
+    case EPI_RESID: return tc_launch<EPI_RESID>(a, maps, pl, grid, st);
+    case EPI_GLU: return tc_launch<EPI_GLU>(a, maps, pl, grid, st);
+  }
+  *done = false;
+  return fail(SUB_EINVAL, "bad gemm epilogue");
+}
+
+int32_t gemm_tc_timeouts(unsigned int* out) {
+  SUB_CUDA_TRY(cudaMemcpyFromSymbol(out, g_tc_timeouts, sizeof(unsigned int)));
+  return SUB_OK;
+}
+
+}  // namespace sub

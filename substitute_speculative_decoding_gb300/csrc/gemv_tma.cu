@@ -512,6 +512,22 @@ gemv_tma_kernel(const __grid_constant__ TmaMaps maps, const GemvArgs a, const Tm
       consumer_sync();   // the exchange buffer is free again
     } else {
       float ss[MT][2] = {};
+      // residual: every old value of the lane first (a load after a store to Y
+      // would wait for the store)
+      float yold[MT][4];
+      if constexpr (EPI == EPI_RESID) {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int tok = token_of(mt, j);
+            const int rs = r0 + ((j & 2) ? hi : lo) + pg;
+            yold[mt][j] = (tok < a.M && rs < seg_rows)
+                              ? __ldcg(reinterpret_cast<const float*>(a.Y) + (int64_t)tok * a.ldy +
+                                       seg_start + rs)
+                              : 0.f;
+          }
+      }
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -527,9 +543,8 @@ gemv_tma_kernel(const __grid_constant__ TmaMaps maps, const GemvArgs a, const Tm
           } else if constexpr (EPI == EPI_F32) {
             reinterpret_cast<float*>(a.Y)[o] = v;
           } else {   // EPI_RESID
-            float* yp = reinterpret_cast<float*>(a.Y) + o;
-            const float xnew = *yp + v;
-            *yp = xnew;
+            const float xnew = yold[mt][j] + v;
+            reinterpret_cast<float*>(a.Y)[o] = xnew;
             if (a.norm.xn) {
               a.norm.xn[o] = f32_to_bf16_bits(xnew * bf16_bits_to_f32(a.norm.gain[row]));
               ss[mt][j & 1] = fmaf(xnew, xnew, ss[mt][j & 1]);

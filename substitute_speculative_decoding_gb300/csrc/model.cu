@@ -538,6 +538,7 @@ extern "C" int32_t sub_model_create(const sub_model_desc* desc, sub_model** out)
   }
   CREATE_TRY(gemm_init());
   CREATE_TRY(gemv_init());
+  CREATE_TRY(gemm_tc_init());
   CREATE_TRY(attn_init());
   CREATE_CUDA(cudaStreamCreateWithFlags(&m->s_main, cudaStreamNonBlocking));
   CREATE_CUDA(cudaStreamCreateWithFlags(&m->s_copy, cudaStreamNonBlocking));
@@ -594,7 +595,7 @@ extern "C" int32_t sub_model_create(const sub_model_desc* desc, sub_model** out)
   CREATE_TRY(dalloc_t(m, &m->act, R * F));
   CREATE_TRY(dalloc_t(m, &m->logits, (size_t)m->logit_rows * d.vocab));
   CREATE_TRY(dalloc_t(m, &m->rows_tok, R));
-  m->split_cap = (size_t)1 << 23;            // 32 MB of partial sums
+  m->split_cap = (size_t)1 << 24;            // 64 MB of partial sums
   m->split_cnt_cap = 8192;
   CREATE_TRY(dalloc_t(m, &m->split_part, m->split_cap));
   CREATE_TRY(dalloc_t(m, &m->split_cnt, m->split_cnt_cap));
