@@ -284,58 +284,70 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const GemvArgs a, const TcPl
   }
 
   if (last) {
-    for (int cb = 0; cb < tn; cb += 16) {
-      float v[16];
+    // 64 columns (tokens) per round: four TMEM loads, or four splits' worth of
+    // partial sums, and all their global loads in flight together
+    for (int cg = 0; cg < tn; cg += 64) {
+      const int ncol = min(64, tn - cg);   // a multiple of 16
+      float v[64];
       if (ks > 1) {
-        // splits in order; the 16 loads of one split are in flight together
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = 0.f;
+        for (int j = 0; j < 64; ++j) v[j] = 0.f;
         for (int z = 0; z < ks; ++z) {
-          float p[16];
+          float p[64];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) p[j] = __ldcg(part + ((size_t)z * TC_TN + cb + j) * TC_BM + lrow);
+          for (int j = 0; j < 64; ++j)
+            p[j] = j < ncol ? __ldcg(part + ((size_t)z * TC_TN + cg + j) * TC_BM + lrow) : 0.f;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] += p[j];
+          for (int j = 0; j < 64; ++j) v[j] += p[j];
         }
       } else {
-        tc_ld16(taddr + cb, v);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float t[16];
+          if (q * 16 < ncol) tc_ld16(taddr + cg + q * 16, t);
+          else
+#pragma unroll
+            for (int j = 0; j < 16; ++j) t[j] = 0.f;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[q * 16 + j] = t[j];
+        }
       }
       if constexpr (GLU) {
         // up rows (lanes 64..127) hand their values to the gate rows (lanes 0..63)
         __syncthreads();
         if (lrow >= HALF)
 #pragma unroll
-          for (int j = 0; j < 16; ++j) xch[j * HALF + (lrow - HALF)] = v[j];
+          for (int j = 0; j < 64; ++j) xch[j * HALF + (lrow - HALF)] = v[j];
         __syncthreads();
         if (lrow < HALF && row_ok) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int m = tok0 + cb + j;
-            if (m < a.M)
+          for (int j = 0; j < 64; ++j) {
+            const int m = tok0 + cg + j;
+            if (j < ncol && m < a.M)
               reinterpret_cast<__nv_bfloat16*>(a.Y)[(int64_t)m * a.ldy + rs] =
                   __float2bfloat16_rn(silu_f(v[j]) * xch[j * HALF + lrow]);
           }
         }
       } else if (row_ok) {
         if constexpr (EPI == EPI_RESID) {
-          // all 16 old values first: a load after a store to Y would wait for it
+          // all old values first: a load after a store to Y would wait for it
           float* const Y = reinterpret_cast<float*>(a.Y);
-          float y[16];
+          float y[64];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int m = tok0 + cb + j;
-            y[j] = m < a.M ? __ldcg(Y + (int64_t)m * a.ldy + n_glob) : 0.f;
+          for (int j = 0; j < 64; ++j) {
+            const int m = tok0 + cg + j;
+            y[j] = (j < ncol && m < a.M) ? __ldcg(Y + (int64_t)m * a.ldy + n_glob) : 0.f;
           }
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int m = tok0 + cb + j;
-            if (m < a.M) Y[(int64_t)m * a.ldy + n_glob] = y[j] + v[j];
+          for (int j = 0; j < 64; ++j) {
+            const int m = tok0 + cg + j;
+            if (j < ncol && m < a.M) Y[(int64_t)m * a.ldy + n_glob] = y[j] + v[j];
           }
         } else {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int m = tok0 + cb + j;
-            if (m >= a.M) continue;
+          for (int j = 0; j < 64; ++j) {
+            const int m = tok0 + cg + j;
+            if (j >= ncol || m >= a.M) continue;
             const int64_t o = (int64_t)m * a.ldy + n_glob;
             if constexpr (EPI == EPI_BF16) {
               reinterpret_cast<__nv_bfloat16*>(a.Y)[o] = __float2bfloat16_rn(v[j]);
@@ -448,12 +460,10 @@ static bool tc_plan(const GemvArgs& a, bool w4, int epi, TcPlan* pl, dim3* grid,
   pl->xrows = 16;
   while (pl->xrows < TC_TN && pl->xrows < a.M) pl->xrows *= 2;
   const int tok_tiles = (a.M + TC_TN - 1) / TC_TN;
-  // split K only when the tiles alone would leave most SMs idle (the tensor
-  // cores finish a tile's K quickly; splits cost a round of fp32 partials)
+  // split K while the splits still fit one wave of one CTA per SM (a round of
+  // fp32 partials is cheaper than idle SMs), at least 16 chunks per split
   const int ctas = nb * tok_tiles;
-  int ks = 1;
-  if (4 * ctas < tc_sm_count())
-    ks = std::max(1, std::min((tc_sm_count() + ctas - 1) / ctas, std::min(8, pl->chunks / 16)));
+  int ks = std::max(1, std::min(tc_sm_count() / ctas, std::min(8, pl->chunks / 16)));
   size_t need = ks > 1 ? (size_t)ctas * ks * TC_TN * TC_BM : 0;
   while (ks > 1 && (need > a.split_cap || ctas > a.split_cnt_cap || !a.split_part || !a.split_cnt)) {
     --ks;
