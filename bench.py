@@ -179,14 +179,29 @@ def measure_link(dev):
 
 
 def time_launches(fn, iters, stream):
+    """Milliseconds per call: `iters` calls captured once in a CUDA graph (on
+    a side stream) and replayed three times between CUDA events on the
+    replaying stream (host launch cost drops out; each call's own scratch
+    allocation stays in)."""
+    fn(0)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            for i in range(iters):
+                fn(i)
+    # replays run on the current stream: the events go there too
+    cur = torch.cuda.current_stream()
+    g.replay()
+    torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(cur)
+    for _ in range(3):
+        g.replay()
+    e1.record(cur)
     torch.cuda.synchronize()
-    e0.record(stream)
-    for i in range(iters):
-        fn(i)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    return e0.elapsed_time(e1) / iters
+    return e0.elapsed_time(e1) / (3 * iters)
 
 
 def kernel_measurements(sub, cfg, weights, model, pk, dev, quick):
@@ -194,35 +209,46 @@ def kernel_measurements(sub, cfg, weights, model, pk, dev, quick):
     launching stream; every operand set is larger than L2 or rotated)."""
     st = torch.cuda.current_stream()
     out = {}
-    # --- dominant kernel: bf16 GEMV of the resident layers at draft width M=8
+    # --- dominant kernel: int4 GEMV of the substitutes at draft width M=8
+    subs = model.w4_mats
+    xs = {s[4]: torch.randn(WIDTH, s[4], device=dev).to(torch.bfloat16) for s in subs}
+    ys = {s[3]: torch.empty(WIDTH, s[3], device=dev, dtype=torch.bfloat16) for s in subs}
+
+    def run_w4(i):
+        q, s_, z, n, k = subs[i % len(subs)]
+        sub.w4_gemm(xs[k], q, s_, z, n, k, out=ys[n])
+    ms4 = time_launches(run_w4, len(subs) * 2, st)
+    b4 = sum(q.numel() + s_.numel() * 2 + z.numel() * 2 + WIDTH * (n + k) * 2
+             for q, s_, z, n, k in subs) / len(subs)
+    out["w4_gemv_m8"] = dict(ms_per_launch=ms4, bytes_per_launch=b4,
+                             gbs=b4 / (ms4 / 1e3) / 1e9,
+                             what="int4 substitutes (q/k/v, o, gate, up, down) in turn, M=8")
+    # --- bf16 GEMV of the resident layers at M=8
     mats = []
     for i in range(cfg.n_resident):
         for n in ("wo", "wg", "wu", "wd"):
             mats.append(weights["layers"][i][n])
     x = {m.shape[1]: torch.randn(WIDTH, m.shape[1], device=dev).to(torch.bfloat16) for m in mats}
     y = {m.shape[0]: torch.empty(WIDTH, m.shape[0], device=dev, dtype=torch.bfloat16) for m in mats}
-    for m in mats[:4]:
-        sub.bf16_gemm(x[m.shape[1]], m, out=y[m.shape[0]])
     ms = time_launches(lambda i: sub.bf16_gemm(x[mats[i % len(mats)].shape[1]], mats[i % len(mats)],
                                                out=y[mats[i % len(mats)].shape[0]]),
-                       len(mats) * 3, st)
+                       len(mats) * 2, st)
     nbytes = sum(m.numel() * 2 + WIDTH * (m.shape[0] + m.shape[1]) * 2 for m in mats) / len(mats)
     out["gemv_bf16_m8"] = dict(ms_per_launch=ms, bytes_per_launch=nbytes,
                                gbs=nbytes / (ms / 1e3) / 1e9)
-    # --- int4 GEMV of the substitutes at M=8
-    subs = model.w4_mats
-    if subs:
-        xs = {s[4]: torch.randn(WIDTH, s[4], device=dev).to(torch.bfloat16) for s in subs}
-        ys = {s[3]: torch.empty(WIDTH, s[3], device=dev, dtype=torch.bfloat16) for s in subs}
-
-        def run_w4(i):
-            q, s_, z, n, k = subs[i % len(subs)]
-            sub.w4_gemm(xs[k], q, s_, z, n, k, out=ys[n])
-        ms4 = time_launches(run_w4, len(subs) * 3, st)
-        b4 = sum(q.numel() + s_.numel() * 2 + z.numel() * 2 + WIDTH * (n + k) * 2
-                 for q, s_, z, n, k in subs) / len(subs)
-        out["w4_gemv_m8"] = dict(ms_per_launch=ms4, bytes_per_launch=b4,
-                                 gbs=b4 / (ms4 / 1e3) / 1e9)
+    # --- verify GEMM on the tensor cores: all tree nodes through resident matrices
+    n_tree = 1 + DEPTH * WIDTH
+    xv = {m.shape[1]: torch.randn(n_tree, m.shape[1], device=dev).to(torch.bfloat16) for m in mats}
+    yv = {m.shape[0]: torch.empty(n_tree, m.shape[0], device=dev, dtype=torch.bfloat16) for m in mats}
+    msv = time_launches(lambda i: sub.bf16_gemm(xv[mats[i % len(mats)].shape[1]], mats[i % len(mats)],
+                                                out=yv[mats[i % len(mats)].shape[0]]),
+                        len(mats), st)
+    fl = sum(2 * n_tree * m.numel() for m in mats) / len(mats)
+    out["verify_gemm_bf16"] = dict(ms_per_launch=msv, flops_per_launch=fl,
+                                   tflops=fl / (msv / 1e3) / 1e12,
+                                   frac_of_peak=fl / (msv / 1e3) / 1e12 / pk["bf16"],
+                                   what=f"tcgen05 GEMM, M={n_tree} tree nodes, resident o/gate/up/down")
+    del xv, yv
     if quick:
         return out
     # --- int4 sweep on Qwen2.5-32B layer shapes
@@ -445,9 +471,9 @@ def main():
                "note": "h2d counts the prompt and the offloaded originals streamed for the "
                        "prefill and every verify pass"}
 
-    g = kern["gemv_bf16_m8"]
-    traffic = profile_traffic("gemv_bf16")
-    roof = {"kernel": "gemv_kernel (bf16 weights, M=8: resident layers of the draft)",
+    g = kern["w4_gemv_m8"]
+    traffic = profile_traffic("gemv_w4")
+    roof = {"kernel": "gemv_tma_kernel (int4 substitutes, M=8: the draft's substitute layers)",
             "bound": "hbm", "achieved": round(g["gbs"], 1), "peak": pk["hbm"],
             "unit": "GB/s", "frac": round(g["gbs"] / pk["hbm"], 4),
             "traffic": traffic, "peak_source": pk["src"] + " (burst copy)",

@@ -9,8 +9,10 @@ than the 129 MB L2):
   gemv_w4     int4 weights 37888x3584, M = 8 (a substitute gate+up pair)
   attn_draft  8 tree queries, 28/4 heads, d 128, 640 committed keys
   attn_verify 385 tree queries, same heads and keys
-  gemm_bf16   bf16 weights 18944x3584, M = 385 (a verify FFN matrix)
+  gemm_bf16   bf16 weights 18944x3584, M = 385 (a verify FFN matrix, tcgen05)
   gemv_{bf16,w4}_{down,o}  down projection 3584x18944 / o projection 3584x3584, M = 8
+  w4_mix      the four int4 substitute matrices of one layer (o, gate, up, down)
+              in turn, M = 8
   draft_level one draft forward of 8 tree nodes through the whole Qwen2.5-7B-shaped
               model (11 resident + 17 int4 layers, lm_head), inside the NVTX range
               "draft_level" (the second of two runs)
@@ -114,6 +116,20 @@ def main():
             ms = _time(lambda i: sub.bf16_gemm(x, ws[i % reps], out=y), a.iters)
             byt = n * k * 2 + 8 * (n + k) * 2
         res.update(ms=ms, gbs=byt / ms / 1e6)
+    elif a.case == "w4_mix":
+        # the four int4 substitute matrices of a Qwen2.5-7B layer in turn (o,
+        # gate, up, down), M = 8: the shapes bench.py's roofline cycles through
+        shapes = [(3584, 3584), (18944, 3584), (18944, 3584), (3584, 18944)]
+        packs = [synthetic.random_w4(n, k, 11 + i, dev) for i, (n, k) in enumerate(shapes)]
+        xs = {k: torch.randn(8, k, device=dev).to(torch.bfloat16) for _, k in shapes}
+        ys = {n: torch.empty(8, n, device=dev, dtype=torch.bfloat16) for n, _ in shapes}
+
+        def run(i):
+            n, k = shapes[i % 4]
+            sub.w4_gemm(xs[k], *packs[i % 4], n, k, out=ys[n])
+        ms = _time(run, a.iters)
+        byt = sum(n * ((k + 63) // 64) * 36 + 8 * (n + k) * 2 for n, k in shapes) / 4
+        res.update(ms=ms, gbs=byt / ms / 1e6, bytes_per_launch=byt)
     elif a.case in ("gemv_bf16", "gemm_bf16"):
         m = 8 if a.case == "gemv_bf16" else 385
         ws = [synthetic.randn_bf16((18944, 3584), s, 0.02, dev) for s in range(4)]
