@@ -59,7 +59,11 @@ __global__ void __launch_bounds__(THREADS) tree_attn_kernel(AttnArgs a) {
   uint32_t* sBits = reinterpret_cast<uint32_t*>(sV + 2 * KT * D * 2);
   auto sw = [](int row, int ch) { return row * CH + (ch ^ (row & 7)); };
 
-  pdl_wait();   // Q, K/V and the tree come from earlier kernels
+  // Programmatic dependent launch: only Q and the K/V of the query rows' own
+  // slots come from the kernel just before this one (the q/k/v projection).
+  // The tree (ancestors, depths), the page table, the counters and every other
+  // key were written by kernels that finished before that one started, so they
+  // are read before the wait.
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int kvh = blockIdx.y;
   const int G = a.n_heads_q / a.n_heads_kv;
@@ -86,18 +90,6 @@ __global__ void __launch_bounds__(THREADS) tree_attn_kernel(AttnArgs a) {
     for (int i = tid; i < nq * words; i += THREADS) sBits[i] = 0;
     if (tid < nq) sDep[tid] = a.depth[q_lo + tid];
   }
-  // ---- Q tile ----
-  const size_t q_row_stride = (size_t)a.n_heads_q * D;
-  for (int c = tid; c < ROWS * CH; c += THREADS) {
-    const int r = c / CH, ch = c % CH;
-    const int gr = row0 + r;
-    const bool ok = gr < n_rows;
-    const int q = ok ? gr / G : 0, h = ok ? gr % G : 0;
-    const uint16_t* src = a.Q + (size_t)q * q_row_stride + (size_t)(kvh * G + h) * D + ch * 8;
-    cp_async16(smem_u32(sQ + sw(r, ch) * 16), src, ok);
-  }
-  cp_commit();
-
   const size_t head_stride = (size_t)a.page_size * D;
   const size_t page_stride = (size_t)a.n_heads_kv * head_stride;
   const size_t layer_off = (size_t)a.layer * a.n_pages * page_stride;
@@ -145,8 +137,26 @@ __global__ void __launch_bounds__(THREADS) tree_attn_kernel(AttnArgs a) {
       if (s >= 0 && s < a.n_slots) atomicOr(&sBits[qq * words + (s >> 5)], 1u << (s & 31));
     }
   }
-  if (t_begin < t_end) load_kv(0, t_begin);
-  cp_commit();
+  // the first tile before the wait unless it holds a slot of the query rows
+  // (keys n_prefix + chain_slot0 .. + n_q - 1 are this pass's own K/V)
+  const int fresh_lo = (n_prefix + a.chain_slot0) / KT;
+  const int fresh_hi = (n_prefix + a.chain_slot0 + a.n_q - 1) / KT;
+  const bool first_fresh = t_begin >= fresh_lo && t_begin <= fresh_hi;
+  if (t_begin < t_end && !first_fresh) load_kv(0, t_begin);
+  pdl_wait();
+  if (t_begin < t_end && first_fresh) load_kv(0, t_begin);
+  cp_commit();   // group: the first K/V tile
+  // ---- Q tile ----
+  const size_t q_row_stride = (size_t)a.n_heads_q * D;
+  for (int c = tid; c < ROWS * CH; c += THREADS) {
+    const int r = c / CH, ch = c % CH;
+    const int gr = row0 + r;
+    const bool ok = gr < n_rows;
+    const int q = ok ? gr / G : 0, h = ok ? gr % G : 0;
+    const uint16_t* src = a.Q + (size_t)q * q_row_stride + (size_t)(kvh * G + h) * D + ch * 8;
+    cp_async16(smem_u32(sQ + sw(r, ch) * 16), src, ok);
+  }
+  cp_commit();   // group: Q
 
   // per-lane rows: g and g+8 of this warp's 16
   const int g = lane >> 2, tig = lane & 3;
@@ -165,7 +175,7 @@ __global__ void __launch_bounds__(THREADS) tree_attn_kernel(AttnArgs a) {
 #pragma unroll
   for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 
-  cp_wait<1>();   // Q landed
+  cp_wait<0>();   // Q and the first K/V tile landed
   __syncthreads();
   uint32_t qf[D / 16][4];
   {
