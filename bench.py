@@ -440,7 +440,9 @@ def main():
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
+    torch.cuda.nvtx.range_push("timed_cycles")   # lets a profiler select exactly the steps
     model.decode_cycles(dcfg, args.steps, stream)
+    torch.cuda.nvtx.range_pop()
     ev1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
