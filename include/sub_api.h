@@ -52,6 +52,14 @@ const char* sub_last_error(void);
 /* Library version string and the compile target, e.g. "0.1 sm_103a". */
 const char* sub_version(void);
 
+/* Pipeline waits that ran out on the current device since the library was
+ * loaded.  Every wait inside the TMA-streamed GEMV and the tensor-core GEMM
+ * (mbarrier phases, the grid-wide counters) is bounded: one that runs out
+ * bumps this count and lets the kernel finish with wrong numbers instead of
+ * hanging.  A correct run leaves it at 0; a non-zero value means the results
+ * of that run are invalid.  *out receives the count. */
+int32_t sub_pipeline_timeouts(uint32_t* out);
+
 /* ------------------------------------------------------------------------ */
 /* Int4 substitutes.  The draft replaces each offloaded target layer by a
  * data-free 4-bit copy ("Low-Bit Shadow" report 2.2 Step 4; card, Approach).

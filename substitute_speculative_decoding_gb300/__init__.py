@@ -87,6 +87,7 @@ _lib.sub_last_error.restype = C.c_char_p
 _lib.sub_last_error.argtypes = []
 _lib.sub_version.restype = C.c_char_p
 _lib.sub_version.argtypes = []
+_pipeline_timeouts = _decl("sub_pipeline_timeouts", [_vp])
 
 _w4_pack = _decl("sub_w4_pack", [_vp, _i64, _i64, _i32, _vp, _vp, _vp, _vp])
 _w4_dequant = _decl("sub_w4_dequant", [_vp, _vp, _vp, _i64, _i64, _i32, _vp, _vp])
@@ -115,7 +116,7 @@ _decode_read = _decl("sub_decode_read", [_vp, _vp, _i32, C.POINTER(_i32), C.POIN
 _cycle_info = _decl("sub_cycle_info", [_vp, C.POINTER(DecodeCfg), C.POINTER(_i64),
                                        C.POINTER(_i64)])
 
-EXPORTED = ["sub_last_error", "sub_version", "sub_w4_pack", "sub_w4_dequant", "sub_w4_gemm",
+EXPORTED = ["sub_last_error", "sub_version", "sub_pipeline_timeouts", "sub_w4_pack", "sub_w4_dequant", "sub_w4_gemm",
             "sub_bf16_gemm", "sub_tree_attn", "sub_draft_expand", "sub_verify_accept",
             "sub_verify_accept_static",
             "sub_kv_compact", "sub_model_create", "sub_model_destroy", "sub_model_memory",
@@ -130,6 +131,13 @@ def _check(code):
 
 def version() -> str:
     return _lib.sub_version().decode()
+
+
+def pipeline_timeouts() -> int:
+    """Bounded pipeline waits that ran out on this device (0 in a correct run)."""
+    n = C.c_uint32(0)
+    _check(_pipeline_timeouts(C.byref(n)))
+    return int(n.value)
 
 
 def _p(t):

@@ -58,6 +58,15 @@ using namespace sub;
 extern "C" const char* sub_last_error(void) { return g_last_error.c_str(); }
 extern "C" const char* sub_version(void) { return "0.1 sm_103a"; }
 
+extern "C" int32_t sub_pipeline_timeouts(uint32_t* out) {
+  SUB_CHECK_ARG(out, "null pointer");
+  unsigned int a = 0, b = 0;
+  SUB_TRY(gemv_tma_timeouts(&a));
+  SUB_TRY(gemm_tc_timeouts(&b));
+  *out = a + b;
+  return SUB_OK;
+}
+
 static int32_t matmul_public(const sub_bf16* X, int64_t M, bool w4, const void* W,
                              const sub_bf16* scale, const sub_bf16* zero, int64_t N, int64_t K,
                              sub_bf16* Y, void* stream) {
