@@ -323,7 +323,7 @@ int32_t launch_gemm(const GemvArgs& a, bool is_w4, int epi, cudaStream_t st) {
   SUB_CHECK_ARG(a.K % 8 == 0 && a.ldx % 8 == 0, "gemm: K and ldx must be multiples of 8");
   SUB_CHECK_ARG(a.n_seg >= 1 && a.n_seg <= 4, "gemm: 1..4 segments");
   SUB_CHECK_ARG((int64_t)a.M < (1ll << 20), "gemm: M too large");
-  SUB_CHECK_ARG(!a.xscale && !(epi == EPI_RESID && a.norm.xn),
+  SUB_CHECK_ARG(!a.xscale.partial && !(epi == EPI_RESID && a.norm.xn),
                 "gemm: factored-norm inputs and outputs are GEMV-only");
   bool done = false;
   SUB_TRY(launch_gemm_tc(a, is_w4, epi, st, &done));

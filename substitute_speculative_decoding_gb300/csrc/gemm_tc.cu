@@ -19,6 +19,16 @@
 // tiles splits over CTAs (grid.z); the last split of a tile adds the fp32
 // partials in split order.  Weight tiles never straddle a segment (q/k/v
 // stacked, or gate/up for SiLU-GLU: 64 gate rows + 64 up rows per tile).
+//
+// Int4 weights (group 64, one group per K chunk): TMA moves the packed codes
+// (32 bytes per row and chunk) beside the activations, and converter warps
+// turn them into the bf16 A tile, bf16((q - z) * s) for their row's group
+// scale and zero, written straight into the 128-byte swizzled layout the MMA
+// descriptor reads.  Each converter fences its shared-memory writes into the
+// async proxy and arrives on the stage's converted barrier, which the MMA lane
+// waits on as well as the TMA barrier.  With int4, eight converter warps (two
+// threads per row) fill the tile, warps 0..3 of them also run the epilogue,
+// and warps 8 and 9 lend lane 0 to the producer and the MMA issuer.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <algorithm>
@@ -39,6 +49,14 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TC_STAGES = 4;
 constexpr int TC_SMEM = 1024 + TC_STAGES * STAGE_BYTES + 256;   // + barriers, TMEM address
 constexpr int TMEM_COLS = 256;
+// int4 weights: the stage also holds the packed codes of its 128 rows
+constexpr int Q_BYTES = TC_BM * 32;                              // 4 KB
+constexpr int STAGE_BYTES_W4 = A_BYTES + B_BYTES + Q_BYTES;      // 52 KB
+constexpr int TC_CONV_WARPS = 8;                                 // two threads per row
+constexpr int TC_THREADS_W4 = (TC_CONV_WARPS + 2) * 32;
+constexpr int TC_SMEM_W4 = 1024 + TC_STAGES * STAGE_BYTES_W4 + 256;
+static_assert(STAGE_BYTES_W4 % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
+static_assert(TC_SMEM_W4 <= 227 * 1024, "int4 ring must fit one CTA's shared memory");
 
 __device__ unsigned int g_tc_timeouts;   // waits that ran out (never expected)
 
@@ -49,6 +67,9 @@ __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x));
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
@@ -94,6 +115,26 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
   d |= (uint64_t)2 << 61;
   return d;
 }
+// The four epilogue warps (0..3) meet here; other warps may still be running.
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// One word of eight 4-bit codes (byte p: element 2p in the low nibble, 2p+1
+// in the high one) to eight bf16 weights (q - z) * s, each rounded once to
+// fp32 by the subtraction (exact) and the product, then to bf16.
+__device__ __forceinline__ uint4 dequant8(uint32_t w, float s, float z) {
+  uint32_t out[4];
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    // 2^23 + q as an fp32 bit pattern, minus 2^23: the code as an exact float
+    const float q0 = __uint_as_float(0x4B000000u | ((w >> (8 * p)) & 15u)) - 8388608.0f;
+    const float q1 = __uint_as_float(0x4B000000u | ((w >> (8 * p + 4)) & 15u)) - 8388608.0f;
+    const float d0 = __fmul_rn(__fsub_rn(q0, z), s);
+    const float d1 = __fmul_rn(__fsub_rn(q1, z), s);
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(out[p]) : "f"(d1), "f"(d0));
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
 // K-major, M = 128, N = n.
 __device__ __forceinline__ uint32_t idesc_bf16(int n) {
@@ -137,7 +178,8 @@ __device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
 }  // namespace
 
 struct alignas(64) TcMaps {
-  CUtensorMap w[3];   // weight segments [rows, K] bf16, box 64 x (128 or 64 rows)
+  CUtensorMap w[3];   // weight segments: [rows, K] bf16, box 64 x (128 or 64 rows);
+                      // int4: packed codes [rows, K/2] bytes, box 32 x (128 or 64 rows)
   CUtensorMap x;      // activations [M, K] bf16, box 64 x token-tile rows
 };
 
@@ -149,19 +191,23 @@ struct TcPlan {
   int xrows;          // token rows of the activation box
 };
 
-template <int EPI>
-__global__ void __launch_bounds__(TC_THREADS, 1)
+template <int EPI, bool W4>
+__global__ void __launch_bounds__(W4 ? TC_THREADS_W4 : TC_THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ TcMaps maps, const GemvArgs a, const TcPlan pl) {
   constexpr bool GLU = EPI == EPI_GLU;
   constexpr int HALF = GLU ? TC_BM / 2 : TC_BM;   // rows of one segment in a tile
+  constexpr int SB = W4 ? STAGE_BYTES_W4 : STAGE_BYTES;
+  constexpr int PROD_WARP = W4 ? TC_CONV_WARPS : 0;
+  constexpr int MMA_WARP = PROD_WARP + 1;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* const base_ptr = smem_raw + (base - smem_u32(smem_raw));
-  const uint32_t bars = base + TC_STAGES * STAGE_BYTES;   // full[S], empty[S], done
+  const uint32_t bars = base + TC_STAGES * SB;   // full[S], empty[S], converted[S], done
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto empty_bar = [&](int s) { return bars + 8u * (TC_STAGES + s); };
-  const uint32_t done_bar = bars + 8u * (2 * TC_STAGES);
-  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + TC_STAGES * STAGE_BYTES + 128);
+  auto conv_bar = [&](int s) { return bars + 8u * (2 * TC_STAGES + s); };
+  const uint32_t done_bar = bars + 8u * (3 * TC_STAGES);
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + TC_STAGES * SB + 128);
   float* const xch = reinterpret_cast<float*>(base_ptr);   // epilogue exchange (reuses stage 0)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -186,6 +232,7 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const GemvArgs a, const TcPl
     for (int s = 0; s < TC_STAGES; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
+      mbar_init(conv_bar(s), TC_CONV_WARPS * 32);
     }
     mbar_init(done_bar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -195,18 +242,23 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const GemvArgs a, const TcPl
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // Warps 0 and 1 lend lane 0 to the producer and the MMA issuer; their other
+  // The producer and the MMA issuer are lane 0 of their warps; the other
   // lanes wait at the warp barrier (not on the done barrier) so they never
   // compete with the working lane's instruction stream.
-  if (warp == 0 && lane == 0) {
+  if (warp == PROD_WARP && lane == 0) {
     // ---------------------------------------------------------- producer
     auto issue = [&](int i, bool weights, bool acts) {
-      const int s = i % TC_STAGES, kx = (c0 + i) * TC_BK;
-      const uint32_t st = base + s * STAGE_BYTES, fb = full_bar(s);
+      const int s = i % TC_STAGES, c = c0 + i, kx = c * TC_BK;
+      const uint32_t st = base + s * SB, fb = full_bar(s);
       if (weights) {
-        mbar_expect_tx(fb, STAGE_BYTES);
-        for (int h = 0; h < (GLU ? 2 : 1); ++h)
-          tma_load_2d(st + h * HALF * 128, &maps.w[GLU ? h : seg], kx, r0, fb);
+        mbar_expect_tx(fb, W4 ? Q_BYTES + B_BYTES : STAGE_BYTES);
+        for (int h = 0; h < (GLU ? 2 : 1); ++h) {
+          if constexpr (W4)
+            tma_load_2d(st + A_BYTES + B_BYTES + h * HALF * 32, &maps.w[GLU ? h : seg], c * 32, r0,
+                        fb);
+          else
+            tma_load_2d(st + h * HALF * 128, &maps.w[GLU ? h : seg], kx, r0, fb);
+        }
       }
       if (acts) {
         // the activation box always moves TC_TN rows' worth of bytes: rows past
@@ -223,14 +275,15 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const GemvArgs a, const TcPl
       mbar_wait(empty_bar(i % TC_STAGES), ((i / TC_STAGES) - 1) & 1);
       issue(i, true, true);
     }
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == MMA_WARP && lane == 0) {
     // ---------------------------------------------------------- MMA issuer
     const uint32_t idesc = idesc_bf16(tn);
     for (int i = 0; i < nck; ++i) {
       const int s = i % TC_STAGES;
       mbar_wait(full_bar(s), (i / TC_STAGES) & 1);
+      if constexpr (W4) mbar_wait(conv_bar(s), (i / TC_STAGES) & 1);
       tc_fence_after();
-      const uint32_t st = base + s * STAGE_BYTES;
+      const uint32_t st = base + s * SB;
 #pragma unroll
       for (int kk = 0; kk < TC_BK / 16; ++kk)
         tc_mma(tmem, smem_desc_sw128(st + kk * 32), smem_desc_sw128(st + A_BYTES + kk * 32), idesc,
@@ -238,121 +291,170 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const GemvArgs a, const TcPl
       tc_commit(empty_bar(s));   // the stage is free once these MMAs have read it
     }
     tc_commit(done_bar);
+  } else if (W4 && warp < TC_CONV_WARPS) {
+    // ---------------------------------------------------------- converters
+    // thread pair = row of the tile (half a row each); the group's scale and
+    // zero come one chunk ahead
+    constexpr int CPT = 8 / (TC_CONV_WARPS / 4);   // 16-byte output chunks per thread
+    const int rr = threadIdx.x & (TC_BM - 1), part = threadIdx.x >> 7;
+    const int sseg = GLU ? (rr >= HALF ? 1 : 0) : seg;
+    const int rs = r0 + (GLU ? (rr & (HALF - 1)) : rr);
+    const int rows = GLU ? a.N : a.seg_end[sseg] - (sseg ? a.seg_end[sseg - 1] : 0);
+    const int G = (a.K + TC_BK - 1) / TC_BK;   // groups per row = K chunks
+    const bool ok = rs < rows;
+    const uint16_t* const sp = a.S[sseg] + (int64_t)(ok ? rs : 0) * G;
+    const uint16_t* const zp = a.Z[sseg] + (int64_t)(ok ? rs : 0) * G;
+    uint16_t sv = 0, zv = 0;
+    if (ok && nck > 0) {
+      sv = __ldg(sp + c0);
+      zv = __ldg(zp + c0);
+    }
+    for (int i = 0; i < nck; ++i) {
+      const int s = i % TC_STAGES;
+      const float sc = bf16_bits_to_f32(sv), zc = bf16_bits_to_f32(zv);
+      if (ok && i + 1 < nck) {
+        sv = __ldg(sp + c0 + i + 1);
+        zv = __ldg(zp + c0 + i + 1);
+      }
+      mbar_wait(full_bar(s), (i / TC_STAGES) & 1);
+      uint8_t* const st = base_ptr + s * SB;
+      const uint4* const qp =
+          reinterpret_cast<const uint4*>(st + A_BYTES + B_BYTES + rr * 32 + part * CPT * 4);
+      uint32_t words[CPT];
+#pragma unroll
+      for (int v = 0; v < CPT / 4; ++v) {
+        const uint4 q = qp[v];
+        words[4 * v] = q.x;
+        words[4 * v + 1] = q.y;
+        words[4 * v + 2] = q.z;
+        words[4 * v + 3] = q.w;
+      }
+      uint8_t* const arow = st + rr * 128;
+#pragma unroll
+      for (int c = 0; c < CPT; ++c) {   // 16-byte chunk j of the row sits at chunk j ^ (row % 8)
+        const int j = part * CPT + c;
+        *reinterpret_cast<uint4*>(arow + ((j ^ (rr & 7)) << 4)) = dequant8(words[c], sc, zc);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive(conv_bar(s));
+    }
   }
   __syncwarp();
   pdl_wait();   // every thread: the epilogue reads what earlier kernels wrote
   pdl_trigger();
 
   // ------------------------------------------------------------ epilogue
-  if (nck > 0) mbar_wait(done_bar, 0);
-  __syncwarp();
-  tc_fence_after();
-  const int lrow = warp * 32 + lane;                          // TMEM lane = row of the tile
-  const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
-  const int seg_rows = GLU ? a.N : a.seg_end[seg] - (seg ? a.seg_end[seg - 1] : 0);
-  const int seg_start = GLU ? 0 : (seg ? a.seg_end[seg - 1] : 0);
-  const int rs = r0 + (GLU ? (lrow & (HALF - 1)) : lrow);     // row within the segment
-  const bool row_ok = rs < seg_rows;
-  const int n_glob = seg_start + rs;
+  if (warp < 4) {
+    if (nck > 0) mbar_wait(done_bar, 0);
+    __syncwarp();
+    tc_fence_after();
+    const int lrow = warp * 32 + lane;                          // TMEM lane = row of the tile
+    const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
+    const int seg_rows = GLU ? a.N : a.seg_end[seg] - (seg ? a.seg_end[seg - 1] : 0);
+    const int seg_start = GLU ? 0 : (seg ? a.seg_end[seg - 1] : 0);
+    const int rs = r0 + (GLU ? (lrow & (HALF - 1)) : lrow);     // row within the segment
+    const bool row_ok = rs < seg_rows;
+    const int n_glob = seg_start + rs;
 
-  // split of K: park fp32 partials [tile][split][token][row], the last split sums
-  bool last = true;
-  float* part = nullptr;
-  if (ks > 1) {
-    const size_t tile_lin = (size_t)blockIdx.y * gridDim.x + blockIdx.x;
-    part = a.split_part + tile_lin * ks * (size_t)(TC_TN * TC_BM);
-    float* mine = part + (size_t)kz * (TC_TN * TC_BM);
-    for (int cb = 0; cb < tn; cb += 16) {
-      float v[16];
-      if (nck > 0) tc_ld16(taddr + cb, v);
-      else
+    // split of K: park fp32 partials [tile][split][token][row], the last split sums
+    bool last = true;
+    float* part = nullptr;
+    if (ks > 1) {
+      const size_t tile_lin = (size_t)blockIdx.y * gridDim.x + blockIdx.x;
+      part = a.split_part + tile_lin * ks * (size_t)(TC_TN * TC_BM);
+      float* mine = part + (size_t)kz * (TC_TN * TC_BM);
+      for (int cb = 0; cb < tn; cb += 16) {
+        float v[16];
+        if (nck > 0) tc_ld16(taddr + cb, v);
+        else
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = 0.f;
+          for (int j = 0; j < 16; ++j) v[j] = 0.f;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) __stcg(mine + (size_t)(cb + j) * TC_BM + lrow, v[j]);
-    }
-    __shared__ unsigned int s_last;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      __threadfence();
-      s_last = (atomicAdd(a.split_cnt + tile_lin, 1u) == (unsigned)ks - 1) ? 1u : 0u;
-      __threadfence();
-    }
-    __syncthreads();
-    last = s_last != 0;
-    if (last && threadIdx.x == 0) a.split_cnt[tile_lin] = 0u;
-  }
-
-  if (last) {
-    // 64 columns (tokens) per round: four TMEM loads, or four splits' worth of
-    // partial sums, and all their global loads in flight together
-    for (int cg = 0; cg < tn; cg += 64) {
-      const int ncol = min(64, tn - cg);   // a multiple of 16
-      float v[64];
-      if (ks > 1) {
-#pragma unroll
-        for (int j = 0; j < 64; ++j) v[j] = 0.f;
-        for (int z = 0; z < ks; ++z) {
-          float p[64];
-#pragma unroll
-          for (int j = 0; j < 64; ++j)
-            p[j] = j < ncol ? __ldcg(part + ((size_t)z * TC_TN + cg + j) * TC_BM + lrow) : 0.f;
-#pragma unroll
-          for (int j = 0; j < 64; ++j) v[j] += p[j];
-        }
-      } else {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float t[16];
-          if (q * 16 < ncol) tc_ld16(taddr + cg + q * 16, t);
-          else
-#pragma unroll
-            for (int j = 0; j < 16; ++j) t[j] = 0.f;
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[q * 16 + j] = t[j];
-        }
+        for (int j = 0; j < 16; ++j) __stcg(mine + (size_t)(cb + j) * TC_BM + lrow, v[j]);
       }
-      if constexpr (GLU) {
-        // up rows (lanes 64..127) hand their values to the gate rows (lanes 0..63)
-        __syncthreads();
-        if (lrow >= HALF)
+      __shared__ unsigned int s_last;
+      epi_bar();
+      if (threadIdx.x == 0) {
+        __threadfence();
+        s_last = (atomicAdd(a.split_cnt + tile_lin, 1u) == (unsigned)ks - 1) ? 1u : 0u;
+        __threadfence();
+      }
+      epi_bar();
+      last = s_last != 0;
+      if (last && threadIdx.x == 0) a.split_cnt[tile_lin] = 0u;
+    }
+
+    if (last) {
+      // 64 columns (tokens) per round: four TMEM loads, or four splits' worth of
+      // partial sums, and all their global loads in flight together
+      for (int cg = 0; cg < tn; cg += 64) {
+        const int ncol = min(64, tn - cg);   // a multiple of 16
+        float v[64];
+        if (ks > 1) {
 #pragma unroll
-          for (int j = 0; j < 64; ++j) xch[j * HALF + (lrow - HALF)] = v[j];
-        __syncthreads();
-        if (lrow < HALF && row_ok) {
+          for (int j = 0; j < 64; ++j) v[j] = 0.f;
+          for (int z = 0; z < ks; ++z) {
+            float p[64];
 #pragma unroll
-          for (int j = 0; j < 64; ++j) {
-            const int m = tok0 + cg + j;
-            if (j < ncol && m < a.M)
-              reinterpret_cast<__nv_bfloat16*>(a.Y)[(int64_t)m * a.ldy + rs] =
-                  __float2bfloat16_rn(silu_f(v[j]) * xch[j * HALF + lrow]);
-          }
-        }
-      } else if (row_ok) {
-        if constexpr (EPI == EPI_RESID) {
-          // all old values first: a load after a store to Y would wait for it
-          float* const Y = reinterpret_cast<float*>(a.Y);
-          float y[64];
+            for (int j = 0; j < 64; ++j)
+              p[j] = j < ncol ? __ldcg(part + ((size_t)z * TC_TN + cg + j) * TC_BM + lrow) : 0.f;
 #pragma unroll
-          for (int j = 0; j < 64; ++j) {
-            const int m = tok0 + cg + j;
-            y[j] = (j < ncol && m < a.M) ? __ldcg(Y + (int64_t)m * a.ldy + n_glob) : 0.f;
-          }
-#pragma unroll
-          for (int j = 0; j < 64; ++j) {
-            const int m = tok0 + cg + j;
-            if (j < ncol && m < a.M) Y[(int64_t)m * a.ldy + n_glob] = y[j] + v[j];
+            for (int j = 0; j < 64; ++j) v[j] += p[j];
           }
         } else {
 #pragma unroll
-          for (int j = 0; j < 64; ++j) {
-            const int m = tok0 + cg + j;
-            if (j >= ncol || m >= a.M) continue;
-            const int64_t o = (int64_t)m * a.ldy + n_glob;
-            if constexpr (EPI == EPI_BF16) {
-              reinterpret_cast<__nv_bfloat16*>(a.Y)[o] = __float2bfloat16_rn(v[j]);
-            } else {
-              reinterpret_cast<float*>(a.Y)[o] = v[j];
+          for (int q = 0; q < 4; ++q) {
+            float t[16];
+            if (q * 16 < ncol) tc_ld16(taddr + cg + q * 16, t);
+            else
+#pragma unroll
+              for (int j = 0; j < 16; ++j) t[j] = 0.f;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[q * 16 + j] = t[j];
+          }
+        }
+        if constexpr (GLU) {
+          // up rows (lanes 64..127) hand their values to the gate rows (lanes 0..63)
+          epi_bar();
+          if (lrow >= HALF)
+#pragma unroll
+            for (int j = 0; j < 64; ++j) xch[j * HALF + (lrow - HALF)] = v[j];
+          epi_bar();
+          if (lrow < HALF && row_ok) {
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+              const int m = tok0 + cg + j;
+              if (j < ncol && m < a.M)
+                reinterpret_cast<__nv_bfloat16*>(a.Y)[(int64_t)m * a.ldy + rs] =
+                    __float2bfloat16_rn(silu_f(v[j]) * xch[j * HALF + lrow]);
+            }
+          }
+        } else if (row_ok) {
+          if constexpr (EPI == EPI_RESID) {
+            // all old values first: a load after a store to Y would wait for it
+            float* const Y = reinterpret_cast<float*>(a.Y);
+            float y[64];
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+              const int m = tok0 + cg + j;
+              y[j] = (j < ncol && m < a.M) ? __ldcg(Y + (int64_t)m * a.ldy + n_glob) : 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+              const int m = tok0 + cg + j;
+              if (j < ncol && m < a.M) Y[(int64_t)m * a.ldy + n_glob] = y[j] + v[j];
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+              const int m = tok0 + cg + j;
+              if (j >= ncol || m >= a.M) continue;
+              const int64_t o = (int64_t)m * a.ldy + n_glob;
+              if constexpr (EPI == EPI_BF16) {
+                reinterpret_cast<__nv_bfloat16*>(a.Y)[o] = __float2bfloat16_rn(v[j]);
+              } else {
+                reinterpret_cast<float*>(a.Y)[o] = v[j];
+              }
             }
           }
         }
@@ -398,6 +500,20 @@ bool tc_map(CUtensorMap* m, const void* ptr, int64_t cols, int64_t rows, int64_t
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D byte map over packed int4 codes [rows, row_bytes]: 32-byte boxes (one group of
+// 64 codes per row), no swizzle.
+bool tc_map_q(CUtensorMap* m, const void* ptr, int64_t row_bytes, int64_t rows, int box_rows) {
+  auto fn = tc_encode_fn();
+  if (!fn || !aligned16(ptr) || row_bytes % 32 || box_rows < 1 || box_rows > 256) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  const cuuint32_t box[2] = {32, (cuuint32_t)box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int tc_sm_count() {
   static int n = 0;
   static std::once_flag once;
@@ -410,12 +526,25 @@ int tc_sm_count() {
   return n;
 }
 
-template <int EPI>
+template <int EPI, bool W4>
 int32_t tc_launch(const GemvArgs& a, const TcMaps& maps, const TcPlan& pl, dim3 grid,
                   cudaStream_t st) {
   SUB_TRY(gemm_tc_init());
-  SUB_CUDA_TRY(launch_k(gemm_tc_kernel<EPI>, grid, dim3(TC_THREADS), TC_SMEM, st, maps, a, pl));
+  SUB_CUDA_TRY(launch_k(gemm_tc_kernel<EPI, W4>, grid, dim3(W4 ? TC_THREADS_W4 : TC_THREADS),
+                        W4 ? TC_SMEM_W4 : TC_SMEM, st, maps, a, pl));
   return SUB_OK;
+}
+
+template <bool W4>
+int32_t tc_dispatch(const GemvArgs& a, int epi, const TcMaps& maps, const TcPlan& pl, dim3 grid,
+                    cudaStream_t st) {
+  switch (epi) {
+    case EPI_BF16: return tc_launch<EPI_BF16, W4>(a, maps, pl, grid, st);
+    case EPI_F32: return tc_launch<EPI_F32, W4>(a, maps, pl, grid, st);
+    case EPI_RESID: return tc_launch<EPI_RESID, W4>(a, maps, pl, grid, st);
+    case EPI_GLU: return tc_launch<EPI_GLU, W4>(a, maps, pl, grid, st);
+  }
+  return fail(SUB_EINVAL, "bad gemm epilogue");
 }
 
 }  // namespace
@@ -424,22 +553,27 @@ int32_t gemm_tc_init() {
   static std::once_flag once;
   static cudaError_t err = cudaSuccess;
   std::call_once(once, [] {
-    const void* ks[4] = {(const void*)gemm_tc_kernel<EPI_BF16>, (const void*)gemm_tc_kernel<EPI_F32>,
-                         (const void*)gemm_tc_kernel<EPI_RESID>, (const void*)gemm_tc_kernel<EPI_GLU>};
-    for (const void* k : ks)
+    const void* ks[8] = {
+        (const void*)gemm_tc_kernel<EPI_BF16, false>, (const void*)gemm_tc_kernel<EPI_F32, false>,
+        (const void*)gemm_tc_kernel<EPI_RESID, false>, (const void*)gemm_tc_kernel<EPI_GLU, false>,
+        (const void*)gemm_tc_kernel<EPI_BF16, true>,  (const void*)gemm_tc_kernel<EPI_F32, true>,
+        (const void*)gemm_tc_kernel<EPI_RESID, true>, (const void*)gemm_tc_kernel<EPI_GLU, true>};
+    for (int i = 0; i < 8; ++i)
       if (err == cudaSuccess)
-        err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+        err = cudaFuncSetAttribute(ks[i], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   i < 4 ? TC_SMEM : TC_SMEM_W4);
   });
   if (err != cudaSuccess) return fail(SUB_ECUDA, std::string("gemm_tc_init: ") + cudaGetErrorString(err));
   return SUB_OK;
 }
 
 // Tile plan: weight tiles per segment, token tiles, splits of K.  False when
-// the product is not for this kernel (int4 weights, the q/k/v epilogue,
-// fused-norm outputs, a segment count or alignment it does not handle).
+// the product is not for this kernel (the q/k/v epilogue, fused-norm outputs,
+// a segment count or alignment it does not handle).
 static bool tc_plan(const GemvArgs& a, bool w4, int epi, TcPlan* pl, dim3* grid, size_t* scratch) {
   static const bool on = env_flag("SUB_GEMM_TC", true);
-  if (!on || w4 || epi == EPI_QKV || a.M <= 16 || a.xscale) return false;
+  static const bool on_w4 = env_flag("SUB_GEMM_TC_W4", true);
+  if (!on || (w4 && !on_w4) || epi == EPI_QKV || a.M <= 16 || a.xscale.partial) return false;
   if (epi == EPI_RESID && a.norm.xn) return false;
   const bool glu = epi == EPI_GLU;
   if (a.n_seg < 1 || a.n_seg > 3 || (glu && a.n_seg != 2)) return false;
@@ -500,19 +634,17 @@ int32_t launch_gemm_tc(const GemvArgs& a, bool w4, int epi, cudaStream_t st, boo
   memset(&maps, 0, sizeof(maps));
   for (int s = 0; s < pl.n_maps; ++s) {
     const int64_t rows = glu ? a.N : a.seg_end[s] - (s ? a.seg_end[s - 1] : 0);
-    if (!tc_map(&maps.w[s], a.W[s], a.K, rows, (int64_t)a.K * 2, glu ? TC_BM / 2 : TC_BM))
+    const int box = glu ? TC_BM / 2 : TC_BM;
+    // int4 rows hold ceil(K/64) groups of 32 bytes (codes past K are 0 and meet
+    // zero activations: the activation map ends at K)
+    if (w4 ? !tc_map_q(&maps.w[s], a.W[s], (int64_t)pl.chunks * 32, rows, box)
+           : !tc_map(&maps.w[s], a.W[s], a.K, rows, (int64_t)a.K * 2, box))
       return SUB_OK;
   }
   if (!tc_map(&maps.x, a.X, a.K, a.M, (int64_t)a.ldx * 2, pl.xrows)) return SUB_OK;
   *done = true;
-  switch (epi) {
-    case EPI_BF16: return tc_launch<EPI_BF16>(a, maps, pl, grid, st);
-    case EPI_F32: return tc_launch<EPI_F32>(a, maps, pl, grid, st);
-    case EPI_RESID: return tc_launch<EPI_RESID>(a, maps, pl, grid, st);
-    case EPI_GLU: return tc_launch<EPI_GLU>(a, maps, pl, grid, st);
-  }
-  *done = false;
-  return fail(SUB_EINVAL, "bad gemm epilogue");
+  return w4 ? tc_dispatch<true>(a, epi, maps, pl, grid, st)
+            : tc_dispatch<false>(a, epi, maps, pl, grid, st);
 }
 
 int32_t gemm_tc_timeouts(unsigned int* out) {

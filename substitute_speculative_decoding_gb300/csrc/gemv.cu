@@ -350,11 +350,17 @@ gemv_kernel(GemvArgs a) {
     }
     if (threadIdx.x == 0) a.split_cnt[blockIdx.x] = 0u;
   }
-  __syncthreads();
   // factored RMSNorm of the input: scale each token's sums by its row scale
+  __shared__ float s_r[16];
+  if (a.xscale.partial)
+    for (int m = warp; m < a.M; m += WK) {
+      const float r = row_scale(a.xscale, m, lane);
+      if (lane == 0) s_r[m] = r;
+    }
+  __syncthreads();
   auto total = [&](int e, int tok) {
     const float v = tot_s[e];
-    return a.xscale ? v * __ldcg(a.xscale + tok) : v;
+    return a.xscale.partial ? v * s_r[tok] : v;
   };
 
   if constexpr (EPI == EPI_QKV) {
@@ -427,37 +433,26 @@ gemv_kernel(GemvArgs a) {
   }
 
   if constexpr (EPI == EPI_RESID) {
+    // next RMSNorm: per 16-row tile of this CTA, each token's sum of squares
     const NormOut& no = a.norm;
     if (!no.xn) return;
-    __shared__ unsigned int s_last;
     const float* Y = reinterpret_cast<const float*>(a.Y);
     __syncthreads();   // this CTA's residual rows are written
     if (warp == 0 && lane < a.M) {
-      float v[16 * RT];
 #pragma unroll
-      for (int r = 0; r < 16 * RT; ++r) {
-        const int row = blockIdx.x * RT * 16 + r;
-        v[r] = row < a.N ? __ldcg(Y + (int64_t)lane * a.ldy + row) : 0.f;
+      for (int t = 0; t < RT; ++t) {
+        const int row0 = (blockIdx.x * RT + t) * 16;
+        if (row0 >= a.N) continue;
+        float v[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r)
+          v[r] = row0 + r < a.N ? __ldcg(Y + (int64_t)lane * a.ldy + row0 + r) : 0.f;
+        float ss = 0.f;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) ss = fmaf(v[r], v[r], ss);
+        no.partial[(row0 / 16) * 16 + lane] = ss;
       }
-      float ss = 0.f;
-#pragma unroll
-      for (int r = 0; r < 16 * RT; ++r) ss = fmaf(v[r], v[r], ss);
-      no.partial[blockIdx.x * 16 + lane] = ss;
     }
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) s_last = (atomicAdd(no.counter, 1u) == gridDim.x - 1) ? 1u : 0u;
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    // last unit: r[m] = rsqrt(mean(x^2) + eps) from the per-unit partials in unit order
-    for (int m = warp; m < a.M; m += WK) {
-      float tot = 0.f;
-      for (int b = lane; b < (int)gridDim.x; b += 32) tot += __ldcg(no.partial + b * 16 + m);
-      tot = warp_sum(tot);
-      if (lane == 0) no.rvec[m] = rsqrtf(tot / (float)a.ldy + no.eps);
-    }
-    if (threadIdx.x == 0) *no.counter = 0u;
   }
 }
 
@@ -558,8 +553,8 @@ int32_t launch_gemv(const GemvArgs& a, bool is_w4, int epi, cudaStream_t st) {
                   "gemv: q/k/v segment sizes");
   }
   if (epi == EPI_RESID && a.norm.xn)
-    SUB_CHECK_ARG(a.norm.partial && a.norm.counter && a.norm.gain && a.norm.rvec && a.ldy == a.N,
-                  "gemv: norm epilogue needs partial, counter, gain, rvec and ldy == N");
+    SUB_CHECK_ARG(a.norm.partial && a.norm.gain && a.ldy == a.N && a.n_seg == 1,
+                  "gemv: norm epilogue needs partial, gain, one segment and ldy == N");
   bool done = false;
   SUB_TRY(launch_gemv_tma(a, is_w4, epi, st, &done));
   if (done) return SUB_OK;

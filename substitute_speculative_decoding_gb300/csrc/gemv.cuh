@@ -39,19 +39,50 @@ enum GemvEpi : int {
 };
 
 // Residual epilogue extension (the next RMSNorm, factored): every unit writes
-// xn[m, rows] = bf16(Y[m, rows] * gain[rows]) for its own rows and its partial
-// sum of squares; the last unit writes rvec[m] = rsqrt(mean(Y[m]^2) + eps).
-// The consumer GEMV multiplies its accumulators by rvec[m] (GemvArgs::xscale):
+// xn[m, rows] = bf16(Y[m, rows] * gain[rows]) for its own rows and, for each
+// 16-row tile t of the output, partial[t * 16 + m] = sum over the tile's rows
+// of Y[m, row]^2.  The consumer GEMV forms the row scale itself (RowScale):
 // RMSNorm is a per-row scalar, so sum_k W[n,k] x[m,k] r[m] g[k] =
 // r[m] sum_k W[n,k] (x[m,k] g[k]), with the bf16 rounding taken before the scale.
+// No grid-wide step is left in the producer: the consumer starts after it ends.
 struct NormOut {
   uint16_t* xn;              // [M, ldy] bf16, or null for a plain residual add
   const uint16_t* gain;      // [ldy]
-  float eps;
-  float* rvec;               // [M] row scales for the consumer
-  float* partial;            // [units * 16] per-unit sums of squares
-  unsigned int* counter;     // zero before launch; the last unit resets it
+  float* partial;            // [ceil(ldy / 16) * 16] per-tile sums of squares
 };
+
+// Row scales of a factored RMSNorm, formed by the consumer from the producer's
+// per-tile sums of squares: r[m] = rsqrt(sum_p partial[p * 16 + tok0 + m] /
+// hidden + eps), the parts summed in one fixed order (row_scale below).
+struct RowScale {
+  const float* partial;      // null: no scale
+  int n_parts;
+  int hidden;
+  float eps;
+  int tok0;                  // token offset of the consumer's row 0
+};
+
+// r[m] for one token, computed by a whole warp (every lane returns it): lane l
+// adds parts l, l + 32, ... in order, eight loads in flight per round, then a
+// butterfly sum.  Every kernel that applies a RowScale uses this routine, so
+// all of them see the same r.
+__device__ inline float row_scale(const RowScale& rs, int m, int lane) {
+  float t = 0.f;
+  const float* p = rs.partial + rs.tok0 + m;
+  for (int p0 = 0; p0 < rs.n_parts; p0 += 256) {
+    float v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int q = p0 + k * 32 + lane;
+      v[k] = q < rs.n_parts ? __ldcg(p + (size_t)q * 16) : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) t += v[k];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+  return rsqrtf(t / (float)rs.hidden + rs.eps);
+}
 
 // q/k/v epilogue: rows are q (Hq*D), k (Hkv*D), v (Hkv*D); token m sits at
 // position base + depth[m] and its K/V go to cache position base + slot0 + m.
@@ -82,7 +113,7 @@ struct GemvArgs {
   int N;                 // rows covered by the grid (for GLU: rows of one segment)
   void* Y;               // output (bf16 or fp32)
   int ldy;
-  const float* xscale;   // [M] per-row scale of the result (a factored RMSNorm), or null
+  RowScale xscale;       // per-row scale of the result (a factored RMSNorm), or none
   NormOut norm;          // EPI_RESID only
   QkvOut qkv;            // EPI_QKV only
   // split of K over CTAs (grid.y): partial sums meet in split_part and the

@@ -14,7 +14,10 @@
 //     into a ring of S stages, each guarded by a full and an empty mbarrier;
 //   * eight consumer warps each own a 16-row tile of the block and run
 //     mma.sync m16n8k16 (swap-AB: W is the A operand, X the B operand)
-//     straight from the swizzled stages, then release the stage.
+//     straight from the swizzled stages, then release the stage;
+//   * with int4 weights one more warp forms each stage's per-group activation
+//     sums Sx (an mma with an all-ones A operand) once for all eight tiles and
+//     hands them over in the stage, so the consumers only run the products.
 //
 // The weights of the first stages are requested before the wait on the
 // producing kernel (programmatic dependent launch); only X waits for it.
@@ -43,6 +46,7 @@ namespace {
 
 constexpr int NCW = 8;                  // consumer warps; one 16-row tile each
 constexpr int NTHR = (NCW + 1) * 32;    // plus the producer warp
+constexpr int NTHR_W4 = NTHR + 32;      // plus the group-sum warp (int4)
 constexpr int BR = NCW * 16;            // rows of a block
 constexpr int SMEM_LIMIT = 220 * 1024;  // dynamic shared memory of one CTA (1 per SM)
 constexpr int MAX_STAGES = 6;
@@ -108,6 +112,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// 3-D tiled TMA load: coordinates (x, y, z), innermost first.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
 // Pull a tensor-map descriptor into the TMA unit's cache ahead of first use.
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -123,7 +137,7 @@ struct alignas(64) TmaMaps {
   CUtensorMap w[3];   // bf16 weights, or packed int4 codes, per segment
   CUtensorMap s[3];   // int4 scales per segment
   CUtensorMap z[3];   // int4 zeros per segment
-  CUtensorMap x;      // activations [M, K]
+  CUtensorMap x;      // activations [M, K] viewed as [K/64][M][64]: one box per stage
 };
 
 struct TmaPlan {
@@ -147,18 +161,20 @@ struct TmaGeom {
   static constexpr int S_OFF = WBOXES * WBOX;
   static constexpr int Z_OFF = S_OFF + SZBOX;
   static constexpr int X_OFF = (Z_OFF + SZBOX + 1023) / 1024 * 1024;
-  static constexpr int STAGE = (X_OFF + XBOXES * XBOX + 1023) / 1024 * 1024;
+  static constexpr int SX_OFF = X_OFF + XBOXES * XBOX;   // int4: Sx [8 groups][MT * 8 tokens] fp32
+  static constexpr int SXB = W4 ? 8 * MT * 8 * 4 : 0;
+  static constexpr int STAGE = (SX_OFF + SXB + 1023) / 1024 * 1024;
   static constexpr int TX = WBOXES * WBOX + 2 * SZBOX + XBOXES * XBOX;   // bytes per stage
-  static constexpr int EPI_FLOATS = 4 * MT * 128 + NCW * 16 + 16;
+  static constexpr int EPI_FLOATS = 4 * MT * 128 + NCW * 16 + 32;   // + flag, row scales
   // alignment slack, ring, barriers and epilogue buffers within the limit
   static constexpr int STAGES =
-      std::min(MAX_STAGES, (SMEM_LIMIT - 1024 - 2 * MAX_STAGES * 8 - EPI_FLOATS * 4) / STAGE);
-  static constexpr int SMEM = 1024 + STAGES * STAGE + 2 * STAGES * 8 + EPI_FLOATS * 4;
+      std::min(MAX_STAGES, (SMEM_LIMIT - 1024 - 3 * MAX_STAGES * 8 - EPI_FLOATS * 4) / STAGE);
+  static constexpr int SMEM = 1024 + STAGES * STAGE + 3 * STAGES * 8 + EPI_FLOATS * 4;
   static_assert(STAGES >= 3 && SMEM <= SMEM_LIMIT, "TMA GEMV ring does not fit");
 };
 
 template <bool W4, int MT, int EPI>
-__global__ void __launch_bounds__(NTHR, 1)
+__global__ void __launch_bounds__(W4 ? NTHR_W4 : NTHR, 1)
 gemv_tma_kernel(const __grid_constant__ TmaMaps maps, const GemvArgs a, const TmaPlan pl) {
   using Geo = TmaGeom<W4, MT>;
   constexpr int S = Geo::STAGES;
@@ -167,10 +183,11 @@ gemv_tma_kernel(const __grid_constant__ TmaMaps maps, const GemvArgs a, const Tm
   // 1024-byte aligned base for the swizzled boxes
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* const base_ptr = smem_raw + (base - smem_u32(smem_raw));
-  const uint32_t bars = base + S * Geo::STAGE;          // full[S], then empty[S]
-  float* const epi = reinterpret_cast<float*>(base_ptr + S * Geo::STAGE + 2 * S * 8);
+  const uint32_t bars = base + S * Geo::STAGE;          // full[S], empty[S], sums[S]
+  float* const epi = reinterpret_cast<float*>(base_ptr + S * Geo::STAGE + 3 * S * 8);
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
+  auto sx_bar = [&](int s) { return bars + 8u * (2 * S + s); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int P = gridDim.x, c = blockIdx.x;
@@ -190,6 +207,7 @@ gemv_tma_kernel(const __grid_constant__ TmaMaps maps, const GemvArgs a, const Tm
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), NCW);
+      mbar_init(sx_bar(s), 1);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -234,11 +252,8 @@ gemv_tma_kernel(const __grid_constant__ TmaMaps maps, const GemvArgs a, const Tm
             }
           }
         }
-        if (acts) {
-          const int kx = kst * Geo::KC;
-          for (int j = 0; j < Geo::XBOXES; ++j)
-            tma_load_2d(st + Geo::X_OFF + j * Geo::XBOX, &maps.x, kx + 64 * j, 0, fb);
-        }
+        // the stage's XBOXES 64-column slices of X, one after another, in one copy
+        if (acts) tma_load_3d(st + Geo::X_OFF, &maps.x, 0, 0, kst * Geo::XBOXES, fb);
       };
       const int npre = std::min(S, u1 - u0);
       for (int u = u0; u < u0 + npre; ++u) issue(u, true, false);   // weights before the wait
@@ -254,9 +269,67 @@ gemv_tma_kernel(const __grid_constant__ TmaMaps maps, const GemvArgs a, const Tm
     return;
   }
 
+  const int g = lane >> 2, tig = lane & 3;
+  const uint32_t ONES = 0x3f803f80u;   // bf16x2 (1, 1)
+  const uint32_t ONES_A[4] = {ONES, ONES, ONES, ONES};
+  // B fragments of the 16 columns of 64-column activation box xbox that lane
+  // (g, tig) holds for token tile mt: columns (k, k + 4) paired, k-step kk
+  auto x_frags = [&](uint32_t xbox, int mt, uint32_t (&bfr)[4][2]) {
+    const int xr = mt * 8 + g;
+    const uint4 xa = lds128(xbox + xr * 128 + (((2 * tig) ^ g) << 4));
+    const uint4 xc = lds128(xbox + xr * 128 + (((2 * tig + 1) ^ g) << 4));
+    bfr[0][0] = __byte_perm(xa.x, xa.z, 0x5410);
+    bfr[0][1] = __byte_perm(xa.x, xa.z, 0x7632);
+    bfr[1][0] = __byte_perm(xa.y, xa.w, 0x5410);
+    bfr[1][1] = __byte_perm(xa.y, xa.w, 0x7632);
+    bfr[2][0] = __byte_perm(xc.x, xc.z, 0x5410);
+    bfr[2][1] = __byte_perm(xc.x, xc.z, 0x7632);
+    bfr[3][0] = __byte_perm(xc.y, xc.w, 0x5410);
+    bfr[3][1] = __byte_perm(xc.y, xc.w, 0x7632);
+  };
+
+  // ================================================================ group sums
+  if constexpr (W4) {
+    if (warp == NCW + 1) {
+      for (int u = u0; u < u1; ++u) {
+        const int i = u - u0, s = i % S;
+        const uint32_t st = base + s * Geo::STAGE;
+        mbar_wait(full_bar(s), (i / S) & 1);
+#pragma unroll
+        for (int gs = 0; gs < 8; ++gs)
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            uint32_t bfr[4][2];
+            x_frags(st + Geo::X_OFF + gs * Geo::XBOX, mt, bfr);
+            float sx[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) mma_bf16_16816(sx, ONES_A, bfr[k][0], bfr[k][1]);
+            // every row of the result is Sx; row 0 holds tokens 2 tig, 2 tig + 1
+            if (g == 0)
+              asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(
+                               st + Geo::SX_OFF + (((gs * MT + mt) * 8 + 2 * tig) << 2)),
+                           "f"(sx[0]), "f"(sx[1])
+                           : "memory");
+          }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sx_bar(s));
+      }
+      pdl_trigger();
+      return;
+    }
+  }
+
   // ================================================================ consumers
   pdl_wait();
-  const int g = lane >> 2, tig = lane & 3;
+  // row scales of a factored RMSNorm input, from the producer's per-tile sums
+  float* const s_r = epi + 4 * MT * 128 + NCW * 16 + 16;
+  if (a.xscale.partial) {
+    for (int m = warp; m < a.M; m += NCW) {
+      const float r = row_scale(a.xscale, m, lane);
+      if (lane == 0) s_r[m] = r;
+    }
+    consumer_sync();
+  }
   // row permutation pi of the fragment rows (and bf16 token rows)
   const int pg = W4 ? ((g & 3) * 2 + (g >> 2)) : ((g & 1) * 4 + (g >> 1));
   const int ptok_x = W4 ? g : pg;   // smem token row of B column g
@@ -285,7 +358,7 @@ gemv_tma_kernel(const __grid_constant__ TmaMaps maps, const GemvArgs a, const Tm
         for (int j = 0; j < 4; ++j) acc[mt][j] = 0.f;
     }
     const uint32_t st = base + s * Geo::STAGE;
-    mbar_wait(full_bar(s), (i / S) & 1);
+    mbar_wait(W4 ? sx_bar(s) : full_bar(s), (i / S) & 1);   // sums imply the bytes landed
     const int r0s = lo + pg, r1s = hi + pg;   // smem rows; (r & 7) == pg
 
     if constexpr (!W4) {
@@ -311,8 +384,6 @@ gemv_tma_kernel(const __grid_constant__ TmaMaps maps, const GemvArgs a, const Tm
       }
     } else {
       // ---------------------------------------------------- int4 weights
-      const uint32_t ONES = 0x3f803f80u;
-      const uint32_t ONES_A[4] = {ONES, ONES, ONES, ONES};
       // scales and zeros of the stage's 8 groups for rows r0s, r1s
       const uint4 sv0 = lds128(st + Geo::S_OFF + r0s * 16), sv1 = lds128(st + Geo::S_OFF + r1s * 16);
       const uint4 zv0 = lds128(st + Geo::Z_OFF + r0s * 16), zv1 = lds128(st + Geo::Z_OFF + r1s * 16);
@@ -327,24 +398,13 @@ gemv_tma_kernel(const __grid_constant__ TmaMaps maps, const GemvArgs a, const Tm
         const uint2 q1 = lds64(qb + r1s * 128 + qo);
         const uint32_t xbox = st + Geo::X_OFF + gs * Geo::XBOX;
         uint32_t bfr[MT][4][2];
-        float sx[MT][4];
+        float sx[MT][2];
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-          const int xr = mt * 8 + g;
-          const uint4 xa = lds128(xbox + xr * 128 + (((2 * tig) ^ g) << 4));
-          const uint4 xc = lds128(xbox + xr * 128 + (((2 * tig + 1) ^ g) << 4));
-          bfr[mt][0][0] = __byte_perm(xa.x, xa.z, 0x5410);
-          bfr[mt][0][1] = __byte_perm(xa.x, xa.z, 0x7632);
-          bfr[mt][1][0] = __byte_perm(xa.y, xa.w, 0x5410);
-          bfr[mt][1][1] = __byte_perm(xa.y, xa.w, 0x7632);
-          bfr[mt][2][0] = __byte_perm(xc.x, xc.z, 0x5410);
-          bfr[mt][2][1] = __byte_perm(xc.x, xc.z, 0x7632);
-          bfr[mt][3][0] = __byte_perm(xc.y, xc.w, 0x5410);
-          bfr[mt][3][1] = __byte_perm(xc.y, xc.w, 0x7632);
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj) sx[mt][jj] = 0.f;
-#pragma unroll
-          for (int k = 0; k < 4; ++k) mma_bf16_16816(sx[mt], ONES_A, bfr[mt][k][0], bfr[mt][k][1]);
+          x_frags(xbox, mt, bfr[mt]);
+          asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];"
+                       : "=f"(sx[mt][0]), "=f"(sx[mt][1])
+                       : "r"(st + Geo::SX_OFF + (((gs * MT + mt) * 8 + 2 * tig) << 2)));
         }
         const uint32_t a0s = (gs & 1) ? (sw0[gs >> 1] >> 16) : (sw0[gs >> 1] & 0xffffu);
         const uint32_t a1s = (gs & 1) ? (sw1[gs >> 1] >> 16) : (sw1[gs >> 1] & 0xffffu);
@@ -378,8 +438,8 @@ gemv_tma_kernel(const __grid_constant__ TmaMaps maps, const GemvArgs a, const Tm
           }
           acc[mt][0] = fmaf(sr0, fmaf(-zr0, sx[mt][0], p[0]), acc[mt][0]);
           acc[mt][1] = fmaf(sr0, fmaf(-zr0, sx[mt][1], p[1]), acc[mt][1]);
-          acc[mt][2] = fmaf(sr1, fmaf(-zr1, sx[mt][2], p[2]), acc[mt][2]);
-          acc[mt][3] = fmaf(sr1, fmaf(-zr1, sx[mt][3], p[3]), acc[mt][3]);
+          acc[mt][2] = fmaf(sr1, fmaf(-zr1, sx[mt][0], p[2]), acc[mt][2]);
+          acc[mt][3] = fmaf(sr1, fmaf(-zr1, sx[mt][1], p[3]), acc[mt][3]);
         }
       }
     }
@@ -390,6 +450,32 @@ gemv_tma_kernel(const __grid_constant__ TmaMaps maps, const GemvArgs a, const Tm
     if (kst != pl.s_blk - 1 && u != u1 - 1) continue;
     if (u == u1 - 1) pdl_trigger();
     const bool whole = piece_start == 0 && kst == pl.s_blk - 1;
+    // fragment element j of token tile mt: smem row (j & 2 ? hi : lo) + pg,
+    // B column 2 tig + (j & 1) -> token mt * 8 + tokmap(column)
+    auto token_of = [&](int mt, int j) {
+      const int col = 2 * tig + (j & 1);
+      const int pc = W4 ? col : ((col & 1) * 4 + (col >> 1));
+      return mt * 8 + pc;
+    };
+    const int seg_rows = GLU ? a.N : a.seg_end[seg] - (seg ? a.seg_end[seg - 1] : 0);
+    const int seg_start = GLU ? 0 : (seg ? a.seg_end[seg - 1] : 0);
+    // residual: the old values of the lane's elements, loaded before the
+    // pieces are exchanged so that their latency hides behind it (only the
+    // CTA that finishes the block writes these rows, and only after this)
+    float yold[MT][4];
+    if constexpr (EPI == EPI_RESID) {
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int tok = token_of(mt, j);
+          const int rs = r0 + ((j & 2) ? hi : lo) + pg;
+          yold[mt][j] = (tok < a.M && rs < seg_rows)
+                            ? __ldcg(reinterpret_cast<const float*>(a.Y) + (int64_t)tok * a.ldy +
+                                     seg_start + rs)
+                            : 0.f;
+        }
+    }
     float tot[MT][4];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
@@ -411,45 +497,56 @@ gemv_tma_kernel(const __grid_constant__ TmaMaps maps, const GemvArgs a, const Tm
       unsigned int* flag = reinterpret_cast<unsigned int*>(epi + 4 * MT * 128 + NCW * 16);
       consumer_sync();
       if (threadIdx.x == 0) {
-        __threadfence();
-        *flag = (atomicAdd(a.split_cnt + b, 1u) == (unsigned)n_c - 1) ? 1u : 0u;
-        __threadfence();
+        // release this CTA's piece, acquire the others' (one acq_rel atomic)
+        unsigned int old;
+        asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;"
+                     : "=r"(old)
+                     : "l"(a.split_cnt + b)
+                     : "memory");
+        *flag = old == (unsigned)n_c - 1 ? 1u : 0u;
       }
       consumer_sync();
       if (!*flag) continue;
+      // sum the pieces in CTA order; eight pieces' loads in flight per round
+      // (one load at a time would put n_c round trips on the kernel's tail)
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          float v = 0.f;
-          for (int y = 0; y < n_c; ++y)
-            v += __ldcg(slots + (size_t)y * PER + warp * MT * 128 + mt * 128 + j * 32 + lane);
-          tot[mt][j] = v;
-        }
+        for (int j = 0; j < 4; ++j) tot[mt][j] = 0.f;
+      const float* mine0 = slots + warp * MT * 128 + lane;
+      for (int y0 = 0; y0 < n_c; y0 += 8) {
+        float t[8][MT][4];
+#pragma unroll
+        for (int yy = 0; yy < 8; ++yy)
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              t[yy][mt][j] = y0 + yy < n_c
+                                 ? __ldcg(mine0 + (size_t)(y0 + yy) * PER + mt * 128 + j * 32)
+                                 : 0.f;
+#pragma unroll
+        for (int yy = 0; yy < 8; ++yy)
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (y0 + yy < n_c) tot[mt][j] += t[yy][mt][j];
+      }
       consumer_sync();   // every consumer has read the flag before it is reused
       if (threadIdx.x == 0) a.split_cnt[b] = 0u;
     }
 
     // ---------------------------------------------------- final epilogue of block b
-    // fragment element j of token tile mt: smem row (j & 2 ? hi : lo) + pg,
-    // B column 2 tig + (j & 1) -> token mt * 8 + tokmap(column)
-    auto token_of = [&](int mt, int j) {
-      const int col = 2 * tig + (j & 1);
-      const int pc = W4 ? col : ((col & 1) * 4 + (col >> 1));
-      return mt * 8 + pc;
-    };
-    if (a.xscale) {
+    if (a.xscale.partial) {
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int tok = token_of(mt, j);
-          if (tok < a.M) tot[mt][j] *= __ldcg(a.xscale + tok);
+          if (tok < a.M) tot[mt][j] *= s_r[tok];
         }
     }
-    const int seg_rows = GLU ? a.N : a.seg_end[seg] - (seg ? a.seg_end[seg - 1] : 0);
-    const int seg_start = GLU ? 0 : (seg ? a.seg_end[seg - 1] : 0);
-
     if constexpr (EPI == EPI_QKV) {
       const QkvOut& qo = a.qkv;
       const int D = qo.head_dim, half = D / 2;
@@ -512,22 +609,6 @@ gemv_tma_kernel(const __grid_constant__ TmaMaps maps, const GemvArgs a, const Tm
       consumer_sync();   // the exchange buffer is free again
     } else {
       float ss[MT][2] = {};
-      // residual: every old value of the lane first (a load after a store to Y
-      // would wait for the store)
-      float yold[MT][4];
-      if constexpr (EPI == EPI_RESID) {
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int tok = token_of(mt, j);
-            const int rs = r0 + ((j & 2) ? hi : lo) + pg;
-            yold[mt][j] = (tok < a.M && rs < seg_rows)
-                              ? __ldcg(reinterpret_cast<const float*>(a.Y) + (int64_t)tok * a.ldy +
-                                       seg_start + rs)
-                              : 0.f;
-          }
-      }
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -552,12 +633,9 @@ gemv_tma_kernel(const __grid_constant__ TmaMaps maps, const GemvArgs a, const Tm
           }
         }
       if constexpr (EPI == EPI_RESID) {
-        if (a.norm.xn) {
-          // sums of squares per token over the block's rows, then the last block
-          // turns the per-block partials into the row scales
-          const NormOut& no = a.norm;
-          float* s_ss = epi + 4 * MT * 128;        // [NCW][16]
-          unsigned int* flag = reinterpret_cast<unsigned int*>(epi + 4 * MT * 128 + NCW * 16);
+        if (a.norm.xn && r0 + lo < seg_rows) {
+          // sums of squares per token over this warp's 16-row tile, one part per tile
+          float* const part = a.norm.partial + (size_t)((r0 + lo) / 16) * 16;
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -566,33 +644,8 @@ gemv_tma_kernel(const __grid_constant__ TmaMaps maps, const GemvArgs a, const Tm
               v += __shfl_xor_sync(0xffffffffu, v, 4);
               v += __shfl_xor_sync(0xffffffffu, v, 8);
               v += __shfl_xor_sync(0xffffffffu, v, 16);
-              if (g == 0) s_ss[warp * 16 + token_of(mt, jb)] = v;
+              if (g == 0) part[token_of(mt, jb)] = v;
             }
-          consumer_sync();
-          if (threadIdx.x < MT * 8) {
-            float v = 0.f;
-#pragma unroll
-            for (int w = 0; w < NCW; ++w) v += s_ss[w * 16 + threadIdx.x];
-            no.partial[b * 16 + threadIdx.x] = v;
-          }
-          consumer_sync();
-          if (threadIdx.x == 0) {
-            __threadfence();
-            *flag = (atomicAdd(no.counter, 1u) == (unsigned)pl.n_blocks - 1) ? 1u : 0u;
-            __threadfence();
-          }
-          consumer_sync();
-          const bool last = *flag != 0;
-          consumer_sync();
-          if (last) {
-            for (int m = warp; m < a.M; m += NCW) {
-              float t = 0.f;
-              for (int bb = lane; bb < pl.n_blocks; bb += 32) t += __ldcg(no.partial + bb * 16 + m);
-              t = warp_sum(t);
-              if (lane == 0) no.rvec[m] = rsqrtf(t / (float)a.ldy + no.eps);
-            }
-            if (threadIdx.x == 0) *no.counter = 0u;
-          }
         }
       }
     }
@@ -670,8 +723,8 @@ template <bool W4, int MT, int EPI>
 int32_t tma_launch(const GemvArgs& a, const TmaMaps& maps, const TmaPlan& pl, int grid,
                    cudaStream_t st) {
   SUB_TRY(gemv_init());
-  SUB_CUDA_TRY(launch_k(gemv_tma_kernel<W4, MT, EPI>, dim3(grid), dim3(NTHR), TmaGeom<W4, MT>::SMEM,
-                        st, maps, a, pl));
+  SUB_CUDA_TRY(launch_k(gemv_tma_kernel<W4, MT, EPI>, dim3(grid), dim3(W4 ? NTHR_W4 : NTHR),
+                        TmaGeom<W4, MT>::SMEM, st, maps, a, pl));
   return SUB_OK;
 }
 
@@ -710,7 +763,9 @@ static bool tma_plan(const GemvArgs& a, bool w4, int epi, TmaPlan* pl, int* grid
   if (glu && a.n_seg != 2) return false;
   const int G = (a.K + 63) / 64;
   if (w4 && G % 8) return false;   // scale/zero rows must be whole 16-byte strides
+  if (a.K % 64) return false;      // X moves in whole 64-column slices
   if (epi == EPI_QKV && (BR % a.qkv.head_dim || a.qkv.head_dim < 16)) return false;
+  if (epi == EPI_RESID && a.norm.xn && a.n_seg != 1) return false;   // tiles index one segment
   const int kc = w4 ? 512 : 128;
   pl->s_blk = (a.K + kc - 1) / kc;
   int nb = 0;
@@ -762,9 +817,21 @@ int32_t launch_gemv_tma(const GemvArgs& a, bool w4, int epi, cudaStream_t st, bo
     }
     if (!ok) return SUB_OK;
   }
-  if (!make_map(&maps.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.X, a.K, a.M, (int64_t)a.ldx * 2, 64,
-                mt * 8, true))
-    return SUB_OK;
+  {
+    // X [M, K] as [K/64][M][64]: a stage's 64-column slices land one after
+    // another (the layout the consumers read), rows past M as zeros
+    auto fn = encode_fn();
+    if (!fn || !aligned16(a.X) || a.ldx % 8) return SUB_OK;
+    const int xboxes = w4 ? 8 : 2;
+    const cuuint64_t dims[3] = {64, (cuuint64_t)a.M, (cuuint64_t)(a.K / 64)};
+    const cuuint64_t strides[2] = {(cuuint64_t)a.ldx * 2, 128};
+    const cuuint32_t box[3] = {64, (cuuint32_t)(mt * 8), (cuuint32_t)xboxes};
+    const cuuint32_t es[3] = {1, 1, 1};
+    if (fn(&maps.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(a.X), dims, strides,
+           box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return SUB_OK;
+  }
   *done = true;
   if (w4) return mt == 1 ? tma_epi<true, 1>(a, epi, maps, pl, grid, st)
                          : tma_epi<true, 2>(a, epi, maps, pl, grid, st);

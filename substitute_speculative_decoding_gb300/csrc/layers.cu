@@ -12,12 +12,12 @@ __device__ __forceinline__ int64_t row_base(const RowSet& rs) {
 }
 
 // x[r] = embed[token[r]] (fp32 residual) and the first layer's matmul input:
-// xn[r] = bf16(RMSNorm(x[r]) * gain), or, factored (rvec non-null),
-// xn[r] = bf16(x[r] * gain) and rvec[r] = rsqrt(mean(x[r]^2) + eps) for the
-// consumer to apply to its sums.  One CTA per row.
+// xn[r] = bf16(RMSNorm(x[r]) * gain), or, factored (ss non-null),
+// xn[r] = bf16(x[r] * gain) and ss[r] = sum of x[r]^2, the single part from
+// which the consumer forms the row scale rsqrt(ss / hidden + eps).  One CTA per row.
 __global__ void embed_kernel(const uint16_t* __restrict__ embed, int hidden, RowSet rs,
                              float* __restrict__ x, const uint16_t* __restrict__ gain, float eps,
-                             uint16_t* __restrict__ xn, float* __restrict__ rvec) {
+                             uint16_t* __restrict__ xn, float* __restrict__ ss_out) {
   __shared__ float s_part[32];
   pdl_trigger();
   pdl_wait();
@@ -36,18 +36,18 @@ __global__ void embed_kernel(const uint16_t* __restrict__ embed, int hidden, Row
   float tot = 0.f;
   for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += s_part[w];
   const float inv = rsqrtf(tot / (float)hidden + eps);
-  if (rvec && threadIdx.x == 0) rvec[r] = inv;
-  const float scale = rvec ? 1.0f : inv;
+  if (ss_out && threadIdx.x == 0) ss_out[r] = tot;
+  const float scale = ss_out ? 1.0f : inv;
   for (int i = threadIdx.x; i < hidden; i += blockDim.x)
     reinterpret_cast<__nv_bfloat16*>(xn)[(int64_t)r * hidden + i] =
         __float2bfloat16_rn(bf16_bits_to_f32(src[i]) * scale * bf16_bits_to_f32(gain[i]));
 }
 
 int32_t launch_embed(const uint16_t* embed, int hidden, const RowSet& rs, int rows, float* x,
-                     const uint16_t* gain, float eps, uint16_t* xn, float* rvec, cudaStream_t st) {
+                     const uint16_t* gain, float eps, uint16_t* xn, float* ss_out, cudaStream_t st) {
   if (rows <= 0) return SUB_OK;
   SUB_CUDA_TRY(launch_k(embed_kernel, dim3(rows), dim3(256), 0, st, embed, hidden, rs, x, gain,
-                        eps, xn, rvec));
+                        eps, xn, ss_out));
   return SUB_OK;
 }
 

@@ -16,9 +16,10 @@ struct RowSet {
   const int32_t* base_dev;   // ... or read on the device
 };
 
-// rvec non-null: factored RMSNorm (xn = bf16(x * gain), rvec[r] = row scale).
+// ss_out non-null: factored RMSNorm (xn = bf16(x * gain), ss_out[r] = sum of
+// x[r]^2, one part of the consumer's RowScale).
 int32_t launch_embed(const uint16_t* embed, int hidden, const RowSet& rs, int rows, float* x,
-                     const uint16_t* gain, float eps, uint16_t* xn, float* rvec, cudaStream_t st);
+                     const uint16_t* gain, float eps, uint16_t* xn, float* ss_out, cudaStream_t st);
 int32_t launch_rmsnorm(const float* x, const uint16_t* gain, int rows, int hidden, float eps,
                        uint16_t* out, cudaStream_t st);
 

@@ -66,11 +66,9 @@ struct sub_model {
   size_t split_cap = 0;
   unsigned int* split_cnt = nullptr;
   int split_cnt_cap = 0;
-  float* rvec = nullptr;             // [2][16] row scales of the factored RMSNorms:
-                                     // attention input, FFN input
-  float* norm_partial = nullptr;     // [norm_parts] per-CTA sums of squares
+  float* norm_partial = nullptr;     // [2][norm_parts] per-tile sums of squares of the
+                                     // factored RMSNorms' inputs: attention, FFN
   int norm_parts = 0;
-  unsigned int* norm_counters = nullptr;
   // tree + decode state
   sub_tree tree{};
   int32_t* state = nullptr;
@@ -307,12 +305,17 @@ static int32_t forward(sub_model* m, bool draft, const FwdRows& r, float* logits
   rs.base = r.base;
   rs.base_dev = r.base_dev;
   trace_mark(m, "embed");
-  // Fused path: RMSNorm in factored form.  xn holds bf16(x * gain) and the
-  // consumer GEMV scales its sums by the row's rsqrt(mean(x^2) + eps).
-  float* const r_attn = fuse_norm ? m->rvec : nullptr;
-  float* const r_ffn = fuse_norm ? m->rvec + 16 : nullptr;
-  SUB_TRY(launch_embed(d.embed, H, rs, M, m->x, m->layers[0].attn_norm, d.rms_eps, m->xn, r_attn,
-                       st));
+  // Fused path: RMSNorm in factored form.  xn holds bf16(x * gain), the
+  // producer leaves per-tile sums of squares, and the consumer GEMV scales its
+  // sums by the row's rsqrt(mean(x^2) + eps), formed from those parts.
+  const int tiles = (H + 15) / 16;
+  RowScale r_attn{}, r_ffn{};
+  if (fuse_norm) {
+    r_attn = RowScale{m->norm_partial, 1, H, d.rms_eps, 0};   // the embedding: one part
+    r_ffn = RowScale{m->norm_partial + m->norm_parts, tiles, H, d.rms_eps, 0};
+  }
+  SUB_TRY(launch_embed(d.embed, H, rs, M, m->x, m->layers[0].attn_norm, d.rms_eps, m->xn,
+                       fuse_norm ? m->norm_partial : nullptr, st));
 
   AttnArgs at{};
   at.Q = m->q;
@@ -371,14 +374,11 @@ static int32_t forward(sub_model* m, bool draft, const FwdRows& r, float* logits
   qo.page_size = m->page_size;
   qo.n_pages = m->n_pages;
 
-  auto norm_out = [&](const uint16_t* gain, int which, float* rv) {
+  auto norm_out = [&](const uint16_t* gain, const RowScale& to) {
     NormOut no{};
     no.xn = m->xn;
     no.gain = gain;
-    no.eps = d.rms_eps;
-    no.rvec = rv;
-    no.partial = m->norm_partial;
-    no.counter = m->norm_counters + which;
+    no.partial = const_cast<float*>(to.partial);
     return no;
   };
 
@@ -422,7 +422,7 @@ static int32_t forward(sub_model* m, bool draft, const FwdRows& r, float* logits
     {
       GemvArgs oa = mm_args(m->attn, M, m->q_dim, W, o_idx, 1, o_rows, m->x, H, m);
       if (fuse_norm) {
-        oa.norm = norm_out(L.ffn_norm, 0, r_ffn);
+        oa.norm = norm_out(L.ffn_norm, r_ffn);
         SUB_TRY(launch_gemv(oa, w4, EPI_RESID, st));
       } else {
         SUB_TRY(launch_matmul(oa, w4, EPI_RESID, st));
@@ -440,8 +440,9 @@ static int32_t forward(sub_model* m, bool draft, const FwdRows& r, float* logits
     {
       GemvArgs da = mm_args(m->act, M, F, W, dn_idx, 1, o_rows, m->x, H, m);
       if (fuse_norm) {
-        da.norm = norm_out(next_gain, 1, r_attn);
+        da.norm = norm_out(next_gain, r_attn);
         SUB_TRY(launch_gemv(da, w4, EPI_RESID, st));
+        r_attn.n_parts = tiles;   // from here on the attention input comes from this GEMV
       } else {
         SUB_TRY(launch_matmul(da, w4, EPI_RESID, st));
       }
@@ -472,7 +473,8 @@ static int32_t forward(sub_model* m, bool draft, const FwdRows& r, float* logits
     const int idx0[1] = {0};
     const int vrows[1] = {d.vocab};
     GemvArgs la = mm_args(xin, nrow, H, lm, idx0, 1, vrows, logits, d.vocab, m);
-    la.xscale = r_attn ? r_attn + first : nullptr;
+    la.xscale = r_attn;
+    la.xscale.tok0 = first;
     SUB_TRY(launch_matmul(la, false, EPI_F32, st));
   }
   trace_mark(m, "end");
@@ -601,10 +603,7 @@ extern "C" int32_t sub_model_create(const sub_model_desc* desc, sub_model** out)
   CREATE_TRY(dalloc_t(m, &m->split_cnt, m->split_cnt_cap));
   CREATE_CUDA(cudaMemset(m->split_cnt, 0, m->split_cnt_cap * 4));
   m->norm_parts = (H / 16 + 1) * 16;
-  CREATE_TRY(dalloc_t(m, &m->norm_partial, m->norm_parts));
-  CREATE_TRY(dalloc_t(m, &m->rvec, 32));
-  CREATE_TRY(dalloc_t(m, &m->norm_counters, 4));
-  CREATE_CUDA(cudaMemset(m->norm_counters, 0, 16));
+  CREATE_TRY(dalloc_t(m, &m->norm_partial, 2 * m->norm_parts));
 
   // tree (slot 0 = root: parent -1, depth 0, score 0, anc [0, -1...])
   {

@@ -10,6 +10,7 @@ than the 129 MB L2):
   attn_draft  8 tree queries, 28/4 heads, d 128, 640 committed keys
   attn_verify 385 tree queries, same heads and keys
   gemm_bf16   bf16 weights 18944x3584, M = 385 (a verify FFN matrix, tcgen05)
+  gemm_w4     int4 weights 18944x3584, M = 385 (tcgen05 with the dequantising stage)
   gemv_{bf16,w4}_{down,o}  down projection 3584x18944 / o projection 3584x3584, M = 8
   w4_mix      the four int4 substitute matrices of one layer (o, gate, up, down)
               in turn, M = 8
@@ -138,6 +139,14 @@ def main():
         ms = _time(lambda i: sub.bf16_gemm(x, ws[i % 4], out=y), a.iters)
         byt = 18944 * 3584 * 2 + m * (3584 + 18944) * 2
         res.update(ms=ms, gbs=byt / ms / 1e6, tflops=2 * m * 18944 * 3584 / ms / 1e9)
+    elif a.case == "gemm_w4":
+        m, n, k = 385, 18944, 3584
+        packs = [synthetic.random_w4(n, k, s, dev) for s in range(4)]
+        x = torch.randn(m, k, device=dev).to(torch.bfloat16)
+        y = torch.empty(m, n, device=dev, dtype=torch.bfloat16)
+        ms = _time(lambda i: sub.w4_gemm(x, *packs[i % 4], n, k, out=y), a.iters)
+        byt = n * (k // 64) * 36 + m * (n + k) * 2
+        res.update(ms=ms, gbs=byt / ms / 1e6, tflops=2 * m * n * k / ms / 1e9)
     elif a.case == "gemv_w4":
         packs = [synthetic.random_w4(37888, 3584, s, dev) for s in range(4)]
         x = torch.randn(8, 3584, device=dev).to(torch.bfloat16)

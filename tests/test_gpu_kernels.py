@@ -45,7 +45,7 @@ def test_w4_pack_and_dequant_bit_exact(sub, n, k):
     assert np.array_equal(np32(deq), quant.w4_dequant(rq, rs, rz, k))
 
 
-@pytest.mark.parametrize("m", [1, 3, 8, 13, 16, 17, 48, 130])
+@pytest.mark.parametrize("m", [1, 3, 8, 13, 16, 17, 48, 130, 385])
 @pytest.mark.parametrize("n,k", [(256, 688), (4608, 3584), (96, 512)])
 def test_w4_gemm(sub, m, n, k):
     w = synthetic.randn_bf16((n, k), 3 + n + k, std=0.02)

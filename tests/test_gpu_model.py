@@ -99,6 +99,17 @@ def test_draft_logits_two_levels(tiny):
     close(lg1.cpu().numpy(), r1)
 
 
+def test_draft_prefill_wide(tiny):
+    """The draft over all prompt rows (M > 16): int4 products on the
+    tensor-core GEMM, with the FFN's 688 columns ending in a partial group."""
+    p = tiny["prompt"].to(DEV)
+    lg = torch.empty((len(p), CFG.vocab), dtype=torch.float32, device=DEV)
+    tiny["model"].forward(1, p, 0, 0, logits=lg)
+    torch.cuda.synchronize()
+    ref, _, _ = prefill(CFG, tiny["glob"], tiny["draft"], tiny["prompt"].numpy())
+    close(lg.cpu().numpy(), ref)
+
+
 def _check_lossless(tiny, out, mode="greedy", temp=1.0, seed=7):
     r = decode.check_stream(CFG, tiny["glob"], tiny["layers"], tiny["prompt"].numpy(),
                             out.numpy(), mode, temp, seed, gap=1e-2)

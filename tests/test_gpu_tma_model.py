@@ -72,6 +72,18 @@ def test_tma_draft_logits_two_levels(small):
 
 
 @pytest.mark.gpu
+def test_tma_draft_prefill_wide(small):
+    """The draft over all 32 prompt rows: its int4 products are tree-width
+    (M > 16) and run on the tensor-core GEMM with the dequantising stage."""
+    p = small["prompt"].to(DEV)
+    lg = torch.empty((len(p), CFG.vocab), dtype=torch.float32, device=DEV)
+    small["model"].forward(1, p, 0, 0, logits=lg)
+    torch.cuda.synchronize()
+    ref, _, _ = prefill(CFG, small["glob"], small["draft"], small["prompt"].numpy())
+    close(lg.cpu().numpy(), ref)
+
+
+@pytest.mark.gpu
 def test_tma_generate_is_lossless(small):
     out, st = small["model"].generate(small["prompt"], 40, 6, 3)
     r = decode.check_stream(CFG, small["glob"], small["layers"], small["prompt"].numpy(),
