@@ -83,12 +83,26 @@ __global__ void __launch_bounds__(THREADS) tree_attn_kernel(AttnArgs a) {
   const int words = (a.n_slots + 31) / 32;
 
   // ---- visibility bitmaps of this CTA's queries ----
-  // depths first (one parallel load), then every ancestor entry in parallel
-  __shared__ int sDep[ROWS + 2];
+  // every ancestor entry and its query's depth are loaded together into
+  // registers (one round trip), and set into the cleared bitmaps after the
+  // barrier below
+  constexpr int ANC_PER = 6;   // entries per thread per round
+  const int nq = q_hi - q_lo + 1;
+  const int n_anc = a.anc ? nq * a.anc_stride : 0;
+  int anc_s[ANC_PER], anc_d[ANC_PER];
   if (a.anc) {
-    const int nq = q_hi - q_lo + 1;
     for (int i = tid; i < nq * words; i += THREADS) sBits[i] = 0;
-    if (tid < nq) sDep[tid] = a.depth[q_lo + tid];
+#pragma unroll
+    for (int u = 0; u < ANC_PER; ++u) {
+      const int i = tid + u * THREADS;
+      anc_s[u] = -1;
+      anc_d[u] = -1;
+      if (i < n_anc) {
+        const int qq = i / a.anc_stride;
+        anc_s[u] = a.anc[(int64_t)(q_lo + qq) * a.anc_stride + i % a.anc_stride];
+        anc_d[u] = a.depth[q_lo + qq];
+      }
+    }
   }
   const size_t head_stride = (size_t)a.page_size * D;
   const size_t page_stride = (size_t)a.n_heads_kv * head_stride;
@@ -126,15 +140,21 @@ __global__ void __launch_bounds__(THREADS) tree_attn_kernel(AttnArgs a) {
 
   row_offsets(0, t_begin);
   row_offsets(1, t_begin + 1);
-  __syncthreads();   // depths, cleared bitmaps and the first row offsets are visible
+  __syncthreads();   // cleared bitmaps and the first row offsets are visible
   if (a.anc) {
-    const int nq = q_hi - q_lo + 1;
-    for (int i = tid; i < nq * a.anc_stride; i += THREADS) {
+    // entry j of query q counts for depths 0..depth[q]
+    auto set_bit = [&](int i, int sv, int dv) {
       const int qq = i / a.anc_stride, j = i % a.anc_stride;
-      const int q = q_lo + qq;
-      if (j > sDep[qq]) continue;
-      const int s = a.anc[(int64_t)q * a.anc_stride + j];
-      if (s >= 0 && s < a.n_slots) atomicOr(&sBits[qq * words + (s >> 5)], 1u << (s & 31));
+      if (j <= dv && sv >= 0 && sv < a.n_slots)
+        atomicOr(&sBits[qq * words + (sv >> 5)], 1u << (sv & 31));
+    };
+#pragma unroll
+    for (int u = 0; u < ANC_PER; ++u)
+      if (tid + u * THREADS < n_anc) set_bit(tid + u * THREADS, anc_s[u], anc_d[u]);
+    for (int i = tid + ANC_PER * THREADS; i < n_anc; i += THREADS) {   // wider trees
+      const int qq = i / a.anc_stride;
+      set_bit(i, a.anc[(int64_t)(q_lo + qq) * a.anc_stride + i % a.anc_stride],
+              a.depth[q_lo + qq]);
     }
   }
   // the first tile before the wait unless it holds a slot of the query rows
@@ -209,6 +229,41 @@ __global__ void __launch_bounds__(THREADS) tree_attn_kernel(AttnArgs a) {
         mma_bf16_16816(s[2 * jj], qf[kk], b0, b1);
         mma_bf16_16816(s[2 * jj + 1], qf[kk], b2, b3);
       }
+    // visibility of the tile's 64 keys for the lane's two rows, as two 32-bit
+    // masks per row: a key of the prefix is seen by every query, a tree slot
+    // by the queries it is an ancestor of (chain: the slots up to the query's
+    // own), keys past n_keys by none.  Rows past the queries (padding) see the
+    // whole tile; their results are never written.
+    const int key0 = t * KT;
+    uint32_t vm[2][2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t lo = ~0u, hi = ~0u;
+      if (key0 + KT > n_prefix && rq[h] >= 0) {
+        const int sl0 = key0 - n_prefix;   // slot of the tile's first key (> -KT)
+        if (a.anc) {
+          const uint32_t* bits = sBits + (rq[h] - q_lo) * words;
+          auto word = [&](int wi) -> uint32_t {   // prefix keys sit at negative slots
+            return wi < 0 ? ~0u : (wi < words ? bits[wi] : 0u);
+          };
+          const int w0 = sl0 >> 5, off = sl0 & 31;   // floor division
+          const uint32_t a0 = word(w0), a1 = word(w0 + 1), a2 = word(w0 + 2);
+          lo = __funnelshift_r(a0, a1, off);
+          hi = __funnelshift_r(a1, a2, off);
+        } else {
+          const int cnt = rslot[h] - sl0 + 1;   // keys key0 .. key0 + cnt - 1 are seen
+          lo = cnt >= 32 ? ~0u : (cnt <= 0 ? 0u : (1u << cnt) - 1u);
+          hi = cnt >= 64 ? ~0u : (cnt <= 32 ? 0u : (1u << (cnt - 32)) - 1u);
+        }
+        const int nv = n_keys - key0;   // >= 1 keys of the tile exist
+        if (nv < 64) {
+          lo &= nv >= 32 ? ~0u : (1u << nv) - 1u;
+          hi &= nv <= 32 ? 0u : (1u << (nv - 32)) - 1u;
+        }
+      }
+      vm[h][0] = lo;
+      vm[h][1] = hi;
+    }
     // mask, scale, online softmax
     float tmax[2] = {-INFINITY, -INFINITY};
 #pragma unroll
@@ -216,16 +271,8 @@ __global__ void __launch_bounds__(THREADS) tree_attn_kernel(AttnArgs a) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int h = e >> 1;
-        const int key = t * KT + j * 8 + 2 * tig + (e & 1);
-        bool vis = false;
-        if (rq[h] >= 0 && key < n_keys) {
-          if (key < n_prefix) vis = true;
-          else {
-            const int sl = key - n_prefix;
-            if (a.anc) vis = (sBits[(rq[h] - q_lo) * words + (sl >> 5)] >> (sl & 31)) & 1u;
-            else vis = sl <= rslot[h];
-          }
-        }
+        const int kk = (j & 3) * 8 + 2 * tig + (e & 1);   // bit within the 32-key half j / 4
+        const bool vis = (vm[h][j >> 2] >> kk) & 1u;
         const float v = vis ? s[j][e] * sl2 : -INFINITY;
         s[j][e] = v;
         tmax[h] = fmaxf(tmax[h], v);
@@ -306,23 +353,23 @@ __global__ void __launch_bounds__(THREADS) tree_attn_kernel(AttnArgs a) {
   // Key splits form one thread-block cluster: each CTA parks its partial
   // (max, sum, unnormalised O) in its own shared memory, and after a cluster
   // barrier every CTA merges a slice of the rows by reading its peers' shared
-  // memory (distributed shared memory), in split order.
+  // memory (distributed shared memory), in split order: the peers' maxima and
+  // sums once per (row, split) into local memory, then one round of their
+  // partial outputs, four columns per thread.
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   constexpr int PLD = D + 4;
   float* sO = reinterpret_cast<float*>(sK);            // [ROWS][PLD], reuses the K/V tiles
   float* sM = sO + ROWS * PLD;                          // [ROWS]
   float* sL = sM + ROWS;                                // [ROWS]
-  float* sW = sL + ROWS;                                // [rows_per][S] merge weights
+  float* const sMl = sL + ROWS;                         // [rows_per][S] peer maxima
+  float* const sWl = sMl + ROWS * ATTN_MAX_SPLIT;       // [rows_per][S] merge weights
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int r = wrow + g + 8 * h;
 #pragma unroll
-    for (int i = 0; i < D / 8; ++i) {
-      const int c = i * 8 + 2 * tig;
-      sO[r * PLD + c] = o[i][2 * h];
-      sO[r * PLD + c + 1] = o[i][2 * h + 1];
-    }
+    for (int i = 0; i < D / 8; ++i)
+      *reinterpret_cast<float2*>(sO + r * PLD + i * 8 + 2 * tig) = make_float2(o[i][2 * h], o[i][2 * h + 1]);
     if (tig == 0) {
       sM[r] = m_run[h];
       sL[r] = l_run[h];
@@ -333,51 +380,53 @@ __global__ void __launch_bounds__(THREADS) tree_attn_kernel(AttnArgs a) {
   const int rank = (int)cluster.block_rank();
   const int rows_per = (ROWS + S - 1) / S;
   const int r_lo = rank * rows_per, r_hi = min(ROWS, r_lo + rows_per);
-  for (int i = tid; i < (r_hi - r_lo); i += THREADS) {
-    const int r = r_lo + i;
-    float ms[ATTN_MAX_SPLIT], ls[ATTN_MAX_SPLIT];
-#pragma unroll
-    for (int s2 = 0; s2 < ATTN_MAX_SPLIT; ++s2) {   // all remote loads in flight at once
-      ms[s2] = s2 < S ? cluster.map_shared_rank(sM, s2)[r] : -INFINITY;
-      ls[s2] = s2 < S ? cluster.map_shared_rank(sL, s2)[r] : 0.f;
-    }
-    float mx = -INFINITY;
-#pragma unroll
-    for (int s2 = 0; s2 < ATTN_MAX_SPLIT; ++s2) mx = fmaxf(mx, ms[s2]);
-    float den = 0.f;
-#pragma unroll
-    for (int s2 = 0; s2 < ATTN_MAX_SPLIT; ++s2) {
-      ms[s2] = (ms[s2] == -INFINITY) ? 0.f : exp2f(ms[s2] - mx);
-      den += ms[s2] * ls[s2];
-    }
-    const float inv = den > 0.f ? 1.f / den : 0.f;
-#pragma unroll
-    for (int s2 = 0; s2 < ATTN_MAX_SPLIT; ++s2)
-      if (s2 < S) sW[i * ATTN_MAX_SPLIT + s2] = ms[s2] * inv;
+  const int n_ms = (r_hi - r_lo) * S;
+  const bool act = tid < n_ms;
+  const int mi = act ? tid / S : 0, ms2 = act ? tid % S : 0;
+  float l_peer = 0.f, w_peer = 0.f;
+  if (act) {
+    sMl[mi * S + ms2] = cluster.map_shared_rank(sM, ms2)[r_lo + mi];
+    l_peer = cluster.map_shared_rank(sL, ms2)[r_lo + mi];
   }
   __syncthreads();
-  for (int idx = tid; idx < (r_hi - r_lo) * (D / 2); idx += THREADS) {
-    const int i = idx / (D / 2), c = (idx % (D / 2)) * 2;
+  if (act) {
+    float mx = -INFINITY;
+    for (int t2 = 0; t2 < S; ++t2) mx = fmaxf(mx, sMl[mi * S + t2]);
+    const float m2 = sMl[mi * S + ms2];
+    w_peer = (m2 == -INFINITY) ? 0.f : exp2f(m2 - mx);
+    sWl[mi * S + ms2] = w_peer * l_peer;   // this split's share of the denominator
+  }
+  __syncthreads();
+  float den = 0.f;
+  if (act)
+    for (int t2 = 0; t2 < S; ++t2) den += sWl[mi * S + t2];   // in split order
+  __syncthreads();
+  if (act) sWl[mi * S + ms2] = w_peer * (den > 0.f ? 1.f / den : 0.f);
+  __syncthreads();
+  for (int idx = tid; idx < (r_hi - r_lo) * (D / 4); idx += THREADS) {
+    const int i = idx / (D / 4), c = (idx % (D / 4)) * 4;
     const int r = r_lo + i;
     const int gr = row0 + r;
     if (gr >= n_rows) continue;
-    float2 pv[ATTN_MAX_SPLIT];
+    float4 pv[ATTN_MAX_SPLIT];
 #pragma unroll
     for (int s2 = 0; s2 < ATTN_MAX_SPLIT; ++s2)
-      pv[s2] = s2 < S ? *reinterpret_cast<const float2*>(cluster.map_shared_rank(sO, s2) + r * PLD + c)
-                      : make_float2(0.f, 0.f);
-    float v0 = 0.f, v1 = 0.f;
+      pv[s2] = s2 < S ? *reinterpret_cast<const float4*>(cluster.map_shared_rank(sO, s2) + r * PLD + c)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+    float v0 = 0.f, v1 = 0.f, v2 = 0.f, v3 = 0.f;
 #pragma unroll
     for (int s2 = 0; s2 < ATTN_MAX_SPLIT; ++s2) {
       if (s2 < S) {
-        const float w = sW[i * ATTN_MAX_SPLIT + s2];
+        const float w = sWl[i * S + s2];
         v0 = fmaf(w, pv[s2].x, v0);
         v1 = fmaf(w, pv[s2].y, v1);
+        v2 = fmaf(w, pv[s2].z, v2);
+        v3 = fmaf(w, pv[s2].w, v3);
       }
     }
     const int q = gr / G, hh = gr % G;
     const size_t orow = (size_t)q * a.n_heads_q + kvh * G + hh;
-    *reinterpret_cast<uint32_t*>(a.O + orow * D + c) = pack_bf16x2(v0, v1);
+    *reinterpret_cast<uint2*>(a.O + orow * D + c) = make_uint2(pack_bf16x2(v0, v1), pack_bf16x2(v2, v3));
   }
   cluster.sync();   // peers may still be reading this CTA's shared memory
 }
@@ -389,9 +438,9 @@ int attn_smem_bytes(const AttnArgs& a) {
   const int words = (a.n_slots + 31) / 32;
   return ROWS * d * 2 + 4 * KT * d * 2 + (a.anc ? nq * words * 4 : 0);
 }
-static_assert(ROWS * (128 + 4) * 4 + 2 * ROWS * 4 + ROWS * ATTN_MAX_SPLIT * 4 <= 4 * KT * 128 * 2,
+static_assert(ROWS * (128 + 4) * 4 + 2 * ROWS * 4 + 2 * ROWS * ATTN_MAX_SPLIT * 4 <= 4 * KT * 128 * 2,
               "the cluster merge buffers must fit in the K/V tiles (head_dim 128)");
-static_assert(ROWS * (64 + 4) * 4 + 2 * ROWS * 4 + ROWS * ATTN_MAX_SPLIT * 4 <= 4 * KT * 64 * 2,
+static_assert(ROWS * (64 + 4) * 4 + 2 * ROWS * 4 + 2 * ROWS * ATTN_MAX_SPLIT * 4 <= 4 * KT * 64 * 2,
               "the cluster merge buffers must fit in the K/V tiles (head_dim 64)");
 
 static int g_max_split = 8;   // largest cluster the device runs (set by attn_init)
