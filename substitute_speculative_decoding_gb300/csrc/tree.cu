@@ -154,11 +154,43 @@ __global__ void __launch_bounds__(EXP_THREADS) expand_kernel(ExpandArgs a) {
   __shared__ unsigned long long s_cand[MAX_WIDTH * MAX_WIDTH];   // [row][i] token keys
   __shared__ unsigned long long s_glob[MAX_WIDTH * MAX_WIDTH];   // score keys
   const int kp = a.k_prev;
+  // every CTA's partial results into shared memory first, eight loads in
+  // flight per thread (read one at a time they put a round trip per chunk
+  // on the launch's tail)
+  const int n_part = kp * a.n_chunks;
+  extern __shared__ unsigned long long s_dyn[];
+  unsigned long long* const s_key = s_dyn;                        // [part][k]
+  float* const s_pm = reinterpret_cast<float*>(s_key + (size_t)n_part * k);
+  float* const s_ps = s_pm + n_part;
+  for (int i0 = threadIdx.x; i0 < n_part * k; i0 += 8 * EXP_THREADS) {
+    unsigned long long v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * EXP_THREADS;
+      v[u] = i < n_part * k ? __ldcg(a.part_key + (size_t)(i / k) * MAX_WIDTH + i % k) : 0ull;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (i0 + u * EXP_THREADS < n_part * k) s_key[i0 + u * EXP_THREADS] = v[u];
+  }
+  for (int i0 = threadIdx.x; i0 < n_part; i0 += 2 * EXP_THREADS) {
+    const int i1 = i0 + EXP_THREADS;
+    const float m0 = __ldcg(a.part_max + i0), q0 = __ldcg(a.part_sum + i0);
+    const float m1 = i1 < n_part ? __ldcg(a.part_max + i1) : 0.f;
+    const float q1 = i1 < n_part ? __ldcg(a.part_sum + i1) : 0.f;
+    s_pm[i0] = m0;
+    s_ps[i0] = q0;
+    if (i1 < n_part) {
+      s_pm[i1] = m1;
+      s_ps[i1] = q1;
+    }
+  }
+  __syncthreads();
   if (threadIdx.x < kp) {
     float bm = -INFINITY, bs = 0.f;
     for (int cc = 0; cc < a.n_chunks; ++cc) {
-      const size_t p = (size_t)threadIdx.x * a.n_chunks + cc;
-      lse_merge(bm, bs, a.part_max[p], a.part_sum[p]);
+      const int p = threadIdx.x * a.n_chunks + cc;
+      lse_merge(bm, bs, s_pm[p], s_ps[p]);
     }
     s_lse[threadIdx.x] = bm + logf(bs);
   }
@@ -168,8 +200,7 @@ __global__ void __launch_bounds__(EXP_THREADS) expand_kernel(ExpandArgs a) {
     for (int r = 0; r < k; ++r) {
       unsigned long long best = 0ull;
       for (int i = lane; i < nc; i += 32) {
-        const unsigned long long key =
-            a.part_key[((size_t)row * a.n_chunks + i / k) * MAX_WIDTH + i % k];
+        const unsigned long long key = s_key[(size_t)row * nc + i];
         bool taken = false;
         for (int q = 0; q < r; ++q) taken |= (s_cand[row * MAX_WIDTH + q] == key);
         if (!taken && key > best) best = key;
@@ -244,9 +275,13 @@ int32_t launch_expand(const ExpandArgs& a, cudaStream_t st) {
   SUB_CHECK_ARG(a.V >= k && a.V <= (1 << 20), "expand: V must be in [k, 2^20]");
   SUB_CHECK_ARG(1 + (int64_t)a.tree.max_depth * k < 4096, "expand: tree too large");
   SUB_CHECK_ARG(a.temp > 0.f, "expand: temperature must be positive");
+  SUB_CHECK_ARG(a.n_chunks >= 1 && a.k_prev >= 1 && a.k_prev <= MAX_WIDTH, "expand: bad split");
   dim3 grid(a.n_chunks, a.k_prev);
-  if (k <= 8) SUB_CUDA_TRY(launch_k(expand_kernel<8>, grid, dim3(EXP_THREADS), 0, st, a));
-  else SUB_CUDA_TRY(launch_k(expand_kernel<16>, grid, dim3(EXP_THREADS), 0, st, a));
+  // the last CTA stages every partial: keys [parts][k], then max and sum per part
+  const size_t smem = (size_t)a.n_chunks * a.k_prev * (k * 8 + 8);
+  SUB_CHECK_ARG(smem <= 43 * 1024, "expand: too many chunks for the staging buffer");
+  if (k <= 8) SUB_CUDA_TRY(launch_k(expand_kernel<8>, grid, dim3(EXP_THREADS), smem, st, a));
+  else SUB_CUDA_TRY(launch_k(expand_kernel<16>, grid, dim3(EXP_THREADS), smem, st, a));
   return SUB_OK;
 }
 
