@@ -163,7 +163,12 @@ struct TmaGeom {
   static constexpr int X_OFF = (Z_OFF + SZBOX + 1023) / 1024 * 1024;
   static constexpr int SX_OFF = X_OFF + XBOXES * XBOX;   // int4: Sx [8 groups][MT * 8 tokens] fp32
   static constexpr int SXB = W4 ? 8 * MT * 8 * 4 : 0;
-  static constexpr int STAGE = (SX_OFF + SXB + 1023) / 1024 * 1024;
+  // int4, one token tile: the stage's activation B fragments in lane order,
+  // [8 groups][2 halves][32 lanes][16 bytes], formed once by the group-sum warp
+  static constexpr bool XFRAG = W4 && MT == 1;
+  static constexpr int XF_OFF = SX_OFF + SXB;
+  static constexpr int XFB = XFRAG ? 8 * 2 * 32 * 16 : 0;
+  static constexpr int STAGE = (XF_OFF + XFB + 1023) / 1024 * 1024;
   static constexpr int TX = WBOXES * WBOX + 2 * SZBOX + XBOXES * XBOX;   // bytes per stage
   static constexpr int EPI_FLOATS = 4 * MT * 128 + NCW * 16 + 32;   // + flag, row scales
   // alignment slack, ring, barriers and epilogue buffers within the limit
@@ -301,6 +306,15 @@ gemv_tma_kernel(const __grid_constant__ TmaMaps maps, const GemvArgs a, const Tm
           for (int mt = 0; mt < MT; ++mt) {
             uint32_t bfr[4][2];
             x_frags(st + Geo::X_OFF + gs * Geo::XBOX, mt, bfr);
+            if constexpr (Geo::XFRAG) {
+              const uint32_t xf = st + Geo::XF_OFF + ((gs * 2) * 32 + lane) * 16;
+              asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(xf), "r"(bfr[0][0]),
+                           "r"(bfr[0][1]), "r"(bfr[1][0]), "r"(bfr[1][1])
+                           : "memory");
+              asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(xf + 32 * 16),
+                           "r"(bfr[2][0]), "r"(bfr[2][1]), "r"(bfr[3][0]), "r"(bfr[3][1])
+                           : "memory");
+            }
             float sx[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int k = 0; k < 4; ++k) mma_bf16_16816(sx, ONES_A, bfr[k][0], bfr[k][1]);
@@ -401,7 +415,20 @@ gemv_tma_kernel(const __grid_constant__ TmaMaps maps, const GemvArgs a, const Tm
         float sx[MT][2];
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-          x_frags(xbox, mt, bfr[mt]);
+          if constexpr (Geo::XFRAG) {
+            const uint32_t xf = st + Geo::XF_OFF + ((gs * 2) * 32 + lane) * 16;
+            const uint4 f0 = lds128(xf), f1 = lds128(xf + 32 * 16);
+            bfr[mt][0][0] = f0.x;
+            bfr[mt][0][1] = f0.y;
+            bfr[mt][1][0] = f0.z;
+            bfr[mt][1][1] = f0.w;
+            bfr[mt][2][0] = f1.x;
+            bfr[mt][2][1] = f1.y;
+            bfr[mt][3][0] = f1.z;
+            bfr[mt][3][1] = f1.w;
+          } else {
+            x_frags(xbox, mt, bfr[mt]);
+          }
           asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];"
                        : "=f"(sx[mt][0]), "=f"(sx[mt][1])
                        : "r"(st + Geo::SX_OFF + (((gs * MT + mt) * 8 + 2 * tig) << 2)));
