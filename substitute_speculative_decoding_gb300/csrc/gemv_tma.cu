@@ -15,9 +15,11 @@
 //   * eight consumer warps each own a 16-row tile of the block and run
 //     mma.sync m16n8k16 (swap-AB: W is the A operand, X the B operand)
 //     straight from the swizzled stages, then release the stage;
-//   * with int4 weights one more warp forms each stage's per-group activation
-//     sums Sx (an mma with an all-ones A operand) once for all eight tiles and
-//     hands them over in the stage, so the consumers only run the products.
+//   * with int4 weights two more warps (even and odd groups) form each
+//     stage's per-group activation sums Sx (an mma with an all-ones A
+//     operand) and, for one token tile, the activation B fragments in lane
+//     order, once for all eight tiles, and hand them over in the stage, so
+//     the consumers only unpack, multiply and fold.
 //
 // The weights of the first stages are requested before the wait on the
 // producing kernel (programmatic dependent launch); only X waits for it.
@@ -46,7 +48,7 @@ namespace {
 
 constexpr int NCW = 8;                  // consumer warps; one 16-row tile each
 constexpr int NTHR = (NCW + 1) * 32;    // plus the producer warp
-constexpr int NTHR_W4 = NTHR + 32;      // plus the group-sum warp (int4)
+constexpr int NTHR_W4 = NTHR + 64;      // plus two group-sum warps (int4)
 constexpr int BR = NCW * 16;            // rows of a block
 constexpr int SMEM_LIMIT = 220 * 1024;  // dynamic shared memory of one CTA (1 per SM)
 constexpr int MAX_STAGES = 6;
@@ -212,7 +214,7 @@ gemv_tma_kernel(const __grid_constant__ TmaMaps maps, const GemvArgs a, const Tm
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), NCW);
-      mbar_init(sx_bar(s), 1);
+      mbar_init(sx_bar(s), 2);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -295,15 +297,17 @@ gemv_tma_kernel(const __grid_constant__ TmaMaps maps, const GemvArgs a, const Tm
 
   // ================================================================ group sums
   if constexpr (W4) {
-    if (warp == NCW + 1) {
+    if (warp == NCW + 1 || warp == NCW + 2) {
+      const int par = warp - (NCW + 1);   // this warp's groups: par, par + 2, ...
       for (int u = u0; u < u1; ++u) {
         const int i = u - u0, s = i % S;
         const uint32_t st = base + s * Geo::STAGE;
         mbar_wait(full_bar(s), (i / S) & 1);
 #pragma unroll
-        for (int gs = 0; gs < 8; ++gs)
+        for (int gh = 0; gh < 4; ++gh)
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt) {
+            const int gs = 2 * gh + par;
             uint32_t bfr[4][2];
             x_frags(st + Geo::X_OFF + gs * Geo::XBOX, mt, bfr);
             if constexpr (Geo::XFRAG) {
