@@ -80,8 +80,11 @@ int32_t sub_w4_dequant(const uint8_t* q, const sub_bf16* scale, const sub_bf16* 
                        int64_t N, int64_t K, int32_t group, sub_bf16* W_out, void* stream);
 
 /* Y[M, N] (bf16) = X[M, K] (bf16) . deq(W)^T, fp32 accumulation.
- * M <= 16 runs the warp-level GEMV (one pass over the packed weights);
- * larger M runs the tiled tensor-core kernel.  K % 8 == 0. */
+ * M <= 16 runs the warp-level GEMV (one pass over the packed weights; the
+ * zero point and scale are folded into the fp32 sums, so deq(W) is not
+ * rounded to bf16 there).  Larger M runs the tcgen05 tensor-core GEMM, which
+ * dequantises each 64-column group to bf16((q - z) * s), the values
+ * sub_w4_dequant returns, before the multiply.  K % 8 == 0. */
 int32_t sub_w4_gemm(const sub_bf16* X, int64_t M, const uint8_t* q, const sub_bf16* scale,
                     const sub_bf16* zero, int64_t N, int64_t K, int32_t group,
                     sub_bf16* Y, void* stream);
