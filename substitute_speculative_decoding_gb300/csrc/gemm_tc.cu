@@ -318,12 +318,15 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const GemvArgs a, const TcPl
       }
       mbar_wait(full_bar(s), (i / TC_STAGES) & 1);
       uint8_t* const st = base_ptr + s * SB;
-      const uint4* const qp =
-          reinterpret_cast<const uint4*>(st + A_BYTES + B_BYTES + rr * 32 + part * CPT * 4);
+      // the codes arrive with the 32-byte swizzle: 16-byte half h of row rr
+      // sits at half h ^ ((rr >> 2) & 1), so eight consecutive rows of one
+      // read phase cover all 32 banks
+      const uint8_t* const qrow = st + A_BYTES + B_BYTES + rr * 32;
       uint32_t words[CPT];
 #pragma unroll
       for (int v = 0; v < CPT / 4; ++v) {
-        const uint4 q = qp[v];
+        const int hf = part * (CPT / 4) + v;   // 16-byte half of the row's 32 bytes
+        const uint4 q = *reinterpret_cast<const uint4*>(qrow + ((hf ^ ((rr >> 2) & 1)) << 4));
         words[4 * v] = q.x;
         words[4 * v + 1] = q.y;
         words[4 * v + 2] = q.z;
@@ -501,7 +504,7 @@ bool tc_map(CUtensorMap* m, const void* ptr, int64_t cols, int64_t rows, int64_t
 }
 
 // 2-D byte map over packed int4 codes [rows, row_bytes]: 32-byte boxes (one group of
-// 64 codes per row), no swizzle.
+// 64 codes per row), 32-byte swizzle.
 bool tc_map_q(CUtensorMap* m, const void* ptr, int64_t row_bytes, int64_t rows, int box_rows) {
   auto fn = tc_encode_fn();
   if (!fn || !aligned16(ptr) || row_bytes % 32 || box_rows < 1 || box_rows > 256) return false;
@@ -510,7 +513,7 @@ bool tc_map_q(CUtensorMap* m, const void* ptr, int64_t row_bytes, int64_t rows, 
   const cuuint32_t box[2] = {32, (cuuint32_t)box_rows};
   const cuuint32_t es[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
