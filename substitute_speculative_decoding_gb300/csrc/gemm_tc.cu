@@ -9,26 +9,30 @@
 // consecutive weight rows) of a token column, so its global stores of Y[m, n]
 // are coalesced.
 //
-// One CTA: 128 threads.  Warp 0 lane 0 streams K chunks of 64 columns (128
-// bytes per row, the TMA 128-byte swizzle atom) of both operands into an
-// S-stage shared-memory ring by TMA; warp 1 lane 0 issues tcgen05.mma
-// (kind::f16, M = 128, N = token tile, K = 16 per instruction) from the
-// stages and hands each stage back with tcgen05.commit to its empty
-// mbarrier; after the last chunk a final commit releases the four warps into
-// the epilogue, which reads TMEM with tcgen05.ld.  Long K with few weight
-// tiles splits over CTAs (grid.z); the last split of a tile adds the fp32
-// partials in split order.  Weight tiles never straddle a segment (q/k/v
-// stacked, or gate/up for SiLU-GLU: 64 gate rows + 64 up rows per tile).
+// Persistent CTAs, one per SM at most, take the work items (token tile,
+// weight tile, split of K) round-robin.  Warps 0..3 run the epilogue (one
+// TMEM lane quarter each); the next warp's lane 0 streams K chunks of 64
+// columns (128 bytes per row, the TMA 128-byte swizzle atom) of both operands
+// into an S-stage shared-memory ring by TMA, and the last warp's lane 0 issues
+// tcgen05.mma (kind::f16, M = 128, N = token tile, K = 16 per instruction)
+// from the stages, handing each stage back with tcgen05.commit to its empty
+// mbarrier.  The fp32 sums of consecutive items alternate between two TMEM
+// accumulators (256 columns each): a commit marks one full, the epilogue
+// reads it with tcgen05.ld and marks it empty, so the epilogue of one item
+// overlaps the mainloop of the next and the ring never drains between items.
+// Long K with few weight tiles splits over items; the last split of a tile
+// adds the fp32 partials in split order.  Weight tiles never straddle a
+// segment (q/k/v stacked, or gate/up for SiLU-GLU: 64 gate rows + 64 up rows
+// per tile, the up half handed to the gate half through shared memory).
 //
 // Int4 weights (group 64, one group per K chunk): TMA moves the packed codes
-// (32 bytes per row and chunk) beside the activations, and converter warps
-// turn them into the bf16 A tile, bf16((q - z) * s) for their row's group
-// scale and zero, written straight into the 128-byte swizzled layout the MMA
-// descriptor reads.  Each converter fences its shared-memory writes into the
-// async proxy and arrives on the stage's converted barrier, which the MMA lane
-// waits on as well as the TMA barrier.  With int4, eight converter warps (two
-// threads per row) fill the tile, warps 0..3 of them also run the epilogue,
-// and warps 8 and 9 lend lane 0 to the producer and the MMA issuer.
+// (32 bytes per row and chunk, 32-byte swizzle) beside the activations, and
+// four converter warps (one thread per row) turn them into the bf16 A tile,
+// bf16((q - z) * s) for their row's group scale and zero, written straight
+// into the 128-byte swizzled layout the MMA descriptor reads.  Each converter
+// fences its shared-memory writes into the async proxy and arrives on the
+// stage's converted barrier, which the MMA lane waits on as well as the TMA
+// barrier.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <algorithm>
@@ -39,7 +43,6 @@ namespace sub {
 
 namespace {
 
-constexpr int TC_THREADS = 128;
 constexpr int TC_BM = 128;                 // weight rows per tile (TMEM lanes)
 constexpr int TC_BK = 64;                  // K columns per stage (128 B per row)
 constexpr int TC_TN = 256;                 // token rows per tile (max MMA N)
@@ -47,14 +50,18 @@ constexpr int A_BYTES = TC_BM * TC_BK * 2;     // 16 KB
 constexpr int B_BYTES = TC_TN * TC_BK * 2;     // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TC_STAGES = 4;
-constexpr int TC_SMEM = 1024 + TC_STAGES * STAGE_BYTES + 256;   // + barriers, TMEM address
-constexpr int TMEM_COLS = 256;
+constexpr int XCH_BYTES = 64 * 64 * 4;     // GLU epilogue exchange: 64 up rows x 64 tokens
+constexpr int TC_SMEM = 1024 + TC_STAGES * STAGE_BYTES + XCH_BYTES + 256;   // + barriers, TMEM address
+constexpr int TMEM_COLS = 2 * TC_TN;       // two accumulators
 // int4 weights: the stage also holds the packed codes of its 128 rows
 constexpr int Q_BYTES = TC_BM * 32;                              // 4 KB
 constexpr int STAGE_BYTES_W4 = A_BYTES + B_BYTES + Q_BYTES;      // 52 KB
-constexpr int TC_CONV_WARPS = 8;                                 // two threads per row
-constexpr int TC_THREADS_W4 = (TC_CONV_WARPS + 2) * 32;
-constexpr int TC_SMEM_W4 = 1024 + TC_STAGES * STAGE_BYTES_W4 + 256;
+constexpr int TC_EPI_WARPS = 4;                                  // one per TMEM lane quarter
+constexpr int TC_CONV_WARPS = 4;                                 // one thread per row
+constexpr int TC_THREADS = (TC_EPI_WARPS + 2) * 32;              // + producer, MMA issuer
+constexpr int TC_THREADS_W4 = (TC_EPI_WARPS + TC_CONV_WARPS + 2) * 32;
+constexpr int TC_SMEM_W4 = 1024 + TC_STAGES * STAGE_BYTES_W4 + XCH_BYTES + 256;
+static_assert(8 * (3 * TC_STAGES + 4) + 4 <= 256, "barriers and the TMEM address fit the tail");
 static_assert(STAGE_BYTES_W4 % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
 static_assert(TC_SMEM_W4 <= 227 * 1024, "int4 ring must fit one CTA's shared memory");
 
@@ -189,6 +196,8 @@ struct TcPlan {
   int chunks;         // K chunks of 64 columns
   int per_split;      // chunks per split of K
   int xrows;          // token rows of the activation box
+  int ntx, nty, ks;   // token tiles, weight tiles, splits of K
+  int items;          // ntx * nty * ks work items, shared round-robin by the CTAs
 };
 
 template <int EPI, bool W4>
@@ -197,29 +206,44 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const GemvArgs a, const TcPl
   constexpr bool GLU = EPI == EPI_GLU;
   constexpr int HALF = GLU ? TC_BM / 2 : TC_BM;   // rows of one segment in a tile
   constexpr int SB = W4 ? STAGE_BYTES_W4 : STAGE_BYTES;
-  constexpr int PROD_WARP = W4 ? TC_CONV_WARPS : 0;
+  constexpr int PROD_WARP = TC_EPI_WARPS + (W4 ? TC_CONV_WARPS : 0);
   constexpr int MMA_WARP = PROD_WARP + 1;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* const base_ptr = smem_raw + (base - smem_u32(smem_raw));
-  const uint32_t bars = base + TC_STAGES * SB;   // full[S], empty[S], converted[S], done
+  float* const xch = reinterpret_cast<float*>(base_ptr + TC_STAGES * SB);   // GLU exchange
+  // full[S], empty[S], converted[S], accumulator full[2], accumulator empty[2]
+  const uint32_t bars = base + TC_STAGES * SB + XCH_BYTES;
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto empty_bar = [&](int s) { return bars + 8u * (TC_STAGES + s); };
   auto conv_bar = [&](int s) { return bars + 8u * (2 * TC_STAGES + s); };
-  const uint32_t done_bar = bars + 8u * (3 * TC_STAGES);
-  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + TC_STAGES * SB + 128);
-  float* const xch = reinterpret_cast<float*>(base_ptr);   // epilogue exchange (reuses stage 0)
+  auto accf_bar = [&](int b) { return bars + 8u * (3 * TC_STAGES + b); };
+  auto acce_bar = [&](int b) { return bars + 8u * (3 * TC_STAGES + 2 + b); };
+  uint32_t* const tmem_slot =
+      reinterpret_cast<uint32_t*>(base_ptr + TC_STAGES * SB + XCH_BYTES + 8 * (3 * TC_STAGES + 4));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tok0 = blockIdx.x * TC_TN;
-  const int tn = min(TC_TN, ((a.M - tok0) + 15) / 16 * 16);   // MMA N (multiple of 16)
-  const int tile = blockIdx.y;
-  int seg = 0;
-  while (seg < 2 && tile >= pl.blk_end[seg]) ++seg;
-  const int r0 = (tile - (seg ? pl.blk_end[seg - 1] : 0)) * HALF;   // first row in the segment
-  const int ks = gridDim.z, kz = blockIdx.z;
-  const int c0 = kz * pl.per_split, c1 = min(pl.chunks, c0 + pl.per_split);
-  const int nck = max(0, c1 - c0);
+
+  // work item w -> token tile, weight tile, split of K (token tiles fastest,
+  // so the CTAs running one weight tile's token tiles share it in L2)
+  struct Item {
+    int tok0, tn, tile, seg, r0, kz, c0, nck;
+  };
+  auto item = [&](int w) {
+    Item d;
+    const int tx = w % pl.ntx, rest = w / pl.ntx;
+    d.tile = rest % pl.nty;
+    d.kz = rest / pl.nty;
+    d.tok0 = tx * TC_TN;
+    d.tn = min(TC_TN, ((a.M - d.tok0) + 15) / 16 * 16);   // MMA N (multiple of 16)
+    d.seg = 0;
+    while (d.seg < 2 && d.tile >= pl.blk_end[d.seg]) ++d.seg;
+    d.r0 = (d.tile - (d.seg ? pl.blk_end[d.seg - 1] : 0)) * HALF;   // first row in the segment
+    d.c0 = d.kz * pl.per_split;
+    d.nck = max(0, min(pl.chunks, d.c0 + pl.per_split) - d.c0);
+    return d;
+  };
+  const int ks = pl.ks;
 
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -234,7 +258,10 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const GemvArgs a, const TcPl
       mbar_init(empty_bar(s), 1);
       mbar_init(conv_bar(s), TC_CONV_WARPS * 32);
     }
-    mbar_init(done_bar, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf_bar(b), 1);
+      mbar_init(acce_bar(b), TC_EPI_WARPS);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   tc_fence_before();
@@ -243,229 +270,265 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const GemvArgs a, const TcPl
   const uint32_t tmem = *tmem_slot;
 
   // The producer and the MMA issuer are lane 0 of their warps; the other
-  // lanes wait at the warp barrier (not on the done barrier) so they never
-  // compete with the working lane's instruction stream.
-  if (warp == PROD_WARP && lane == 0) {
-    // ---------------------------------------------------------- producer
-    auto issue = [&](int i, bool weights, bool acts) {
-      const int s = i % TC_STAGES, c = c0 + i, kx = c * TC_BK;
-      const uint32_t st = base + s * SB, fb = full_bar(s);
-      if (weights) {
-        mbar_expect_tx(fb, W4 ? Q_BYTES + B_BYTES : STAGE_BYTES);
-        for (int h = 0; h < (GLU ? 2 : 1); ++h) {
-          if constexpr (W4)
-            tma_load_2d(st + A_BYTES + B_BYTES + h * HALF * 32, &maps.w[GLU ? h : seg], c * 32, r0,
-                        fb);
-          else
-            tma_load_2d(st + h * HALF * 128, &maps.w[GLU ? h : seg], kx, r0, fb);
-        }
-      }
-      if (acts) {
-        // the activation box always moves TC_TN rows' worth of bytes: rows past
-        // the tensor (and past the box) arrive as zeros
-        for (int y = 0; y < TC_TN; y += pl.xrows)
-          tma_load_2d(st + A_BYTES + y * 128, &maps.x, kx, tok0 + y, fb);
-      }
-    };
-    const int npre = min(TC_STAGES, nck);
-    for (int i = 0; i < npre; ++i) issue(i, true, false);   // weights before the wait
-    pdl_wait();
-    for (int i = 0; i < npre; ++i) issue(i, false, true);
-    for (int i = npre; i < nck; ++i) {
-      mbar_wait(empty_bar(i % TC_STAGES), ((i / TC_STAGES) - 1) & 1);
-      issue(i, true, true);
-    }
-  } else if (warp == MMA_WARP && lane == 0) {
-    // ---------------------------------------------------------- MMA issuer
-    const uint32_t idesc = idesc_bf16(tn);
-    for (int i = 0; i < nck; ++i) {
-      const int s = i % TC_STAGES;
-      mbar_wait(full_bar(s), (i / TC_STAGES) & 1);
-      if constexpr (W4) mbar_wait(conv_bar(s), (i / TC_STAGES) & 1);
-      tc_fence_after();
-      const uint32_t st = base + s * SB;
-#pragma unroll
-      for (int kk = 0; kk < TC_BK / 16; ++kk)
-        tc_mma(tmem, smem_desc_sw128(st + kk * 32), smem_desc_sw128(st + A_BYTES + kk * 32), idesc,
-               (i > 0 || kk > 0) ? 1u : 0u);
-      tc_commit(empty_bar(s));   // the stage is free once these MMAs have read it
-    }
-    tc_commit(done_bar);
-  } else if (W4 && warp < TC_CONV_WARPS) {
-    // ---------------------------------------------------------- converters
-    // thread pair = row of the tile (half a row each); the group's scale and
-    // zero come one chunk ahead
-    constexpr int CPT = 8 / (TC_CONV_WARPS / 4);   // 16-byte output chunks per thread
-    const int rr = threadIdx.x & (TC_BM - 1), part = threadIdx.x >> 7;
-    const int sseg = GLU ? (rr >= HALF ? 1 : 0) : seg;
-    const int rs = r0 + (GLU ? (rr & (HALF - 1)) : rr);
-    const int rows = GLU ? a.N : a.seg_end[sseg] - (sseg ? a.seg_end[sseg - 1] : 0);
-    const int G = (a.K + TC_BK - 1) / TC_BK;   // groups per row = K chunks
-    const bool ok = rs < rows;
-    const uint16_t* const sp = a.S[sseg] + (int64_t)(ok ? rs : 0) * G;
-    const uint16_t* const zp = a.Z[sseg] + (int64_t)(ok ? rs : 0) * G;
-    uint16_t sv = 0, zv = 0;
-    if (ok && nck > 0) {
-      sv = __ldg(sp + c0);
-      zv = __ldg(zp + c0);
-    }
-    for (int i = 0; i < nck; ++i) {
-      const int s = i % TC_STAGES;
-      const float sc = bf16_bits_to_f32(sv), zc = bf16_bits_to_f32(zv);
-      if (ok && i + 1 < nck) {
-        sv = __ldg(sp + c0 + i + 1);
-        zv = __ldg(zp + c0 + i + 1);
-      }
-      mbar_wait(full_bar(s), (i / TC_STAGES) & 1);
-      uint8_t* const st = base_ptr + s * SB;
-      // the codes arrive with the 32-byte swizzle: 16-byte half h of row rr
-      // sits at half h ^ ((rr >> 2) & 1), so eight consecutive rows of one
-      // read phase cover all 32 banks
-      const uint8_t* const qrow = st + A_BYTES + B_BYTES + rr * 32;
-      uint32_t words[CPT];
-#pragma unroll
-      for (int v = 0; v < CPT / 4; ++v) {
-        const int hf = part * (CPT / 4) + v;   // 16-byte half of the row's 32 bytes
-        const uint4 q = *reinterpret_cast<const uint4*>(qrow + ((hf ^ ((rr >> 2) & 1)) << 4));
-        words[4 * v] = q.x;
-        words[4 * v + 1] = q.y;
-        words[4 * v + 2] = q.z;
-        words[4 * v + 3] = q.w;
-      }
-      uint8_t* const arow = st + rr * 128;
-#pragma unroll
-      for (int c = 0; c < CPT; ++c) {   // 16-byte chunk j of the row sits at chunk j ^ (row % 8)
-        const int j = part * CPT + c;
-        *reinterpret_cast<uint4*>(arow + ((j ^ (rr & 7)) << 4)) = dequant8(words[c], sc, zc);
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive(conv_bar(s));
-    }
-  }
-  __syncwarp();
-  pdl_wait();   // every thread: the epilogue reads what earlier kernels wrote
-  pdl_trigger();
-
-  // ------------------------------------------------------------ epilogue
-  if (warp < 4) {
-    if (nck > 0) mbar_wait(done_bar, 0);
-    __syncwarp();
-    tc_fence_after();
-    const int lrow = warp * 32 + lane;                          // TMEM lane = row of the tile
-    const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
-    const int seg_rows = GLU ? a.N : a.seg_end[seg] - (seg ? a.seg_end[seg - 1] : 0);
-    const int seg_start = GLU ? 0 : (seg ? a.seg_end[seg - 1] : 0);
-    const int rs = r0 + (GLU ? (lrow & (HALF - 1)) : lrow);     // row within the segment
-    const bool row_ok = rs < seg_rows;
-    const int n_glob = seg_start + rs;
-
-    // split of K: park fp32 partials [tile][split][token][row], the last split sums
-    bool last = true;
-    float* part = nullptr;
-    if (ks > 1) {
-      const size_t tile_lin = (size_t)blockIdx.y * gridDim.x + blockIdx.x;
-      part = a.split_part + tile_lin * ks * (size_t)(TC_TN * TC_BM);
-      float* mine = part + (size_t)kz * (TC_TN * TC_BM);
-      for (int cb = 0; cb < tn; cb += 16) {
-        float v[16];
-        if (nck > 0) tc_ld16(taddr + cb, v);
-        else
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = 0.f;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) __stcg(mine + (size_t)(cb + j) * TC_BM + lrow, v[j]);
-      }
-      __shared__ unsigned int s_last;
-      epi_bar();
-      if (threadIdx.x == 0) {
-        __threadfence();
-        s_last = (atomicAdd(a.split_cnt + tile_lin, 1u) == (unsigned)ks - 1) ? 1u : 0u;
-        __threadfence();
-      }
-      epi_bar();
-      last = s_last != 0;
-      if (last && threadIdx.x == 0) a.split_cnt[tile_lin] = 0u;
-    }
-
-    if (last) {
-      // 64 columns (tokens) per round: four TMEM loads, or four splits' worth of
-      // partial sums, and all their global loads in flight together
-      for (int cg = 0; cg < tn; cg += 64) {
-        const int ncol = min(64, tn - cg);   // a multiple of 16
-        float v[64];
-        if (ks > 1) {
-#pragma unroll
-          for (int j = 0; j < 64; ++j) v[j] = 0.f;
-          for (int z = 0; z < ks; ++z) {
-            float p[64];
-#pragma unroll
-            for (int j = 0; j < 64; ++j)
-              p[j] = j < ncol ? __ldcg(part + ((size_t)z * TC_TN + cg + j) * TC_BM + lrow) : 0.f;
-#pragma unroll
-            for (int j = 0; j < 64; ++j) v[j] += p[j];
-          }
-        } else {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            float t[16];
-            if (q * 16 < ncol) tc_ld16(taddr + cg + q * 16, t);
+  // lanes go straight to the final barrier, so they never compete with the
+  // working lane's instruction stream.
+  if (warp == PROD_WARP) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- producer
+      auto issue = [&](const Item& d, int i, int it, bool weights, bool acts) {
+        const int s = it % TC_STAGES, c = d.c0 + i, kx = c * TC_BK;
+        const uint32_t st = base + s * SB, fb = full_bar(s);
+        if (weights) {
+          mbar_expect_tx(fb, W4 ? Q_BYTES + B_BYTES : STAGE_BYTES);
+          for (int h = 0; h < (GLU ? 2 : 1); ++h) {
+            if constexpr (W4)
+              tma_load_2d(st + A_BYTES + B_BYTES + h * HALF * 32, &maps.w[GLU ? h : d.seg], c * 32,
+                          d.r0, fb);
             else
-#pragma unroll
-              for (int j = 0; j < 16; ++j) t[j] = 0.f;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) v[q * 16 + j] = t[j];
+              tma_load_2d(st + h * HALF * 128, &maps.w[GLU ? h : d.seg], kx, d.r0, fb);
           }
         }
-        if constexpr (GLU) {
-          // up rows (lanes 64..127) hand their values to the gate rows (lanes 0..63)
-          epi_bar();
-          if (lrow >= HALF)
-#pragma unroll
-            for (int j = 0; j < 64; ++j) xch[j * HALF + (lrow - HALF)] = v[j];
-          epi_bar();
-          if (lrow < HALF && row_ok) {
-#pragma unroll
-            for (int j = 0; j < 64; ++j) {
-              const int m = tok0 + cg + j;
-              if (j < ncol && m < a.M)
-                reinterpret_cast<__nv_bfloat16*>(a.Y)[(int64_t)m * a.ldy + rs] =
-                    __float2bfloat16_rn(silu_f(v[j]) * xch[j * HALF + lrow]);
-            }
+        if (acts) {
+          // the activation box always moves TC_TN rows' worth of bytes: rows past
+          // the tensor (and past the box) arrive as zeros
+          for (int y = 0; y < TC_TN; y += pl.xrows)
+            tma_load_2d(st + A_BYTES + y * 128, &maps.x, kx, d.tok0 + y, fb);
+        }
+      };
+      int it = 0;   // chunks issued so far (stage it % S, round it / S)
+      int w = blockIdx.x;
+      if (w < pl.items) {
+        // the first item's first stages: weights before the wait on the
+        // producing kernel, activations after it
+        const Item d = item(w);
+        const int npre = min(TC_STAGES, d.nck);
+        for (int i = 0; i < npre; ++i) issue(d, i, i, true, false);
+        pdl_wait();
+        for (int i = 0; i < npre; ++i) issue(d, i, i, false, true);
+        it = npre;
+        for (int i = npre; i < d.nck; ++i, ++it) {
+          mbar_wait(empty_bar(it % TC_STAGES), ((it / TC_STAGES) - 1) & 1);
+          issue(d, i, it, true, true);
+        }
+        for (w += gridDim.x; w < pl.items; w += gridDim.x) {
+          const Item e = item(w);
+          for (int i = 0; i < e.nck; ++i, ++it) {
+            if (it >= TC_STAGES) mbar_wait(empty_bar(it % TC_STAGES), ((it / TC_STAGES) - 1) & 1);
+            issue(e, i, it, true, true);
           }
-        } else if (row_ok) {
-          if constexpr (EPI == EPI_RESID) {
-            // all old values first: a load after a store to Y would wait for it
-            float* const Y = reinterpret_cast<float*>(a.Y);
-            float y[64];
+        }
+      } else {
+        pdl_wait();
+      }
+    }
+  } else if (warp == MMA_WARP) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      int it = 0, t = 0;   // chunks consumed, items done
+      for (int w = blockIdx.x; w < pl.items; w += gridDim.x, ++t) {
+        const Item d = item(w);
+        const int ab = t & 1;
+        // accumulator ab is free once the epilogue has read item t - 2
+        if (t >= 2) mbar_wait(acce_bar(ab), ((t >> 1) - 1) & 1);
+        tc_fence_after();
+        const uint32_t acc = tmem + (uint32_t)(ab * TC_TN);
+        const uint32_t idesc = idesc_bf16(d.tn);
+        for (int i = 0; i < d.nck; ++i, ++it) {
+          const int s = it % TC_STAGES;
+          mbar_wait(full_bar(s), (it / TC_STAGES) & 1);
+          if constexpr (W4) mbar_wait(conv_bar(s), (it / TC_STAGES) & 1);
+          tc_fence_after();
+          const uint32_t st = base + s * SB;
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-              const int m = tok0 + cg + j;
-              y[j] = (j < ncol && m < a.M) ? __ldcg(Y + (int64_t)m * a.ldy + n_glob) : 0.f;
-            }
+          for (int kk = 0; kk < TC_BK / 16; ++kk)
+            tc_mma(acc, smem_desc_sw128(st + kk * 32), smem_desc_sw128(st + A_BYTES + kk * 32),
+                   idesc, (i > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(empty_bar(s));   // the stage is free once these MMAs have read it
+        }
+        tc_commit(accf_bar(ab));     // the item's sums are complete
+      }
+    }
+  } else if (W4 && warp >= TC_EPI_WARPS) {
+    // ---------------------------------------------------------- converters
+    // thread = row of the tile; the group's scale and zero come one chunk ahead
+    const int rr = threadIdx.x - TC_EPI_WARPS * 32;
+    const int G = (a.K + TC_BK - 1) / TC_BK;   // groups per row = K chunks
+    int it = 0;
+    for (int w = blockIdx.x; w < pl.items; w += gridDim.x) {
+      const Item d = item(w);
+      const int sseg = GLU ? (rr >= HALF ? 1 : 0) : d.seg;
+      const int rs = d.r0 + (GLU ? (rr & (HALF - 1)) : rr);
+      const int rows = GLU ? a.N : a.seg_end[sseg] - (sseg ? a.seg_end[sseg - 1] : 0);
+      const bool ok = rs < rows;
+      const uint16_t* const sp = a.S[sseg] + (int64_t)(ok ? rs : 0) * G;
+      const uint16_t* const zp = a.Z[sseg] + (int64_t)(ok ? rs : 0) * G;
+      uint16_t sv = 0, zv = 0;
+      if (ok && d.nck > 0) {
+        sv = __ldg(sp + d.c0);
+        zv = __ldg(zp + d.c0);
+      }
+      for (int i = 0; i < d.nck; ++i, ++it) {
+        const int s = it % TC_STAGES;
+        const float sc = bf16_bits_to_f32(sv), zc = bf16_bits_to_f32(zv);
+        if (ok && i + 1 < d.nck) {
+          sv = __ldg(sp + d.c0 + i + 1);
+          zv = __ldg(zp + d.c0 + i + 1);
+        }
+        mbar_wait(full_bar(s), (it / TC_STAGES) & 1);
+        uint8_t* const st = base_ptr + s * SB;
+        // the codes arrive with the 32-byte swizzle: 16-byte half h of row rr
+        // sits at half h ^ ((rr >> 2) & 1), so eight consecutive rows of one
+        // read phase cover all 32 banks
+        const uint8_t* const qrow = st + A_BYTES + B_BYTES + rr * 32;
+        const int flip = (rr >> 2) & 1;
+        const uint4 q0 = *reinterpret_cast<const uint4*>(qrow + (flip << 4));
+        const uint4 q1 = *reinterpret_cast<const uint4*>(qrow + ((1 ^ flip) << 4));
+        const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        uint8_t* const arow = st + rr * 128;
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-              const int m = tok0 + cg + j;
-              if (j < ncol && m < a.M) Y[(int64_t)m * a.ldy + n_glob] = y[j] + v[j];
+        for (int c = 0; c < 8; ++c)   // 16-byte chunk c of the row sits at chunk c ^ (row % 8)
+          *reinterpret_cast<uint4*>(arow + ((c ^ (rr & 7)) << 4)) = dequant8(words[c], sc, zc);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive(conv_bar(s));
+      }
+    }
+  } else if (warp < TC_EPI_WARPS) {
+    // ------------------------------------------------------------ epilogue
+    pdl_wait();   // the epilogue reads what earlier kernels wrote
+    // Dependents may launch from here on.  Only threads past their own wait
+    // signal it: a later kernel reads some inputs before its wait (the tree
+    // of the attention kernel) and counts on everything before this kernel's
+    // predecessor having finished when it starts.
+    pdl_trigger();
+    const int lrow = warp * 32 + lane;   // TMEM lane = row of the tile
+    int t = 0;
+    for (int w = blockIdx.x; w < pl.items; w += gridDim.x, ++t) {
+      const Item d = item(w);
+      const int ab = t & 1;
+      mbar_wait(accf_bar(ab), (t >> 1) & 1);
+      __syncwarp();
+      tc_fence_after();
+      const uint32_t taddr = tmem + (uint32_t)(ab * TC_TN) + ((uint32_t)(warp * 32) << 16);
+      const int seg = d.seg, r0 = d.r0, tok0 = d.tok0, tn = d.tn, nck = d.nck, kz = d.kz;
+      const int seg_rows = GLU ? a.N : a.seg_end[seg] - (seg ? a.seg_end[seg - 1] : 0);
+      const int seg_start = GLU ? 0 : (seg ? a.seg_end[seg - 1] : 0);
+      const int rs = r0 + (GLU ? (lrow & (HALF - 1)) : lrow);     // row within the segment
+      const bool row_ok = rs < seg_rows;
+      const int n_glob = seg_start + rs;
+
+      // split of K: park fp32 partials [tile][split][token][row], the last split sums
+      bool last = true;
+      float* part = nullptr;
+      if (ks > 1) {
+        const size_t tile_lin = (size_t)d.tile * pl.ntx + (size_t)(tok0 / TC_TN);
+        part = a.split_part + tile_lin * ks * (size_t)(TC_TN * TC_BM);
+        float* mine = part + (size_t)kz * (TC_TN * TC_BM);
+        for (int cb = 0; cb < tn; cb += 16) {
+          float v[16];
+          if (nck > 0) tc_ld16(taddr + cb, v);
+          else
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = 0.f;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) __stcg(mine + (size_t)(cb + j) * TC_BM + lrow, v[j]);
+        }
+        __shared__ unsigned int s_last;
+        epi_bar();
+        if (threadIdx.x == 0) {
+          __threadfence();
+          s_last = (atomicAdd(a.split_cnt + tile_lin, 1u) == (unsigned)ks - 1) ? 1u : 0u;
+          __threadfence();
+        }
+        epi_bar();
+        last = s_last != 0;
+        if (last && threadIdx.x == 0) a.split_cnt[tile_lin] = 0u;
+      }
+
+      if (last) {
+        // 64 columns (tokens) per round: four TMEM loads, or four splits' worth of
+        // partial sums, and all their global loads in flight together
+        for (int cg = 0; cg < tn; cg += 64) {
+          const int ncol = min(64, tn - cg);   // a multiple of 16
+          float v[64];
+          if (ks > 1) {
+#pragma unroll
+            for (int j = 0; j < 64; ++j) v[j] = 0.f;
+            for (int z = 0; z < ks; ++z) {
+              float p[64];
+#pragma unroll
+              for (int j = 0; j < 64; ++j)
+                p[j] = j < ncol ? __ldcg(part + ((size_t)z * TC_TN + cg + j) * TC_BM + lrow) : 0.f;
+#pragma unroll
+              for (int j = 0; j < 64; ++j) v[j] += p[j];
             }
           } else {
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-              const int m = tok0 + cg + j;
-              if (j >= ncol || m >= a.M) continue;
-              const int64_t o = (int64_t)m * a.ldy + n_glob;
-              if constexpr (EPI == EPI_BF16) {
-                reinterpret_cast<__nv_bfloat16*>(a.Y)[o] = __float2bfloat16_rn(v[j]);
-              } else {
-                reinterpret_cast<float*>(a.Y)[o] = v[j];
+            for (int q = 0; q < 4; ++q) {
+              float tv[16];
+              if (q * 16 < ncol && nck > 0) tc_ld16(taddr + cg + q * 16, tv);
+              else
+#pragma unroll
+                for (int j = 0; j < 16; ++j) tv[j] = 0.f;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v[q * 16 + j] = tv[j];
+            }
+          }
+          if constexpr (GLU) {
+            // up rows (lanes 64..127) hand their values to the gate rows (lanes 0..63)
+            epi_bar();
+            if (lrow >= HALF)
+#pragma unroll
+              for (int j = 0; j < 64; ++j) xch[j * HALF + (lrow - HALF)] = v[j];
+            epi_bar();
+            if (lrow < HALF && row_ok) {
+#pragma unroll
+              for (int j = 0; j < 64; ++j) {
+                const int m = tok0 + cg + j;
+                if (j < ncol && m < a.M)
+                  reinterpret_cast<__nv_bfloat16*>(a.Y)[(int64_t)m * a.ldy + rs] =
+                      __float2bfloat16_rn(silu_f(v[j]) * xch[j * HALF + lrow]);
+              }
+            }
+          } else if (row_ok) {
+            if constexpr (EPI == EPI_RESID) {
+              // all old values first: a load after a store to Y would wait for it
+              float* const Y = reinterpret_cast<float*>(a.Y);
+              float y[64];
+#pragma unroll
+              for (int j = 0; j < 64; ++j) {
+                const int m = tok0 + cg + j;
+                y[j] = (j < ncol && m < a.M) ? __ldcg(Y + (int64_t)m * a.ldy + n_glob) : 0.f;
+              }
+#pragma unroll
+              for (int j = 0; j < 64; ++j) {
+                const int m = tok0 + cg + j;
+                if (j < ncol && m < a.M) Y[(int64_t)m * a.ldy + n_glob] = y[j] + v[j];
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 64; ++j) {
+                const int m = tok0 + cg + j;
+                if (j >= ncol || m >= a.M) continue;
+                const int64_t o = (int64_t)m * a.ldy + n_glob;
+                if constexpr (EPI == EPI_BF16) {
+                  reinterpret_cast<__nv_bfloat16*>(a.Y)[o] = __float2bfloat16_rn(v[j]);
+                } else {
+                  reinterpret_cast<float*>(a.Y)[o] = v[j];
+                }
               }
             }
           }
         }
       }
+      // this item's accumulator may take item t + 2
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce_bar(ab));
     }
   }
   tc_fence_before();
   __syncthreads();
+  tc_fence_after();
   if (warp == 0)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS)
                  : "memory");
@@ -609,7 +672,11 @@ static bool tc_plan(const GemvArgs& a, bool w4, int epi, TcPlan* pl, dim3* grid,
   pl->per_split = (pl->chunks + ks - 1) / ks;
   ks = (pl->chunks + pl->per_split - 1) / pl->per_split;
   need = ks > 1 ? (size_t)ctas * ks * TC_TN * TC_BM : 0;
-  *grid = dim3(tok_tiles, nb, ks);
+  pl->ntx = tok_tiles;
+  pl->nty = nb;
+  pl->ks = ks;
+  pl->items = ctas * ks;
+  *grid = dim3(std::min(pl->items, tc_sm_count()));   // persistent: one CTA per SM at most
   *scratch = need;
   return true;
 }
