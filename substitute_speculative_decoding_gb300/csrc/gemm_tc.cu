@@ -395,17 +395,19 @@ gemm_tc_kernel(const __grid_constant__ TcMaps maps, const GemvArgs a, const TcPl
   } else if (warp < TC_EPI_WARPS) {
     // ------------------------------------------------------------ epilogue
     pdl_wait();   // the epilogue reads what earlier kernels wrote
-    // Dependents may launch from here on.  Only threads past their own wait
-    // signal it: a later kernel reads some inputs before its wait (the tree
-    // of the attention kernel) and counts on everything before this kernel's
-    // predecessor having finished when it starts.
-    pdl_trigger();
     const int lrow = warp * 32 + lane;   // TMEM lane = row of the tile
     int t = 0;
     for (int w = blockIdx.x; w < pl.items; w += gridDim.x, ++t) {
       const Item d = item(w);
       const int ab = t & 1;
       mbar_wait(accf_bar(ab), (t >> 1) & 1);
+      // Dependents may launch once this CTA's last mainloop is done.  Only
+      // threads past their own wait signal it: a later kernel reads some
+      // inputs before its wait (the tree of the attention kernel) and counts on
+      // everything before this kernel's predecessor having finished; and
+      // dependents launched earlier would sit on these SMs for the whole
+      // persistent run.
+      if (w + (int)gridDim.x >= pl.items) pdl_trigger();
       __syncwarp();
       tc_fence_after();
       const uint32_t taddr = tmem + (uint32_t)(ab * TC_TN) + ((uint32_t)(warp * 32) << 16);
