@@ -62,8 +62,10 @@ __global__ void __launch_bounds__(THREADS) tree_attn_kernel(AttnArgs a) {
   // Programmatic dependent launch: only Q and the K/V of the query rows' own
   // slots come from the kernel just before this one (the q/k/v projection).
   // The tree (ancestors, depths), the page table, the counters and every other
-  // key were written by kernels that finished before that one started, so they
-  // are read before the wait.
+  // key were written by kernels that finished before that one's own
+  // predecessor did, so they are read before the wait.  This holds because the
+  // projections (TMA GEMV, tcgen05 GEMM) signal their dependents only from
+  // threads that have passed their own wait.
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int kvh = blockIdx.y;
   const int G = a.n_heads_q / a.n_heads_kv;
