@@ -184,7 +184,7 @@ __device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
 
 }  // namespace
 
-struct alignas(64) TcMaps {
+struct TcMaps {   // aligned as its CUtensorMap members
   CUtensorMap w[3];   // weight segments: [rows, K] bf16, box 64 x (128 or 64 rows);
                       // int4: packed codes [rows, K/2] bytes, box 32 x (128 or 64 rows)
   CUtensorMap x;      // activations [M, K] bf16, box 64 x token-tile rows
