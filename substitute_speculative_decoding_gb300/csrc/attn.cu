@@ -14,7 +14,7 @@
 // heads that share a KV head read each K/V tile once.  A CTA of four warps
 // owns 64 rows; S = Q K^T and O += P V run on mma.sync m16n8k16 with fp32
 // accumulators and an online softmax in fp32 (FlashAttention-2 style).  Keys
-// may be split over up to 8 CTAs (grid.z) that form one thread-block cluster;
+// may be split over up to 16 CTAs (grid.z) that form one thread-block cluster;
 // their partial (max, sum, O) are merged in split order through distributed
 // shared memory, so no global scratch and no second launch are needed.
 #include <mutex>
@@ -59,13 +59,15 @@ __global__ void __launch_bounds__(THREADS) tree_attn_kernel(AttnArgs a) {
   uint32_t* sBits = reinterpret_cast<uint32_t*>(sV + 2 * KT * D * 2);
   auto sw = [](int row, int ch) { return row * CH + (ch ^ (row & 7)); };
 
-  // Programmatic dependent launch: only Q and the K/V of the query rows' own
-  // slots come from the kernel just before this one (the q/k/v projection).
-  // The tree (ancestors, depths), the page table, the counters and every other
-  // key were written by kernels that finished before that one's own
-  // predecessor did, so they are read before the wait.  This holds because the
-  // projections (TMA GEMV, tcgen05 GEMM) signal their dependents only from
-  // threads that have passed their own wait.
+  // Programmatic dependent launch (early_reads): only Q and the K/V of the
+  // query rows' own slots come from the kernel just before this one (the
+  // q/k/v projection).  The tree (ancestors, depths), the page table, the
+  // counters and every other key were written by kernels that finished before
+  // that one's own predecessor did, so they are read before the wait.  This
+  // holds because every kernel of the decode path signals its dependents only
+  // from threads that have passed their own wait.  A caller of the public
+  // entry point may have run anything just before, so there every read waits.
+  if (!a.early_reads) pdl_wait();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int kvh = blockIdx.y;
   const int G = a.n_heads_q / a.n_heads_kv;

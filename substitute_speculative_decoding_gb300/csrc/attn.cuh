@@ -25,6 +25,10 @@ struct AttnArgs {
   const int32_t* depth;         // [n_q] path length - 1 (with anc)
   int chain_slot0;              // chain mode: query i is slot chain_slot0 + i
   float scale;
+  // 1: read the tree, the page table and the keys of other slots before the
+  // launch wait (the model's decode path, whose predecessor is known to signal
+  // its dependents only after its own wait); 0: every read after the wait
+  int early_reads;
 };
 
 constexpr int ATTN_MAX_SMEM = 200 * 1024;

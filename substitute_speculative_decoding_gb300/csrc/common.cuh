@@ -26,8 +26,11 @@ inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s
 // ------------------------------------------- programmatic dependent launch --
 // Kernels of the decode path are launched with programmatic stream
 // serialisation: the next kernel may start while this one drains.  Every such
-// kernel calls pdl_trigger() early and pdl_wait() before it touches anything
-// an earlier kernel wrote (weights may be read before the wait).
+// kernel calls pdl_wait() before it touches anything an earlier kernel wrote
+// (weights may be read before the wait), and signals pdl_trigger() only from
+// threads that have passed their own pdl_wait().  By induction, when a kernel
+// starts, every kernel before its immediate predecessor has finished; the
+// attention kernel's reads ahead of its wait rely on exactly this.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;"); }
 

@@ -53,8 +53,8 @@ template <bool W4, int EPI>
 __global__ void __launch_bounds__(THREADS) gemm_kernel(GemvArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr bool GLU = (EPI == EPI_GLU);
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int wm = warp >> 2, wn = warp & 3;
   const int m0 = blockIdx.y * BM;

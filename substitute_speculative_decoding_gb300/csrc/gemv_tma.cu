@@ -272,6 +272,7 @@ gemv_tma_kernel(const __grid_constant__ TmaMaps maps, const GemvArgs a, const Tm
         issue(u, true, true);
       }
     }
+    __syncwarp();   // lanes 1..31 signal only once lane 0 has passed the wait
     pdl_trigger();
     return;
   }

@@ -19,8 +19,8 @@ __global__ void embed_kernel(const uint16_t* __restrict__ embed, int hidden, Row
                              float* __restrict__ x, const uint16_t* __restrict__ gain, float eps,
                              uint16_t* __restrict__ xn, float* __restrict__ ss_out) {
   __shared__ float s_part[32];
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.x;
   const int64_t tok = rs.tokens[r];
   const uint16_t* src = embed + tok * hidden;
@@ -55,8 +55,8 @@ int32_t launch_embed(const uint16_t* embed, int hidden, const RowSet& rs, int ro
 __global__ void rmsnorm_kernel(const float* __restrict__ x, const uint16_t* __restrict__ gain,
                                int hidden, float eps, uint16_t* __restrict__ out) {
   __shared__ float s_part[32];
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.x;
   const float* xr = x + (int64_t)r * hidden;
   float ss = 0.f;
@@ -82,8 +82,8 @@ int32_t launch_rmsnorm(const float* x, const uint16_t* gain, int rows, int hidde
 // One CTA per row: q heads get RoPE -> bf16 q_out; k heads RoPE -> cache;
 // v heads -> cache.  Rotate-half pairing: element i with i + D/2.
 __global__ void qkv_post_kernel(QkvPostArgs a) {
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.x;
   const int D = a.head_dim, half = D / 2;
   const int nh = a.n_heads_q + 2 * a.n_heads_kv;

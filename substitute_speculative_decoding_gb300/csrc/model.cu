@@ -339,6 +339,7 @@ static int32_t forward(sub_model* m, bool draft, const FwdRows& r, float* logits
   at.depth = r.depth;
   at.chain_slot0 = r.slot0;
   at.scale = 1.0f / sqrtf((float)D);
+  at.early_reads = 1;   // predecessors signal only after their own wait
   const int splits = attn_pick_splits(at, (int)std::min<int64_t>(r.keys_hint, 1 << 30));
 
   QkvPostArgs qp{};
@@ -484,8 +485,8 @@ static int32_t forward(sub_model* m, bool draft, const FwdRows& r, float* logits
 // ------------------------------------------------------------ tiny kernels --
 // After accept: committed length += accepted + 1, the bonus becomes the root.
 __global__ void advance_kernel(int32_t* state, int32_t* root_token) {
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   state[ST_N] += state[ST_NACC] + 1;
   *root_token = state[ST_BONUS];
 }

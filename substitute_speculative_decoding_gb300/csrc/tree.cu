@@ -95,8 +95,8 @@ __global__ void __launch_bounds__(EXP_THREADS) expand_kernel(ExpandArgs a) {
   __shared__ unsigned long long s_red[EXP_THREADS / 32];
   __shared__ float s_m[EXP_THREADS / 32], s_s[EXP_THREADS / 32];
   __shared__ unsigned int s_last;
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int k = a.tree.width;
   const int j = blockIdx.y, c = blockIdx.x;
   const int64_t V = a.V;
@@ -300,8 +300,8 @@ int accept_pick_chunks(int n_nodes, int64_t V) {
 __global__ void __launch_bounds__(ACC_THREADS) accept_kernel(AcceptArgs a) {
   __shared__ unsigned long long s_red[ACC_THREADS / 32];
   __shared__ unsigned int s_last;
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int u = blockIdx.y, c = blockIdx.x;
   const int64_t V = a.V;
   // chunks of whole 4-token Philox blocks
@@ -389,8 +389,8 @@ int32_t launch_accept(const AcceptArgs& a, cudaStream_t st) {
 // a destination that is also a later source cannot be clobbered.
 __global__ void compact_kernel(CompactArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int layer = blockIdx.x, h = blockIdx.y;
   const int n = min(*a.n_accepted, a.max_accept);
   if (n <= 0) return;
