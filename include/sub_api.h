@@ -52,6 +52,17 @@ const char* sub_last_error(void);
 /* Library version string and the compile target, e.g. "0.1 sm_103a". */
 const char* sub_version(void);
 
+/* Host-side fault injection for tests (no device fault is ever made): the
+ * environment variable SUB_FAULT, read at each call, makes a library call fail
+ * as if a CUDA call had failed:
+ *   SUB_FAULT=alloc:N  the N-th device allocation of sub_model_create (0-based)
+ *                      fails: the call returns SUB_ENOMEM and frees what it
+ *                      had allocated;
+ *   SUB_FAULT=h2d      every host-to-device copy of streamed originals fails:
+ *                      sub_prefill / sub_generate / target forwards return
+ *                      SUB_ECUDA; the model stays valid and can be destroyed.
+ * Unset (the default) costs one getenv per allocation or copy. */
+
 /* Pipeline waits that ran out on the current device since the library was
  * loaded.  Every wait inside the TMA-streamed GEMV and the tensor-core GEMM
  * (mbarrier phases, the grid-wide counters) is bounded: one that runs out
@@ -59,6 +70,14 @@ const char* sub_version(void);
  * hanging.  A correct run leaves it at 0; a non-zero value means the results
  * of that run are invalid.  *out receives the count. */
 int32_t sub_pipeline_timeouts(uint32_t* out);
+
+/* Check of the bounded-wait mechanism itself: one kernel thread waits on an
+ * mbarrier that nothing ever arrives on (and no copy targets), polling at most
+ * max_polls times (1 .. 2^20), with the same wait routine the pipelines use.
+ * The wait gives up, the kernel ends normally and the context stays usable:
+ * the call returns SUB_ETIMEOUT (SUB_OK would mean the barrier completed,
+ * which cannot happen).  It leaves sub_pipeline_timeouts unchanged. */
+int32_t sub_bounded_wait_check(uint32_t max_polls);
 
 /* ------------------------------------------------------------------------ */
 /* Int4 substitutes.  The draft replaces each offloaded target layer by a
@@ -173,9 +192,12 @@ int32_t sub_verify_accept(const float* logits, const sub_tree* tree, int32_t n_n
  * arguments, with its per-call scratch (partial argmax keys, the ticket
  * counter and, when choice == NULL, the choice array) taken from one fixed
  * array of device memory that the library holds for each device
- * (SUB_ACCEPT_STATIC_BYTES).  The pages have no counterpart: this is a
- * library convenience for callers that must not allocate inside the decode
- * loop.  Requirement: n_nodes * chunks * 8 + 64 (+ n_nodes * 4 without
+ * (SUB_ACCEPT_STATIC_BYTES, 256 KB; every device that loads the library
+ * keeps it until the process exits).  The paper has no counterpart: it is for
+ * callers that cannot allocate device memory while they decode -- a runtime
+ * that owns the device's memory through its own allocator and does not let
+ * libraries call cudaMalloc or cudaMallocAsync, or a decode loop that must not
+ * stall or fail on an allocation once it has started.  Requirement: n_nodes * chunks * 8 + 64 (+ n_nodes * 4 without
  * choice) <= SUB_ACCEPT_STATIC_BYTES, where chunks = the vocabulary chunks
  * per node (at most ceil(304 / n_nodes)); larger calls return SUB_EINVAL.
  * The first call on a device looks the array up (cudaGetSymbolAddress) and
@@ -220,7 +242,11 @@ typedef struct {
 typedef struct {
   int32_t n_layers, hidden, n_heads_q, n_heads_kv, head_dim, ffn, vocab, n_resident;
   float rope_theta, rms_eps;
-  const sub_bf16* embed;        /* device [vocab, hidden] */
+  const sub_bf16* embed;        /* [vocab, hidden]: device memory, or pinned host memory
+                                   (cudaHostAlloc / cudaHostRegister), which the
+                                   embedding kernel reads in place over the host
+                                   link, one row per token (saves vocab*hidden*2
+                                   bytes of device memory) */
   const sub_bf16* lm_head;      /* device [vocab, hidden] */
   const sub_bf16* final_norm;   /* device [hidden] */
   const sub_layer_desc* layers; /* host array [n_layers] */
@@ -270,6 +296,24 @@ typedef struct {
   double t_prefill_ms;
   double t_decode_ms;
   int64_t accept_hist[65];/* cycles that accepted a tokens, a <= 64 */
+  /* Per-phase device time summed over the cycles (CUDA events on the
+   * compute stream; -1 where the device could not time them):
+   *   t_draft_ms   the D draft levels (forwards + expansions),
+   *   t_verify_ms  the target pass over the tree (it waits for the streamed
+   *                originals of offloaded layers),
+   *   t_copy_unhidden_ms  the part of the verify spent waiting for those
+   *                copies: per offloaded layer, how long after the compute
+   *                stream reached the layer its copy finished (0 if before).
+   * t_draft_ms / t_verify_ms is the draft-to-target cost term
+   * D * t_draft_level / t_target of the speedup's denominator ("Low-Bit
+   * Shadow" report 7.1). */
+  double t_draft_ms;
+  double t_verify_ms;
+  double t_copy_unhidden_ms;
+  /* emitted tokens whose best and runner-up choice scores (logits, or
+   * logits / T + Gumbel noise) differed by less than 1e-2 on the device: the
+   * positions where a rounding difference could pick another token */
+  int64_t near_tie_events;
 } sub_stats;
 
 /* Step-wise decoding (the pieces sub_generate is made of).
@@ -300,7 +344,10 @@ int32_t sub_cycle_info(sub_model* model, const sub_decode_cfg* cfg, int64_t* ker
 /* Generate n_new tokens after prompt_host (int32 [n_prompt], host) into
  * out_tokens_host (int32 [n_new], host): prefill, then draft/verify/accept
  * cycles until n_new tokens are emitted (the first comes from the prefill;
- * the last cycle is truncated).  Synchronous.  stats may be NULL. */
+ * the last cycle is truncated).  Synchronous.  stats may be NULL.
+ * Returns SUB_ETIMEOUT (tokens and stats still written) when a bounded
+ * pipeline wait ran out during the call: the tokens are then not to be
+ * trusted.  sub_decode_read does the same check since the last prefill. */
 int32_t sub_generate(sub_model* model, const int32_t* prompt_host, int32_t n_prompt,
                      int32_t n_new, const sub_decode_cfg* cfg, int32_t* out_tokens_host,
                      sub_stats* stats);

@@ -73,7 +73,9 @@ class DecodeCfg(C.Structure):
 class Stats(C.Structure):
     _fields_ = [("cycles", _i64), ("emitted", _i64), ("tau", C.c_double),
                 ("t_prefill_ms", C.c_double), ("t_decode_ms", C.c_double),
-                ("accept_hist", _i64 * 65)]
+                ("accept_hist", _i64 * 65), ("t_draft_ms", C.c_double),
+                ("t_verify_ms", C.c_double), ("t_copy_unhidden_ms", C.c_double),
+                ("near_tie_events", _i64)]
 
 
 def _decl(name, args):
@@ -88,6 +90,7 @@ _lib.sub_last_error.argtypes = []
 _lib.sub_version.restype = C.c_char_p
 _lib.sub_version.argtypes = []
 _pipeline_timeouts = _decl("sub_pipeline_timeouts", [_vp])
+_bounded_wait_check = _decl("sub_bounded_wait_check", [C.c_uint32])
 
 _w4_pack = _decl("sub_w4_pack", [_vp, _i64, _i64, _i32, _vp, _vp, _vp, _vp])
 _w4_dequant = _decl("sub_w4_dequant", [_vp, _vp, _vp, _i64, _i64, _i32, _vp, _vp])
@@ -116,7 +119,8 @@ _decode_read = _decl("sub_decode_read", [_vp, _vp, _i32, C.POINTER(_i32), C.POIN
 _cycle_info = _decl("sub_cycle_info", [_vp, C.POINTER(DecodeCfg), C.POINTER(_i64),
                                        C.POINTER(_i64)])
 
-EXPORTED = ["sub_last_error", "sub_version", "sub_pipeline_timeouts", "sub_w4_pack", "sub_w4_dequant", "sub_w4_gemm",
+EXPORTED = ["sub_last_error", "sub_version", "sub_pipeline_timeouts", "sub_bounded_wait_check",
+            "sub_w4_pack", "sub_w4_dequant", "sub_w4_gemm",
             "sub_bf16_gemm", "sub_tree_attn", "sub_draft_expand", "sub_verify_accept",
             "sub_verify_accept_static",
             "sub_kv_compact", "sub_model_create", "sub_model_destroy", "sub_model_memory",
@@ -138,6 +142,12 @@ def pipeline_timeouts() -> int:
     n = C.c_uint32(0)
     _check(_pipeline_timeouts(C.byref(n)))
     return int(n.value)
+
+
+def bounded_wait_check(max_polls: int) -> int:
+    """Run the bounded-wait check kernel; returns its status code
+    (SUB_ETIMEOUT when the wait gave up, as it must)."""
+    return int(_bounded_wait_check(max_polls))
 
 
 def _p(t):
@@ -285,7 +295,8 @@ class Model:
     substitutes (packed here with the library's w4_pack) for the draft."""
 
     def __init__(self, cfg, weights: dict, max_seq: int, max_depth: int, max_width: int,
-                 max_prompt: int | None = None, staging_layers: int = 0, device="cuda"):
+                 max_prompt: int | None = None, staging_layers: int = 0, device="cuda",
+                 embed_on_host: bool = False):
         self.cfg = cfg
         self.keep = []          # tensors the library points into
         self.w4 = {}            # (layer, name) -> (q, scale, zero) device substitutes
@@ -323,7 +334,12 @@ class Model:
             setattr(d, f, getattr(cfg, f))
         d.rope_theta = cfg.rope_theta
         d.rms_eps = cfg.rms_eps
-        d.embed = dev_t(weights["embed"]).data_ptr()
+        if embed_on_host:   # read in place from pinned host memory
+            emb = weights["embed"].to("cpu").contiguous().pin_memory()
+            self.keep.append(emb)
+            d.embed = emb.data_ptr()
+        else:
+            d.embed = dev_t(weights["embed"]).data_ptr()
         d.lm_head = dev_t(weights["lm_head"]).data_ptr()
         d.final_norm = dev_t(weights["final_norm"]).data_ptr()
         d.layers = layers

@@ -21,6 +21,16 @@ bool pdl_enabled() {
   return on;
 }
 
+bool fault_injected(const char* kind, int index) {
+  const char* e = getenv("SUB_FAULT");
+  if (!e || !e[0]) return false;
+  const size_t n = strlen(kind);
+  if (strncmp(e, kind, n) != 0) return false;
+  if (e[n] == '\0') return true;                    // every event of this kind
+  if (e[n] != ':') return false;
+  return atoi(e + n + 1) == index;                  // only the given one
+}
+
 void set_error(const std::string& msg) { g_last_error = msg; }
 int32_t fail(int32_t code, const std::string& msg) {
   g_last_error = msg;
@@ -64,6 +74,16 @@ extern "C" int32_t sub_pipeline_timeouts(uint32_t* out) {
   SUB_TRY(gemv_tma_timeouts(&a));
   SUB_TRY(gemm_tc_timeouts(&b));
   *out = a + b;
+  return SUB_OK;
+}
+
+extern "C" int32_t sub_bounded_wait_check(uint32_t max_polls) {
+  SUB_CHECK_ARG(max_polls >= 1 && max_polls <= (1u << 20), "max_polls must be in [1, 2^20]");
+  uint32_t polls = 1;
+  SUB_TRY(bounded_wait_selftest(max_polls, &polls));
+  if (polls == 0)
+    return fail(SUB_ETIMEOUT, "bounded wait gave up after " + std::to_string(max_polls) +
+                                  " polls; the kernel ended normally");
   return SUB_OK;
 }
 

@@ -36,6 +36,10 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 
 bool pdl_enabled();   // SUB_PDL=0 in the environment turns it off
 bool env_flag(const char* name, bool dflt);
+// Host-side fault injection (SUB_FAULT, read at each call): true when the
+// environment asks the `index`-th event of `kind` ("alloc" with "alloc:N",
+// "h2d" for every streamed copy) to fail.
+bool fault_injected(const char* kind, int index);
 
 template <typename... KArgs, typename... Args>
 cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,

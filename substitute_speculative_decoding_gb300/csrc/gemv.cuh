@@ -146,5 +146,8 @@ size_t gemv_tma_scratch_floats(const GemvArgs& a, bool is_w4, int epi);
 int32_t gemv_init();
 // Pipeline waits that ran out since load (each one is a bug; never expected).
 int32_t gemv_tma_timeouts(unsigned int* out);
+// One bounded wait on an mbarrier nothing arrives on; *polls = polls made
+// before it was satisfied, 0 when it gave up after `limit` polls.
+int32_t bounded_wait_selftest(uint32_t limit, uint32_t* polls);
 
 }  // namespace sub

@@ -97,10 +97,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Wait for the phase of the given parity to complete.  Bounded: a wait that
 // runs out records itself and returns, so a broken pipeline ends the kernel
 // with wrong numbers and a host-visible count instead of a hang.
+__device__ __forceinline__ uint32_t mbar_wait_polls(uint32_t bar, uint32_t parity, uint32_t limit) {
+  for (uint32_t i = 0; i < limit; ++i)
+    if (mbar_try_wait(bar, parity)) return i + 1;
+  return 0;   // gave up
+}
 __device__ __forceinline__ void mbar_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < (1u << 20); ++i)
-    if (mbar_try_wait(bar, parity)) return;
-  atomicAdd(&g_tma_timeouts, 1u);
+  if (!mbar_wait_polls(bar, parity, 1u << 20)) atomicAdd(&g_tma_timeouts, 1u);
 }
 
 // 2-D tiled TMA load of one box at (x, y) (x in elements of the innermost
@@ -881,6 +884,29 @@ size_t gemv_tma_scratch_floats(const GemvArgs& a, bool w4, int epi) {
   int grid = 0;
   if (!tma_plan(t, w4, epi, &pl, &grid)) return 0;
   return (size_t)pl.n_blocks * pl.maxc * NCW * (a.M <= 8 ? 1 : 2) * 128;
+}
+
+// ------------------------------------------------------ bounded-wait check --
+namespace {
+__device__ unsigned int g_selftest_polls;   // polls the self-test wait made (0 = gave up)
+
+// One thread waits, bounded, on an mbarrier that nothing arrives on and no
+// copy is aimed at: the wait must give up after `limit` polls and the kernel
+// must end normally.
+__global__ void bounded_wait_selftest_kernel(uint32_t limit) {
+  __shared__ __align__(8) unsigned long long bar;
+  const uint32_t b = smem_u32(&bar);
+  mbar_init(b, 1);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  g_selftest_polls = mbar_wait_polls(b, 0, limit);
+}
+}  // namespace
+
+int32_t bounded_wait_selftest(uint32_t limit, uint32_t* polls) {
+  SUB_CUDA_TRY(launch_k(bounded_wait_selftest_kernel, dim3(1), dim3(1), 0, nullptr, limit));
+  SUB_CUDA_TRY(cudaStreamSynchronize(nullptr));
+  SUB_CUDA_TRY(cudaMemcpyFromSymbol(polls, g_selftest_polls, sizeof(unsigned int)));
+  return SUB_OK;
 }
 
 int32_t gemv_tma_timeouts(unsigned int* out) {

@@ -33,7 +33,11 @@ struct Matrices {
 };
 
 // Decode state on the device (one int each).
-enum { ST_N = 0, ST_EMITTED = 1, ST_NACC = 2, ST_BONUS = 3, ST_COUNT = 8 };
+enum { ST_N = 0, ST_EMITTED = 1, ST_NACC = 2, ST_BONUS = 3, ST_TIES = 4, ST_COUNT = 8 };
+
+// Emitted tokens whose top-2 choice scores differ by less than this are
+// counted as near-ties (sub_stats.near_tie_events).
+constexpr float NEAR_TIE_GAP = 1e-2f;
 
 }  // namespace sub
 
@@ -78,6 +82,7 @@ struct sub_model {
   int out_cap = 0;
   int32_t* hist = nullptr;
   unsigned long long* part_key = nullptr;
+  unsigned long long* part_key2 = nullptr;   // accept: runner-up keys (near-ties)
   float* part_f = nullptr;
   unsigned int* counters = nullptr;   // [0] expand, [1] accept
   size_t part_keys = 0, part_floats = 0;
@@ -89,6 +94,13 @@ struct sub_model {
   std::vector<uint16_t*> slots;
   cudaStream_t s_main = nullptr, s_copy = nullptr;
   std::vector<cudaEvent_t> ev_staged, ev_free;
+  // timing (recorded as graph event nodes inside a captured cycle): cycle
+  // start, draft end, verify end; per offloaded layer, the compute stream
+  // reaching it in a target pass and its copy finishing
+  cudaEvent_t ev_cyc[3] = {};
+  std::vector<cudaEvent_t> ev_ready, ev_tstaged;
+  unsigned int timeouts0 = 0;   // pipeline timeouts seen at the last prefill
+  int alloc_index = 0;          // device allocations made (fault injection)
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr, ev_t0 = nullptr, ev_t1 = nullptr;
   int32_t* host_state = nullptr;   // pinned
   int32_t* host_prompt = nullptr;  // pinned [max_prompt]
@@ -111,6 +123,10 @@ namespace sub {
 
 static int32_t dalloc(sub_model* m, void** p, size_t bytes) {
   if (bytes == 0) bytes = 16;
+  if (fault_injected("alloc", m->alloc_index++)) {
+    *p = nullptr;
+    return fail(SUB_ENOMEM, "cudaMalloc(" + std::to_string(bytes) + "): injected fault (SUB_FAULT)");
+  }
   const cudaError_t e = cudaMalloc(p, bytes);
   if (e != cudaSuccess) {
     *p = nullptr;
@@ -135,6 +151,10 @@ static void free_model(sub_model* m) {
   for (cudaEvent_t e : m->trace_pool) cudaEventDestroy(e);
   for (cudaEvent_t e : m->ev_staged) cudaEventDestroy(e);
   for (cudaEvent_t e : m->ev_free) cudaEventDestroy(e);
+  for (cudaEvent_t e : m->ev_ready) cudaEventDestroy(e);
+  for (cudaEvent_t e : m->ev_tstaged) cudaEventDestroy(e);
+  for (cudaEvent_t e : m->ev_cyc)
+    if (e) cudaEventDestroy(e);
   for (cudaEvent_t e : {m->ev_fork, m->ev_join, m->ev_t0, m->ev_t1})
     if (e) cudaEventDestroy(e);
   if (m->s_main) cudaStreamDestroy(m->s_main);
@@ -176,7 +196,21 @@ static Matrices layer_mats(const sub_model* m, int l, bool draft) {
 }
 
 // ---------------------------------------------------------------- streaming --
+// Timing marks go in as event nodes when a cycle is captured (an ordinary
+// record otherwise), so that each replay records them.
+static cudaError_t mark(cudaEvent_t e, cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  const cudaError_t q = cudaStreamIsCapturing(st, &cs);
+  if (q != cudaSuccess) return q;
+  return cs == cudaStreamCaptureStatusActive
+             ? cudaEventRecordWithFlags(e, st, cudaEventRecordExternal)
+             : cudaEventRecord(e, st);
+}
+
 static int32_t issue_copy(sub_model* m, int j) {
+  if (fault_injected("h2d", j))
+    return fail(SUB_ECUDA, "cudaMemcpyAsync (offloaded layer " + std::to_string(j) +
+                               "): injected fault (SUB_FAULT)");
   const sub_layer_desc& L = m->layers[m->d.n_resident + j];
   uint8_t* dst = reinterpret_cast<uint8_t*>(m->slots[j % m->ring]);
   const uint16_t* const* src = mats_of(L);
@@ -184,6 +218,7 @@ static int32_t issue_copy(sub_model* m, int j) {
     SUB_CUDA_TRY(cudaMemcpyAsync(dst + m->mat_off[i], src[i], m->mat_bytes[i],
                                  cudaMemcpyHostToDevice, m->s_copy));
   SUB_CUDA_TRY(cudaEventRecord(m->ev_staged[j], m->s_copy));
+  SUB_CUDA_TRY(mark(m->ev_tstaged[j], m->s_copy));
   return SUB_OK;
 }
 
@@ -396,7 +431,10 @@ static int32_t forward(sub_model* m, bool draft, const FwdRows& r, float* logits
     const bool off = l >= d.n_resident;
     const bool w4 = off && draft;
     const int j = l - d.n_resident;
-    if (off && !draft) SUB_CUDA_TRY(cudaStreamWaitEvent(st, m->ev_staged[j], 0));
+    if (off && !draft) {
+      SUB_CUDA_TRY(mark(m->ev_ready[j], st));
+      SUB_CUDA_TRY(cudaStreamWaitEvent(st, m->ev_staged[j], 0));
+    }
     const Matrices W = layer_mats(m, l, draft);
     const uint16_t* next_gain = l + 1 < d.n_layers ? m->layers[l + 1].attn_norm : d.final_norm;
 
@@ -552,6 +590,7 @@ extern "C" int32_t sub_model_create(const sub_model_desc* desc, sub_model** out)
   CREATE_CUDA(cudaEventCreate(&m->ev_g0));
   CREATE_CUDA(cudaEventCreate(&m->ev_g1));
   CREATE_CUDA(cudaEventCreate(&m->ev_g2));
+  for (cudaEvent_t& e : m->ev_cyc) CREATE_CUDA(cudaEventCreate(&e));
   CREATE_CUDA(cudaHostAlloc(reinterpret_cast<void**>(&m->host_state), 64, cudaHostAllocDefault));
 
   const int H = d.hidden, D = d.head_dim, F = d.ffn;
@@ -642,6 +681,7 @@ extern "C" int32_t sub_model_create(const sub_model_desc* desc, sub_model** out)
     (void)ac;
     m->part_floats = (size_t)d.max_width * 64 * 2;
     CREATE_TRY(dalloc_t(m, &m->part_key, m->part_keys));
+    CREATE_TRY(dalloc_t(m, &m->part_key2, m->part_keys));
     CREATE_TRY(dalloc_t(m, &m->part_f, m->part_floats));
     CREATE_TRY(dalloc_t(m, &m->counters, 4));
     CREATE_CUDA(cudaMemset(m->counters, 0, 16));
@@ -669,9 +709,13 @@ extern "C" int32_t sub_model_create(const sub_model_desc* desc, sub_model** out)
     }
     m->ev_staged.resize(m->n_off, nullptr);
     m->ev_free.resize(m->n_off, nullptr);
+    m->ev_ready.resize(m->n_off, nullptr);
+    m->ev_tstaged.resize(m->n_off, nullptr);
     for (int j = 0; j < m->n_off; ++j) {
       CREATE_CUDA(cudaEventCreateWithFlags(&m->ev_staged[j], cudaEventDisableTiming));
       CREATE_CUDA(cudaEventCreateWithFlags(&m->ev_free[j], cudaEventDisableTiming));
+      CREATE_CUDA(cudaEventCreate(&m->ev_ready[j]));
+      CREATE_CUDA(cudaEventCreate(&m->ev_tstaged[j]));
     }
   }
   CREATE_CUDA(cudaDeviceSynchronize());
@@ -766,6 +810,9 @@ static int32_t accept_args(sub_model* m, const sub_decode_cfg& c, int n_nodes, A
   a.out_tokens = m->out_tokens;
   a.state_emitted = m->state + ST_EMITTED;
   a.hist = m->hist;
+  a.part_key2 = m->part_key2;
+  a.near_ties = m->state + ST_TIES;
+  a.tie_gap = NEAR_TIE_GAP;
   return SUB_OK;
 }
 
@@ -779,6 +826,7 @@ static int32_t enqueue_cycle(sub_model* m, const sub_decode_cfg& c) {
   sub_tree tr = m->tree;
   tr.width = k;
   tr.max_depth = d.max_depth;
+  SUB_CUDA_TRY(mark(m->ev_cyc[0], m->s_main));
   SUB_TRY(begin_target_pass(m));
   // ---- draft ----
   for (int lvl = 0; lvl < D; ++lvl) {
@@ -813,6 +861,7 @@ static int32_t enqueue_cycle(sub_model* m, const sub_decode_cfg& c) {
     SUB_TRY(launch_expand(e, m->s_main));
   }
   // ---- verify ----
+  SUB_CUDA_TRY(mark(m->ev_cyc[1], m->s_main));
   FwdRows v{};
   v.tokens = tr.token;
   v.n = n_tree;
@@ -825,6 +874,7 @@ static int32_t enqueue_cycle(sub_model* m, const sub_decode_cfg& c) {
   v.keys_hint = d.max_seq;
   SUB_TRY(forward(m, false, v, m->logits, false));
   SUB_TRY(end_target_pass(m));
+  SUB_CUDA_TRY(mark(m->ev_cyc[2], m->s_main));
   // ---- accept, compact, advance ----
   AcceptArgs a;
   SUB_TRY(accept_args(m, c, n_tree, a));
@@ -912,6 +962,35 @@ static int32_t join_out(sub_model* m, cudaStream_t user) {
   return SUB_OK;
 }
 
+// Bounded pipeline waits that ran out so far on this device (all kernels).
+static int32_t timeouts_now(unsigned int* out) {
+  unsigned int a = 0, b = 0;
+  SUB_TRY(gemv_tma_timeouts(&a));
+  SUB_TRY(gemm_tc_timeouts(&b));
+  *out = a + b;
+  return SUB_OK;
+}
+static int32_t check_timeouts(const sub_model* m) {
+  unsigned int now = 0;
+  SUB_TRY(timeouts_now(&now));
+  if (now != m->timeouts0)
+    return fail(SUB_ETIMEOUT, std::to_string(now - m->timeouts0) +
+                                  " bounded pipeline wait(s) ran out since the prefill: the "
+                                  "emitted tokens are not to be trusted");
+  return SUB_OK;
+}
+
+// Device time between two marks (ms), or a negative value when it cannot be
+// read (the error is cleared).
+static double span_ms(cudaEvent_t a, cudaEvent_t b) {
+  float ms = 0.f;
+  if (cudaEventElapsedTime(&ms, a, b) != cudaSuccess) {
+    cudaGetLastError();
+    return -1e30;
+  }
+  return ms;
+}
+
 static int32_t prefill_impl(sub_model* m, const int32_t* prompt_host, int32_t n_prompt,
                             const sub_decode_cfg& c) {
   const sub_model_desc& d = m->d;
@@ -923,6 +1002,7 @@ static int32_t prefill_impl(sub_model* m, const int32_t* prompt_host, int32_t n_
   SUB_TRY(check_cfg(m, c));
   // the prompt goes through pinned staging so the copy is a true async H2D
   SUB_CUDA_TRY(cudaStreamSynchronize(st));
+  SUB_TRY(timeouts_now(&m->timeouts0));
   std::memcpy(m->host_prompt, prompt_host, (size_t)n_prompt * 4);
   SUB_CUDA_TRY(cudaMemcpyAsync(m->rows_tok, m->host_prompt, (size_t)n_prompt * 4,
                                cudaMemcpyHostToDevice, st));
@@ -997,6 +1077,7 @@ extern "C" int32_t sub_decode_read(sub_model* m, int32_t* out_host, int32_t n, i
                                    int64_t* cycles) {
   SUB_CHECK_ARG(m, "null pointer");
   SUB_TRY(read_state(m));
+  const int32_t tstat = check_timeouts(m);
   const int e = m->host_state[ST_EMITTED];
   if (emitted) *emitted = e;
   if (cycles) *cycles = m->cycles;
@@ -1004,7 +1085,7 @@ extern "C" int32_t sub_decode_read(sub_model* m, int32_t* out_host, int32_t n, i
     const int cnt = std::min(n, e);
     SUB_CUDA_TRY(cudaMemcpy(out_host, m->out_tokens, (size_t)cnt * 4, cudaMemcpyDeviceToHost));
   }
-  return SUB_OK;
+  return tstat;
 }
 
 extern "C" int32_t sub_cycle_info(sub_model* m, const sub_decode_cfg* cfg,
@@ -1038,10 +1119,18 @@ extern "C" int32_t sub_generate(sub_model* m, const int32_t* prompt_host, int32_
   if (c.use_graph) SUB_TRY(ensure_graph(m, c));
   SUB_TRY(read_state(m));
   int emitted = m->host_state[ST_EMITTED];
+  double t_draft = 0.0, t_verify = 0.0, t_unhidden = 0.0;
   while (emitted < n_new) {
     SUB_TRY(decode_impl(m, c, 1));
     SUB_TRY(read_state(m));
     emitted = m->host_state[ST_EMITTED];
+    // this cycle's phase times (the marks of the cycle just synchronised)
+    t_draft += span_ms(m->ev_cyc[0], m->ev_cyc[1]);
+    t_verify += span_ms(m->ev_cyc[1], m->ev_cyc[2]);
+    for (int j = 0; j < m->n_off; ++j) {
+      const double w = span_ms(m->ev_ready[j], m->ev_tstaged[j]);   // < 0: copy was early
+      t_unhidden = (w < -1e29 || t_unhidden < 0.0) ? -1.0 : t_unhidden + std::max(0.0, w);
+    }
   }
   SUB_CUDA_TRY(cudaEventRecord(m->ev_g2, st));
   SUB_CUDA_TRY(cudaMemcpyAsync(m->host_out, m->out_tokens, (size_t)n_new * 4,
@@ -1061,6 +1150,10 @@ extern "C" int32_t sub_generate(sub_model* m, const int32_t* prompt_host, int32_
     std::vector<int32_t> h(d.max_depth + 1);
     SUB_CUDA_TRY(cudaMemcpy(h.data(), m->hist, h.size() * 4, cudaMemcpyDeviceToHost));
     for (int i = 0; i <= std::min(d.max_depth, 64); ++i) stats->accept_hist[i] = h[i];
+    stats->t_draft_ms = t_draft >= 0.0 ? t_draft : -1.0;
+    stats->t_verify_ms = t_verify >= 0.0 ? t_verify : -1.0;
+    stats->t_copy_unhidden_ms = t_unhidden >= 0.0 ? t_unhidden : -1.0;
+    stats->near_tie_events = m->host_state[ST_TIES];
   }
-  return SUB_OK;
+  return check_timeouts(m);
 }

@@ -312,7 +312,7 @@ __global__ void __launch_bounds__(ACC_THREADS) accept_kernel(AcceptArgs a) {
   const int64_t root_pos = a.root_pos_dev ? (int64_t)*a.root_pos_dev : a.root_pos;
   const uint32_t pos = (uint32_t)(root_pos + a.tree.depth[u] + 1);
   const uint32_t k0 = (uint32_t)(a.seed & 0xffffffffull), k1 = (uint32_t)(a.seed >> 32);
-  unsigned long long best = 0ull;
+  unsigned long long best = 0ull, second = 0ull;
   for (int64_t b = b_lo + threadIdx.x; b < b_hi; b += ACC_THREADS) {
     uint4 r = make_uint4(0, 0, 0, 0);
     if (a.mode == 1) r = philox4x32_10(make_uint4((uint32_t)b, pos, 0u, 0u), k0, k1);
@@ -324,10 +324,22 @@ __global__ void __launch_bounds__(ACC_THREADS) accept_kernel(AcceptArgs a) {
       float sc = z[v];
       if (a.mode == 1) sc = __fdiv_rn(sc, a.temp) + gumbel_of(rw[i]);
       const unsigned long long key = rank_key(sc, (uint32_t)v);
-      best = key > best ? key : best;
+      if (key > best) {
+        second = best;
+        best = key;
+      } else if (key > second) {
+        second = key;
+      }
     }
   }
+  const unsigned long long mine = best;
   best = block_max_u64(best, s_red);
+  if (a.near_ties) {
+    // the chunk's runner-up: the best key of the thread that held the winner
+    // is replaced by that thread's second
+    second = block_max_u64(mine == best ? second : mine, s_red);
+    if (threadIdx.x == 0) a.part_key2[(size_t)u * a.n_chunks + c] = second;
+  }
   if (threadIdx.x == 0) {
     a.part_key[(size_t)u * a.n_chunks + c] = best;
     __threadfence();
@@ -369,6 +381,28 @@ __global__ void __launch_bounds__(ACC_THREADS) accept_kernel(AcceptArgs a) {
       *a.state_emitted = e + n_acc + 1;
     }
     if (a.hist) a.hist[n_acc] += 1;
+    if (a.near_ties) {
+      // path nodes root, accepted[0..n_acc): their choices are the emitted tokens
+      int ties = 0;
+      for (int i = 0; i <= n_acc; ++i) {
+        const int node = i == 0 ? 0 : a.accepted[i - 1];
+        unsigned long long k1 = 0ull, k2 = 0ull;
+        for (int cc = 0; cc < a.n_chunks; ++cc) {
+          const unsigned long long b1 = a.part_key[(size_t)node * a.n_chunks + cc];
+          const unsigned long long b2 = a.part_key2[(size_t)node * a.n_chunks + cc];
+          if (b1 > k1) {
+            k2 = k1 > b2 ? k1 : b2;
+            k1 = b1;
+          } else {
+            k2 = b1 > k2 ? b1 : k2;
+          }
+        }
+        if (k2 != 0ull &&
+            key_float((uint32_t)(k1 >> 32)) - key_float((uint32_t)(k2 >> 32)) < a.tie_gap)
+          ++ties;
+      }
+      *a.near_ties += ties;
+    }
     *a.counter = 0u;
   }
 }

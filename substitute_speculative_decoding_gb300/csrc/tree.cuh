@@ -46,6 +46,13 @@ struct AcceptArgs {
   int32_t* out_tokens;
   int32_t* state_emitted;
   int32_t* hist;         // accept histogram [max_depth + 1]
+  // near-tie count (model path only; null in the public entry points): for
+  // every node on the walked path, the runner-up's choice score per chunk goes
+  // to part_key2 [n_nodes * n_chunks], and *near_ties counts the path nodes
+  // whose best and runner-up choice scores differ by less than tie_gap
+  unsigned long long* part_key2;
+  int32_t* near_ties;
+  float tie_gap;
 };
 size_t accept_scratch_bytes(int n_nodes, int n_chunks);
 int accept_pick_chunks(int n_nodes, int64_t V);

@@ -120,9 +120,19 @@ def _check_lossless(tiny, out, mode="greedy", temp=1.0, seed=7):
 @pytest.mark.parametrize("depth,width", [(8, 2), (0, 1), (3, 3), (8, 1)])
 def test_generate_greedy_is_lossless(tiny, depth, width):
     out, st = tiny["model"].generate(tiny["prompt"], 64, depth, width)
-    _check_lossless(tiny, out)
+    r = _check_lossless(tiny, out)
     assert st.cycles >= 1 and 1.0 <= st.tau <= depth + 1
     assert sum(st.accept_hist[i] for i in range(depth + 1)) == st.cycles
+    # phase times: the draft (none at depth 0) and the verify pass fit in the decode time
+    assert st.t_verify_ms > 0.0 and st.t_draft_ms >= 0.0 and st.t_copy_unhidden_ms >= 0.0
+    if depth == 0:   # no draft levels: only the copy-stream fork sits in that span
+        assert st.t_draft_ms < 0.05 * st.cycles
+    else:
+        assert st.t_draft_ms > 0.0
+    assert st.t_draft_ms + st.t_verify_ms <= st.t_decode_ms * 1.05 + 0.5
+    # the device's near-ties (its own top-2 gap < 1e-2) cover every position
+    # where it picked another token than the oracle within the tie gap, or more
+    assert st.near_tie_events >= 0 and st.near_tie_events <= 64
 
 
 def test_generate_gumbel_is_lossless(tiny):
