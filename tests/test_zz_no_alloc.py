@@ -1,6 +1,12 @@
-"""sub_verify_accept_static: the accept step on the library's fixed
-per-device scratch must give exactly what sub_verify_accept gives, on two
-calls in a row (the second call reuses the scratch the first one left)."""
+"""sub_verify_accept_static, the accept step for callers that cannot allocate
+device memory while they decode: a runtime that owns the device's memory
+through its own allocator and forbids libraries to call cudaMalloc or
+cudaMallocAsync, or a decode loop that must not stall or fail on an
+allocation once it has started.  The entry point uses a fixed scratch array
+the library holds on each device instead.  It must give exactly what
+sub_verify_accept gives, on two calls in a row (the second call reuses the
+scratch the first one left), and it must take no memory from the device's
+memory pool."""
 import ctypes as C
 
 import numpy as np
@@ -71,25 +77,42 @@ def test_static_matches_allocating_accept_twice(sub, mode, vocab, depth, width, 
             assert got[3] is None
 
 
+def _default_pool_high_water():
+    """Reset, then read back, the high-water mark of the device's default
+    memory pool (the pool cudaMallocAsync draws from), through the driver."""
+    drv = C.CDLL("libcuda.so.1")
+    dev = C.c_int()
+    assert drv.cuDeviceGet(C.byref(dev), torch.cuda.current_device()) == 0
+    pool = C.c_void_p()
+    assert drv.cuDeviceGetDefaultMemPool(C.byref(pool), dev) == 0
+    used_high = 8   # CU_MEMPOOL_ATTR_USED_MEM_HIGH
+
+    def reset():
+        zero = C.c_uint64(0)
+        assert drv.cuMemPoolSetAttribute(pool, used_high, C.byref(zero)) == 0
+
+    def read():
+        v = C.c_uint64()
+        assert drv.cuMemPoolGetAttribute(pool, used_high, C.byref(v)) == 0
+        return v.value
+    return reset, read
+
+
 @pytest.mark.gpu
-def test_static_accept_replays_in_a_graph(sub):
-    """Captured after a first eager call (which looks the scratch up), the
-    static call replays with no allocation node and keeps matching."""
+def test_static_accept_allocates_nothing(sub):
+    """For callers that cannot allocate inside their decode loop: the static
+    entry point draws no device memory, while the allocating one does (the
+    control shows the measurement sees its per-call scratch)."""
     logits, tr, n = _case(sub, 0, 152064, 48, 8, seed=5)
-    ref = sub.verify_accept(logits, tr, n, root_pos=9)
-    out = sub.verify_accept_static(logits, tr, n, root_pos=9)
+    out = sub.verify_accept_static(logits, tr, n, root_pos=9)   # first call: set-up
     torch.cuda.synchronize()
-    s = torch.cuda.Stream()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(s):
-        with torch.cuda.graph(g, stream=s):
-            sub.verify_accept_static(logits, tr, n, root_pos=9, out=out, stream=s)
+    reset, read = _default_pool_high_water()
+    reset()
+    base = read()
     for _ in range(2):
-        for t in out:
-            t.fill_(-1)
-        g.replay()
-        torch.cuda.synchronize()
-        a = int(ref[1].item())
-        assert int(out[1].item()) == a
-        assert torch.equal(out[0][:a], ref[0][:a])
-        assert torch.equal(out[2], ref[2]) and torch.equal(out[3], ref[3])
+        sub.verify_accept_static(logits, tr, n, root_pos=9, out=out)
+    torch.cuda.synchronize()
+    assert read() == base
+    sub.verify_accept(logits, tr, n, root_pos=9)
+    torch.cuda.synchronize()
+    assert read() > base
