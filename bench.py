@@ -1,24 +1,37 @@
 #!/usr/bin/env python
 """SubSpec decode benchmark on GB300.
 
-One step = one SubSpec decode cycle over the Qwen2.5-7B-shaped decoder:
-48 draft levels (shared resident bf16 layers + int4 substitutes, width 8,
-draft temperature 0.2) -> one target pass verifying all 385 tree nodes (the
-offloaded layers' bf16 originals streamed from pinned host memory on a copy
-stream under the draft) -> greedy accept -> KV compaction.  `value` is the
-generated tokens/s of K device-timed cycles with every input resident;
-`e2e` is sub_generate (host prompt in, host tokens out, prefill included).
+One step = one SubSpec decode cycle: D = 48 draft levels (shared resident bf16
+layers + int4 substitutes, width 8, draft temperature 0.2) -> one target pass
+verifying all 385 tree nodes (the offloaded layers' bf16 originals streamed
+from pinned host memory on a copy stream) -> accept -> KV compaction.
+`value` is the generated tokens/s of K device-timed cycles with every input
+resident; `e2e` is sub_generate (host prompt in, host tokens out, prefill
+included).
+
+Workloads (--workload):
+  qwen7b   Qwen2.5-7B-shaped decoder, 11 resident + 17 int4 layers, prompt 512,
+           greedy (the default; 256 tokens for e2e)
+  llama8b  Llama-3.1-8B-shaped decoder (RoPE theta 5e5, eps 1e-5), 8 resident +
+           24 int4 layers, prompt 1024, greedy (512 tokens for e2e)
+  qwen32b  Qwen2.5-32B-shaped decoder under a 24 GB device budget: 1 resident
+           layer, 63 int4 substitutes, a 2-slot staging ring for the streamed
+           originals, the embedding in pinned host memory; prompt 256,
+           Gumbel-max sampling at T = 0.6 with seed 7 (e2e: --new tokens, 256
+           by default; the workload's full length is 4096)
 
 Flags: --gpus N (replicas; one process per GPU under torchrun), --steps K,
 --warmup W, --impl reference (the CPU oracle arm), --quick (skip the kernel
-sweep, e2e and the CPU baseline: for profiler launch lists).
+sweep, e2e and the CPU baseline: for profiler launch lists), --new N.
 """
 from __future__ import annotations
 
 import argparse
 import hashlib
 import json
+import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -33,9 +46,29 @@ import torch  # noqa: E402
 import synthetic  # noqa: E402
 
 METRIC = "generated tokens/s and τ (1 GB300); W4 GEMM + tree-attn GB/s vs 8 TB/s"
-CONFIG = "qwen7b"
 DEPTH, WIDTH, DRAFT_T = 48, 8, 0.2
-E2E_NEW = 256
+L2_BYTES = 129 * 2 ** 20
+ROTATE_BYTES = 4 * L2_BYTES      # operand sets rotated per timed sweep point
+
+WORKLOADS = {
+    "qwen7b": dict(cfg="qwen7b", staging=0, embed_on_host=False, e2e_new=256,
+                   text="Qwen2.5-7B-shaped decoder (28 layers, hidden 3584, 28/4 heads, FFN "
+                        "18944, vocab 152064), random bf16 init; 11 resident layers + 17 int4 "
+                        "g64 substitutes with pinned-host bf16 originals streamed per verify; "
+                        "prompt 512; SubSpec tree depth 48, width 8, draft T 0.2, greedy; "
+                        "step = one draft/verify/accept cycle"),
+    "llama8b": dict(cfg="llama8b", staging=0, embed_on_host=False, e2e_new=512,
+                    text="Llama-3.1-8B-shaped decoder (32 layers, hidden 4096, 32/8 heads, FFN "
+                         "14336, vocab 128256, RoPE theta 5e5), random bf16 init; 8 resident + "
+                         "24 int4 g64 substitutes with pinned-host originals; prompt 1024; "
+                         "depth 48, width 8, greedy; step = one cycle"),
+    "qwen32b": dict(cfg="qwen32b", staging=2, embed_on_host=True, e2e_new=256,
+                    text="Qwen2.5-32B-shaped decoder (64 layers, hidden 5120, 40/8 heads, FFN "
+                         "27648, vocab 152064), random bf16 init, 24 GB device budget: 1 resident "
+                         "layer + 63 int4 g64 substitutes, 2-slot staging ring for the pinned-host "
+                         "originals, host-resident embedding; prompt 256; depth 48, width 8, "
+                         "Gumbel-max T 0.6 seed 7; step = one cycle"),
+}
 
 
 # ------------------------------------------------------------------ setup --
@@ -132,19 +165,34 @@ def gpu_index(local):
     return local
 
 
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.processor() or platform.machine()
+
+
 # ------------------------------------------------------------ workload --
 def layer_bytes_bf16(cfg):
     return cfg.params_per_layer() * 2
 
 
 def layer_bytes_w4(cfg):
-    h, f = cfg.hidden, cfg.ffn
-    rows_k = [(cfg.q_dim, h), (cfg.kv_dim, h), (cfg.kv_dim, h), (h, cfg.q_dim), (f, h), (f, h),
-              (h, f)]
-    return sum(n * ((k + 63) // 64) * (32 + 4) for n, k in rows_k)
+    return sum(n * ((k + 63) // 64) * (32 + 4) for n, k in synthetic.layer_shapes(cfg).values())
 
 
-def cycle_bound(cfg, pk, tau, n_ctx, link_gbs):
+def cycle_bound(cfg, pk, tau, n_ctx, link_gbs, ring):
     """Roofline-derived lower bound on one cycle (ms) and the tokens/s it allows."""
     lm = cfg.vocab * cfg.hidden * 2
     kv = cfg.n_layers * n_ctx * cfg.kv_dim * 2 * 2
@@ -154,9 +202,14 @@ def cycle_bound(cfg, pk, tau, n_ctx, link_gbs):
     n_tree = 1 + DEPTH * WIDTH
     flops = 2 * n_tree * (cfg.n_layers * cfg.params_per_layer() + lm // 2)
     t_verify = flops / (pk["bf16_sus"] * 1e12) * 1e3
-    h2d = (cfg.n_layers - cfg.n_resident) * layer_bytes_bf16(cfg)
-    t_link = h2d / (link_gbs * 1e9) * 1e3 if link_gbs else 0.0
-    t = t_draft + t_verify + max(0.0, t_link - t_draft)
+    n_off = cfg.n_layers - cfg.n_resident
+    t_layer = layer_bytes_bf16(cfg) / (link_gbs * 1e9) * 1e3 if link_gbs else 0.0
+    t_link = n_off * t_layer
+    # a ring of every offloaded layer streams them all under the draft; a ring
+    # of r slots stages r layers there and the other n_off - r during the verify
+    r = n_off if ring <= 0 else min(ring, n_off)
+    link_after_draft = max(0.0, r * t_layer - t_draft) + (n_off - r) * t_layer
+    t = t_draft + max(t_verify, link_after_draft)
     return dict(cycle_ms=t, draft_ms=t_draft, verify_ms=t_verify, link_ms=t_link,
                 level_bytes=level_bytes, tokens_per_s=tau / t * 1e3 if t else None)
 
@@ -204,9 +257,14 @@ def time_launches(fn, iters, stream):
     return e0.elapsed_time(e1) / (3 * iters)
 
 
+def copies_for(nbytes):
+    """Operand sets to rotate so that one sweep point streams >= 4x L2."""
+    return max(2, math.ceil(ROTATE_BYTES / max(nbytes, 1)))
+
+
 def kernel_measurements(sub, cfg, weights, model, pk, dev, quick):
     """Dominant-kernel roofline and the kernel sweep (CUDA events on the
-    launching stream; every operand set is larger than L2 or rotated)."""
+    launching stream; every timed point rotates operands over >= 4x L2)."""
     st = torch.cuda.current_stream()
     out = {}
     # --- dominant kernel: int4 GEMV of the substitutes at draft width M=8
@@ -222,7 +280,9 @@ def kernel_measurements(sub, cfg, weights, model, pk, dev, quick):
              for q, s_, z, n, k in subs) / len(subs)
     out["w4_gemv_m8"] = dict(ms_per_launch=ms4, bytes_per_launch=b4,
                              gbs=b4 / (ms4 / 1e3) / 1e9,
-                             what="int4 substitutes (q/k/v, o, gate, up, down) in turn, M=8")
+                             rotated_bytes=sum(q.numel() for q, *_ in subs),
+                             what="int4 substitutes (o, gate, up, down of every offloaded "
+                                  "layer) in turn, M=8")
     # --- bf16 GEMV of the resident layers at M=8
     mats = []
     for i in range(cfg.n_resident):
@@ -251,26 +311,27 @@ def kernel_measurements(sub, cfg, weights, model, pk, dev, quick):
     del xv, yv
     if quick:
         return out
-    # --- int4 sweep on Qwen2.5-32B layer shapes
+    # --- int4 sweep on Qwen2.5-32B layer shapes, operands rotated over >= 4x L2
     shapes = {"qkv": (7168, 5120), "o": (5120, 5120), "gate_up": (55296, 5120),
               "down": (5120, 27648)}
     sweep = {}
-    packs = {k: [synthetic.random_w4(n, kk, seed, device=dev) for seed in (1, 2)]
-             for k, (n, kk) in shapes.items()}
-    for mrows in (1, 8, 48, 128, 384):
-        row = {}
-        for name, (n, k) in shapes.items():
+    for name, (n, k) in shapes.items():
+        wbytes = n * ((k + 63) // 64) * 36
+        nc = copies_for(wbytes)
+        packs = [synthetic.random_w4(n, k, seed, device=dev) for seed in range(nc)]
+        for mrows in (1, 8, 48, 128, 384):
             xx = torch.randn(mrows, k, device=dev).to(torch.bfloat16)
             yy = torch.empty(mrows, n, device=dev, dtype=torch.bfloat16)
-            pp = packs[name]
-            sub.w4_gemm(xx, *pp[0], n, k, out=yy)
-            msx = time_launches(lambda i: sub.w4_gemm(xx, *pp[i % 2], n, k, out=yy), 20, st)
-            byt = n * ((k + 63) // 64) * 36 + 2 * mrows * (n + k)
-            row[name] = dict(ms=round(msx, 5), gbs=round(byt / (msx / 1e3) / 1e9, 1),
-                             tflops=round(2 * mrows * n * k / (msx / 1e3) / 1e12, 2))
-        sweep[f"M{mrows}"] = row
+            msx = time_launches(lambda i: sub.w4_gemm(xx, *packs[i % nc], n, k, out=yy),
+                                max(20, nc), st)
+            byt = wbytes + 2 * mrows * (n + k)
+            sweep.setdefault(f"M{mrows}", {})[name] = dict(
+                ms=round(msx, 5), gbs=round(byt / (msx / 1e3) / 1e9, 1),
+                frac_hbm=round(byt / (msx / 1e3) / 1e9 / pk["hbm"], 3),
+                tflops=round(2 * mrows * n * k / (msx / 1e3) / 1e12, 2), copies=nc)
+        del packs
     out["w4_sweep_qwen32b"] = sweep
-    # --- tree attention, Qwen2.5-32B heads (40 q / 8 kv, d 128)
+    # --- tree attention, Qwen2.5-32B heads (40 q / 8 kv, d 128); KV rotated over >= 4x L2
     attn = {}
     hq, hkv, d = 40, 8, 128
     tok, par, dep = synthetic.random_tree(DEPTH, WIDTH, 3, 1000)
@@ -279,87 +340,113 @@ def kernel_measurements(sub, cfg, weights, model, pk, dev, quick):
     n_tree = len(par)
     for lkv in (1024, 4096, 16384):
         cap = lkv + n_tree + 64
-        kv, keep = sub.make_kv(1, hkv, d, cap, page_size=64)
-        keep[0].normal_()
-        keep[1].normal_()
+        kv_bytes = (lkv + n_tree) * hkv * d * 2 * 2
+        nc = copies_for(kv_bytes)
+        caches = []
+        for _ in range(nc):
+            kv, keep = sub.make_kv(1, hkv, d, cap, page_size=64)
+            keep[0].normal_()
+            keep[1].normal_()
+            caches.append((kv, keep))
         for nq, tag in ((n_tree, "verify385"), (WIDTH, "draft8")):
             q = torch.randn(nq, hq, d, device=dev).to(torch.bfloat16)
             a_ = anc[-nq:].contiguous()
             dd = depd[-nq:].contiguous()
-            sub.tree_attn(q, kv, 0, lkv, lkv, n_tree, anc=a_, depth=dd)
-            msa = time_launches(lambda i: sub.tree_attn(q, kv, 0, lkv, lkv, n_tree, anc=a_,
-                                                        depth=dd), 20, st)
-            byt = (lkv + n_tree) * hkv * d * 2 * 2 + 2 * nq * hq * d * 2
+            msa = time_launches(lambda i: sub.tree_attn(q, caches[i % nc][0], 0, lkv, lkv, n_tree,
+                                                        anc=a_, depth=dd), max(20, nc), st)
+            byt = kv_bytes + 2 * nq * hq * d * 2
             fl = 4 * nq * hq * (lkv + DEPTH) * d
             attn[f"{tag}_kv{lkv}"] = dict(ms=round(msa, 5), gbs=round(byt / (msa / 1e3) / 1e9, 1),
-                                          tflops=round(fl / (msa / 1e3) / 1e12, 2))
-        del kv, keep
+                                          frac_hbm=round(byt / (msa / 1e3) / 1e9 / pk["hbm"], 3),
+                                          tflops=round(fl / (msa / 1e3) / 1e12, 2), copies=nc)
+        del caches
     out["tree_attn_qwen32b_heads"] = attn
     return out
 
 
 # ------------------------------------------------------------ CPU oracle --
-class LazyLayers:
-    """Oracle-format (float32 NumPy) layer weights, converted on access."""
-
-    def __init__(self, layers, idx):
-        self.layers, self.idx = layers, idx
-
-    def __len__(self):
-        return len(self.idx)
-
-    def __iter__(self):
-        for i in self.idx:
-            yield {k: v.float().cpu().numpy() for k, v in self.layers[i].items()}
+def oracle_weights(weights, layers):
+    """Oracle-format (float32 NumPy, exact bf16 values) globals and layers."""
+    glob = {k: weights[k].float().cpu().numpy() for k in ("embed", "lm_head", "final_norm")}
+    lay = [{k: v.float().cpu().numpy() for k, v in weights["layers"][i].items()} for i in layers]
+    return glob, lay
 
 
-def oracle_token_sample(cfg, weights, n_layers_sample, n_ctx=None):
-    """Time the oracle's plain target decoding of one token at the prompt's
-    context length (random bf16 KV stands in for the prefix) over a subset of
-    layers; returns (seconds for those layers, seconds for the lm_head)."""
+def oracle_token(cfg, glob, layers, n_ctx, seed=0):
+    """Seconds for the oracle's plain target decoding of one token at context
+    n_ctx over the given layers (a random bf16 KV prefix stands in for the
+    prompt's cache), lm_head included."""
     import numpy as np
     from oracle.bf16 import round_bf16
     from oracle.model import forward_rows
-    n_ctx = cfg.prompt_len if n_ctx is None else n_ctx
-    rng = np.random.default_rng(0)
+    rng = np.random.default_rng(seed)
     ks = [round_bf16(rng.standard_normal((n_ctx, cfg.n_heads_kv, cfg.head_dim)).astype(np.float32))
-          for _ in range(n_layers_sample)]
-    glob = {"embed": weights["embed"].float().cpu().numpy(),
-            "lm_head": weights["lm_head"].float().cpu().numpy(),
-            "final_norm": weights["final_norm"].float().cpu().numpy()}
-    layers = LazyLayers(weights["layers"], list(range(n_layers_sample)))
+          for _ in layers]
     t0 = time.perf_counter()
     forward_rows(cfg, glob, layers, [7], [n_ctx], ks, ks, np.ones((1, n_ctx), bool),
                  np.ones((1, 1), bool))
-    t1 = time.perf_counter()
-    # the lm_head share: one more call with no layers at all
-    forward_rows(cfg, glob, LazyLayers(weights["layers"], []), [7], [n_ctx], [], [],
-                 np.ones((1, 0), bool), np.ones((1, 1), bool))
-    t2 = time.perf_counter()
-    return t1 - t0 - (t2 - t1), t2 - t1
+    return time.perf_counter() - t0
 
 
-def cpu_cores():
+_ONE_THREAD = r"""
+import os, sys, time, json
+sys.path.insert(0, {root!r})
+import numpy as np
+import torch
+import synthetic
+from oracle.bf16 import round_bf16
+from oracle.model import forward_rows
+cfg = synthetic.CONFIGS[{cfg!r}]
+g = synthetic.make_globals(cfg)
+glob = {{k: v.float().numpy() for k, v in g.items()}}
+lay = [{{k: v.float().numpy() for k, v in synthetic.make_layer(cfg, i).items()}}
+       for i in range({nl})]
+rng = np.random.default_rng(0)
+ks = [round_bf16(rng.standard_normal(({ctx}, cfg.n_heads_kv, cfg.head_dim)).astype(np.float32))
+      for _ in lay]
+vis = np.ones((1, {ctx}), bool)
+t0 = time.perf_counter()
+forward_rows(cfg, glob, lay, [7], [{ctx}], ks, ks, vis, np.ones((1, 1), bool))
+t1 = time.perf_counter()
+forward_rows(cfg, glob, [], [7], [{ctx}], [], [], np.ones((1, 0), bool), np.ones((1, 1), bool))
+t2 = time.perf_counter()
+print(json.dumps(dict(layers_s=t1 - t0, head_s=t2 - t1)))
+"""
+
+
+def oracle_one_thread(cfg, n_layers_sample=2):
+    """The oracle on one host thread (BLAS pinned to one thread in a child
+    process): seconds for n_layers_sample layers and for the head alone."""
+    env = {**os.environ, "OPENBLAS_NUM_THREADS": "1", "OMP_NUM_THREADS": "1",
+           "MKL_NUM_THREADS": "1", "CUDA_VISIBLE_DEVICES": ""}
+    code = _ONE_THREAD.format(root=ROOT, cfg=cfg.name, nl=n_layers_sample, ctx=cfg.prompt_len)
     try:
-        return len(os.sched_getaffinity(0))
-    except AttributeError:
-        return os.cpu_count()
+        r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                           timeout=600)
+        return json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception as e:   # reported, not fatal: the baseline is context only
+        return {"error": f"{type(e).__name__}: {e}"}
 
 
 def run_reference(args, world, rank):
-    """The reference arm: the CPU oracle, as it stands, on the host cores."""
+    """The reference arm: the CPU oracle, as it stands, on the host cores.
+    One step = the oracle's plain target decoding of one token through every
+    layer and the head at the workload's prompt length."""
     if rank != 0:
         return
-    cfg = synthetic.CONFIGS[CONFIG]
+    wl = WORKLOADS[args.workload]
+    cfg = synthetic.CONFIGS[wl["cfg"]]
     dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t0 = time.perf_counter()
     weights = synthetic.make_model(cfg, device=dev)
-    n_sample = 2
+    glob, layers = oracle_weights(weights, range(cfg.n_layers))
+    del weights
+    setup = time.perf_counter() - t0
     times = []
     for i in range(args.warmup + args.steps):
-        tl, th = oracle_token_sample(cfg, weights, n_sample)
-        t_tok = tl * cfg.n_layers / n_sample + th
+        t = oracle_token(cfg, glob, layers, cfg.prompt_len, seed=i)
         if i >= args.warmup:
-            times.append(t_tok)
+            times.append(t)
     t = statistics.mean(times)
     value = 1.0 / t
     line = {
@@ -367,50 +454,29 @@ def run_reference(args, world, rank):
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": workload_name(), "prompt": cfg.prompt_len},
+        "config": {"workload": wl["text"], "prompt": cfg.prompt_len, "depth": DEPTH,
+                   "width": WIDTH},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(),
-                         "kind": "oracle",
-                         "sample": f"per step: oracle plain target decoding of one token at "
-                                   f"context {cfg.prompt_len} over {n_sample} of "
-                                   f"{cfg.n_layers} layers, scaled to all layers, plus the "
-                                   f"lm_head"},
+                         "cpu": cpu_model(), "kind": "oracle",
+                         "sample": f"per step: the oracle's plain target decoding of one token "
+                                   f"through all {cfg.n_layers} layers and the lm_head at context "
+                                   f"{cfg.prompt_len} (random bf16 KV prefix); float64 GEMMs on "
+                                   f"NumPy's threads"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
+        "step_ms": {"median": statistics.median(times) * 1e3,
+                    "std": (statistics.stdev(times) * 1e3 if len(times) > 1 else 0.0)},
+        "setup_s": round(setup, 1),
     }
     print(json.dumps(line))
 
 
-def workload_name():
-    return ("Qwen2.5-7B-shaped decoder (28 layers, hidden 3584, 28/4 heads, FFN 18944, vocab "
-            "152064), random bf16 init; 11 resident layers + 17 int4 g64 substitutes with "
-            "pinned-host bf16 originals streamed per verify; prompt 512; SubSpec tree depth 48, "
-            "width 8, draft T 0.2, greedy; step = one draft/verify/accept cycle")
-
-
 # ------------------------------------------------------------------ main --
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
-    ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--quick", action="store_true")
-    args = ap.parse_args()
-    world, rank, local = dist_setup()
-    if args.impl == "reference":
-        run_reference(args, world, rank)
-        return
-    import substitute_speculative_decoding_gb300 as sub
-
-    assert args.warmup >= 0 and args.steps >= 1
-    cfg = synthetic.CONFIGS[CONFIG]
-    dev = torch.device("cuda", torch.cuda.current_device())
-    pk = peaks()
-    t_setup = time.perf_counter()
+def build_model(sub, cfg, wl, dev, max_seq):
     weights = synthetic.make_model(cfg, device=dev)
-    max_seq = cfg.prompt_len + max(E2E_NEW, (args.warmup + args.steps + 2) * (DEPTH + 1)) + 64
     model = sub.Model(cfg, weights, max_seq=max_seq, max_depth=DEPTH, max_width=WIDTH,
-                      max_prompt=cfg.prompt_len)
+                      max_prompt=cfg.prompt_len, staging_layers=wl["staging"],
+                      embed_on_host=wl["embed_on_host"])
     # the substitutes' device tensors, for the kernel measurement
     model.w4_mats = []
     for i in range(cfg.n_resident, cfg.n_layers):
@@ -422,11 +488,44 @@ def main():
     for i in range(cfg.n_resident, cfg.n_layers):
         for name in synthetic.LAYER_TENSORS:
             weights["layers"][i][name] = weights["layers"][i][name].to("cpu")
+    if wl["embed_on_host"]:
+        weights["embed"] = weights["embed"].to("cpu")
     torch.cuda.empty_cache()
+    return weights, model
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="qwen7b", choices=sorted(WORKLOADS))
+    ap.add_argument("--new", type=int, default=None, help="tokens generated by the e2e leg")
+    ap.add_argument("--quick", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    import substitute_speculative_decoding_gb300 as sub
+
+    assert args.warmup >= 0 and args.steps >= 1
+    wl = WORKLOADS[args.workload]
+    cfg = synthetic.CONFIGS[wl["cfg"]]
+    mode = 1 if cfg.mode == "gumbel" else 0
+    e2e_new = args.new or wl["e2e_new"]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    pk = peaks()
+    t_setup = time.perf_counter()
+    max_seq = cfg.prompt_len + max(e2e_new, (args.warmup + args.steps + 2) * (DEPTH + 1)) + 64
+    weights, model = build_model(sub, cfg, wl, dev, max_seq)
     t_setup = time.perf_counter() - t_setup
+    timeouts0 = sub.pipeline_timeouts()
 
     prompt = synthetic.make_prompt(cfg)
-    dcfg = sub.Model.decode_cfg(DEPTH, WIDTH, DRAFT_T)
+    dcfg = sub.Model.decode_cfg(DEPTH, WIDTH, DRAFT_T, mode=mode, target_temp=cfg.target_temp,
+                                seed=cfg.seed)
     kernels_per_cycle, h2d_per_cycle = model.cycle_info(dcfg)
     stream = torch.cuda.current_stream()
     model.prefill(prompt, dcfg, stream)
@@ -438,15 +537,17 @@ def main():
     time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    evs[0].record(stream)
     torch.cuda.nvtx.range_push("timed_cycles")   # lets a profiler select exactly the steps
-    model.decode_cycles(dcfg, args.steps, stream)
+    for i in range(args.steps):
+        model.decode_cycles(dcfg, 1, stream)
+        evs[i + 1].record(stream)
     torch.cuda.nvtx.range_pop()
-    ev1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
-    ms = ev0.elapsed_time(ev1)
+    ms = evs[0].elapsed_time(evs[-1])
+    cyc = [evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps)]
     clk = clocks.stop()
     _, e1, c1 = model.decode_read()
     tokens = e1 - e0
@@ -456,22 +557,34 @@ def main():
     value = tokens_all / (ms_max / 1e3)
 
     link = measure_link(dev)
-    bound = cycle_bound(cfg, pk, tau, cfg.prompt_len + tokens, link)
+    bound = cycle_bound(cfg, pk, tau, cfg.prompt_len + tokens, link, wl["staging"])
     kern = kernel_measurements(sub, cfg, weights, model, pk, dev, args.quick)
 
     # e2e: the public call with host buffers, prefill included
     e2e = None
     if not args.quick:
         t0 = time.perf_counter()
-        out, st = model.generate(prompt, E2E_NEW, DEPTH, WIDTH, DRAFT_T)
+        out, st = model.generate(prompt, e2e_new, DEPTH, WIDTH, DRAFT_T, mode=mode,
+                                 target_temp=cfg.target_temp, seed=cfg.seed)
         t_e2e = time.perf_counter() - t0
-        e2e = {"value": E2E_NEW / t_e2e, "unit": "tokens/s",
-               "h2d_bytes_per_step": int(prompt.numel() * 4 + h2d_per_cycle * (st.cycles + 1)),
-               "d2h_bytes_per_step": int(E2E_NEW * 4 + 32 * st.cycles),
-               "tokens": E2E_NEW, "seconds": t_e2e, "prefill_ms": st.t_prefill_ms,
+        cycles = max(int(st.cycles), 1)
+        h2d_total = prompt.numel() * 4 + h2d_per_cycle * (st.cycles + 1)
+        d2h_total = e2e_new * 4 + 32 * (st.cycles + 1)
+        e2e = {"value": e2e_new / t_e2e, "unit": "tokens/s",
+               "h2d_bytes_per_step": int(h2d_total / cycles),
+               "d2h_bytes_per_step": int(d2h_total / cycles),
+               "tokens": e2e_new, "seconds": t_e2e, "prefill_ms": st.t_prefill_ms,
                "decode_ms": st.t_decode_ms, "tau": st.tau, "cycles": st.cycles,
-               "note": "h2d counts the prompt and the offloaded originals streamed for the "
-                       "prefill and every verify pass"}
+               "per_cycle_ms": {"draft": st.t_draft_ms / cycles,
+                                "verify": st.t_verify_ms / cycles,
+                                "copy_unhidden": st.t_copy_unhidden_ms / cycles},
+               "draft_over_target": (st.t_draft_ms / st.t_verify_ms
+                                     if st.t_verify_ms > 0 else None),
+               "near_tie_events": st.near_tie_events,
+               "note": "per step = per decode cycle: the run's host-to-device bytes (prompt, the "
+                       "offloaded originals streamed for the prefill and every verify) and "
+                       "device-to-host bytes (state reads, tokens) over its cycles; "
+                       "draft_over_target is the denominator term D*t_draft/t_target"}
 
     g = kern["w4_gemv_m8"]
     traffic = profile_traffic("gemv_w4")
@@ -483,23 +596,45 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.quick:
-        n_sample = 4
-        tl, th = oracle_token_sample(cfg, weights, n_sample)
-        t_tok = tl * cfg.n_layers / n_sample + th
-        cpu = {"value": 1.0 / t_tok, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
-               "sample": f"oracle plain target decoding of one token at context "
-                         f"{cfg.prompt_len} over {n_sample} of {cfg.n_layers} layers (random "
-                         f"bf16 KV prefix), scaled to all layers, plus the lm_head"}
+        # one full token through every layer and the head on all host cores,
+        # then a one-thread sample (2 layers + head, scaled) in a child process
+        glob, layers = oracle_weights(weights, range(cfg.n_layers)) \
+            if args.workload != "qwen32b" else (None, None)
+        one = oracle_one_thread(cfg)
+        if glob is not None:
+            t_tok = oracle_token(cfg, glob, layers, cfg.prompt_len)
+            del glob, layers
+            cpu = {"value": 1.0 / t_tok, "unit": "tokens/s", "cores": cpu_cores(),
+                   "cpu": cpu_model(), "kind": "oracle",
+                   "sample": f"the oracle's plain target decoding of one token through all "
+                             f"{cfg.n_layers} layers and the lm_head at context {cfg.prompt_len} "
+                             f"(random bf16 KV prefix), float64 GEMMs on NumPy's threads"}
+        else:
+            cpu = {"value": None, "unit": "tokens/s", "cores": cpu_cores(), "cpu": cpu_model(),
+                   "kind": "oracle", "sample": "all-core token skipped (the 32B oracle weights "
+                                               "do not fit beside the pinned originals)"}
+        if "layers_s" in one:
+            t1 = one["layers_s"] * cfg.n_layers / 2 + one["head_s"]
+            cpu["one_thread"] = {"value": 1.0 / t1, "unit": "tokens/s", "cores": 1,
+                                 "sample": "2 layers and the lm_head timed on one thread, "
+                                           f"layers scaled to {cfg.n_layers}"}
+        else:
+            cpu["one_thread"] = one
 
+    timeouts = sub.pipeline_timeouts() - timeouts0
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": workload_name(), "prompt": cfg.prompt_len, "depth": DEPTH,
+        "config": {"workload": wl["text"], "prompt": cfg.prompt_len, "depth": DEPTH,
                    "width": WIDTH, "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (8.5 GB of weights read per draft level)"},
+                   "l2": "inputs larger than L2 (every draft level reads all weights: "
+                         f"{bound['level_bytes'] / 1e9:.2f} GB)"},
         "tau": tau, "tokens_timed": tokens_all,
+        "cycle_ms": {"median": statistics.median(cyc),
+                     "std": statistics.stdev(cyc) if len(cyc) > 1 else 0.0,
+                     "min": min(cyc), "max": max(cyc)},
         "bound": {k: (round(v, 3) if isinstance(v, float) else v) for k, v in bound.items()},
         "frac_of_bound": value / world / bound["tokens_per_s"] if bound["tokens_per_s"] else None,
         "host_link_gbs": round(link, 1),
@@ -507,6 +642,8 @@ def main():
         "gpu_launches": kernels_per_cycle * args.steps, "kernels_per_cycle": kernels_per_cycle,
         "clocks": clk, "setup_s": round(t_setup, 1),
         "model_device_bytes": model.device_bytes(),
+        "device_bytes_total": int(torch.cuda.memory_allocated() + model.device_bytes()),
+        "pipeline_timeouts": timeouts, "valid": timeouts == 0,
     }
     if rank == 0:
         print(json.dumps(line))
@@ -514,6 +651,8 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+    if timeouts:
+        raise SystemExit(f"{timeouts} bounded pipeline wait(s) ran out: the numbers are invalid")
 
 
 def profile_traffic(kernel):

@@ -1,7 +1,7 @@
 """Kernel micro-benchmarks on single shapes of the decode path (for timing and
-for profiler captures on a small case).
+for profiler captures on a small case), a measurement tool beside bench.py.
 
-    python -m substitute_speculative_decoding_gb300.kernel_bench <case> [--iters N]
+    python kernel_bench.py <case> [--iters N]
 
 Cases (Qwen2.5-7B draft/verify shapes; operand sets rotate over more memory
 than the 129 MB L2):
@@ -30,7 +30,7 @@ import sys
 
 import torch
 
-sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
 
 import synthetic  # noqa: E402
 import substitute_speculative_decoding_gb300 as sub  # noqa: E402
