@@ -13,7 +13,8 @@
 // Rows are (query, head-in-group) pairs of one KV head, so the Hq/Hkv query
 // heads that share a KV head read each K/V tile once.  A CTA of four warps
 // owns 64 rows; S = Q K^T and O += P V run on mma.sync m16n8k16 with fp32
-// accumulators and an online softmax in fp32 (FlashAttention-2 style).  Keys
+// accumulators and an online softmax in fp32 (FlashAttention-2 style); P
+// enters P V as a bf16 pair hi + lo, which keeps it to ~2^-17.  Keys
 // may be split over up to 16 CTAs (grid.z) that form one thread-block cluster;
 // their partial (max, sum, O) are merged in split order through distributed
 // shared memory, so no global scratch and no second launch are needed.
@@ -291,7 +292,11 @@ __global__ void __launch_bounds__(THREADS) tree_attn_kernel(AttnArgs a) {
       m_run[h] = m_new;
     }
     float tsum[2] = {0.f, 0.f};
-    uint32_t pa[KT / 16][4];
+    // P as the A operand in two bf16 parts, hi = bf16(p) and lo = bf16(p - hi)
+    // (p - hi is exact in fp32), so that P.V keeps p to ~2^-17 relative: one
+    // bf16 rounding of P (2^-9) shifts a layer's output by ~0.5% against the
+    // exact softmax, which the decode's token choices cannot absorb
+    uint32_t pa[KT / 16][4], pl[KT / 16][4];
 #pragma unroll
     for (int j = 0; j < KT / 8; ++j) {
       float p[4];
@@ -301,14 +306,13 @@ __global__ void __launch_bounds__(THREADS) tree_attn_kernel(AttnArgs a) {
         p[e] = (m_run[h] == -INFINITY) ? 0.f : exp2f(s[j][e] - m_run[h]);
         tsum[h] += p[e];
       }
-      // P as the A operand: n8 tiles 2i, 2i+1 form k16 step i
-      if (j & 1) {
-        pa[j >> 1][2] = pack_bf16x2(p[0], p[1]);
-        pa[j >> 1][3] = pack_bf16x2(p[2], p[3]);
-      } else {
-        pa[j >> 1][0] = pack_bf16x2(p[0], p[1]);
-        pa[j >> 1][1] = pack_bf16x2(p[2], p[3]);
-      }
+      // n8 tiles 2i, 2i+1 form k16 step i
+      const int r0 = (j & 1) ? 2 : 0;
+      const uint32_t h01 = pack_bf16x2(p[0], p[1]), h23 = pack_bf16x2(p[2], p[3]);
+      pa[j >> 1][r0] = h01;
+      pa[j >> 1][r0 + 1] = h23;
+      pl[j >> 1][r0] = pack_bf16x2(p[0] - bf16lo(h01), p[1] - bf16hi(h01));
+      pl[j >> 1][r0 + 1] = pack_bf16x2(p[2] - bf16lo(h23), p[3] - bf16hi(h23));
     }
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -330,6 +334,8 @@ __global__ void __launch_bounds__(THREADS) tree_attn_kernel(AttnArgs a) {
                   b0, b1, b2, b3);
         mma_bf16_16816(o[2 * dd], pa[kk], b0, b1);
         mma_bf16_16816(o[2 * dd + 1], pa[kk], b2, b3);
+        mma_bf16_16816(o[2 * dd], pl[kk], b0, b1);
+        mma_bf16_16816(o[2 * dd + 1], pl[kk], b2, b3);
       }
     row_offsets(buf, t + 2);
     __syncthreads();   // buffer reuse by the next prefetch; row offsets of tile t + 2
