@@ -1,0 +1,32 @@
+"""Oracle parity at full size: the Qwen2.5-7B- and Llama-3.1-8B-shaped
+workloads (depth 48, width 8, greedy), decoded on the GPU through the public
+entry points and checked against the CPU oracle -- the whole emitted stream by
+teacher forcing, and for the first two cycles and every 16th (32nd for Llama): the tree level
+by level against the oracle's selection on the GPU's draft logits, a sample
+of verify rows, the first draft levels' logits, and the accept walk.  At this
+depth the logit tolerance is calibrated against the oracle run with float32
+GEMM accumulation (tests/fullsize.py explains why); the near-tie counts and
+error statistics are printed."""
+import pytest
+
+import synthetic
+import fullsize
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+
+@pytest.fixture(scope="module")
+def sub():
+    import substitute_speculative_decoding_gb300 as s
+    return s
+
+
+def test_qwen7b_workload_matches_the_oracle(sub):
+    r = fullsize.run(sub, synthetic.CONFIGS["qwen7b"], 256)
+    assert r["cycles"] >= 2 and len(r["checked_cycles"]) >= 3
+
+
+def test_llama8b_workload_matches_the_oracle(sub):
+    # every 32nd cycle: the 1.5k-row oracle forwards dominate this test's time
+    r = fullsize.run(sub, synthetic.CONFIGS["llama8b"], 512, verify_sample=16, every=32)
+    assert r["cycles"] >= 2 and len(r["checked_cycles"]) >= 3
