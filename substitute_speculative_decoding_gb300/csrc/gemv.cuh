@@ -26,6 +26,8 @@
 // (RoPE on q and k from rows paired i / i + d/2 inside one tile, bf16 q out,
 // k and v written into the paged KV cache).
 #pragma once
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include "common.cuh"
 
 namespace sub {
@@ -146,6 +148,12 @@ size_t gemv_tma_scratch_floats(const GemvArgs& a, bool is_w4, int epi);
 int32_t gemv_init();
 // Pipeline waits that ran out since load (each one is a bug; never expected).
 int32_t gemv_tma_timeouts(unsigned int* out);
+// The driver's tensor-map encoder (null if unavailable), and a 2-D tiled map
+// over a row-major [rows, cols] array with the given row stride and box
+// (128-byte swizzle when swz); false when the encoder or the alignment refuses.
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn();
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* ptr, int64_t cols,
+              int64_t rows, int64_t stride_bytes, int box_cols, int box_rows, bool swz);
 // One bounded wait on an mbarrier nothing arrives on; *polls = polls made
 // before it was satisfied, 0 when it gave up after `limit` polls.
 int32_t bounded_wait_selftest(uint32_t limit, uint32_t* polls);

@@ -41,10 +41,13 @@
 #include <algorithm>
 #include <mutex>
 #include "gemv.cuh"
+#include "tma.cuh"
 
 namespace sub {
 
 namespace {
+
+using namespace tmah;
 
 constexpr int NCW = 8;                  // consumer warps; one 16-row tile each
 constexpr int NTHR = (NCW + 1) * 32;    // plus the producer warp
@@ -57,79 +60,10 @@ __device__ unsigned int g_tma_timeouts;  // waits that ran out (never expected)
 
 __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-__device__ __forceinline__ uint4 lds128(uint32_t a) {
-  uint4 r;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "r"(a));
-  return r;
-}
-__device__ __forceinline__ uint2 lds64(uint32_t a) {
-  uint2 r;
-  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(a));
-  return r;
-}
-
-// ------------------------------------------------------------- mbarriers --
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Wait for the phase of the given parity to complete.  Bounded: a wait that
-// runs out records itself and returns, so a broken pipeline ends the kernel
-// with wrong numbers and a host-visible count instead of a hang.
-__device__ __forceinline__ uint32_t mbar_wait_polls(uint32_t bar, uint32_t parity, uint32_t limit) {
-  for (uint32_t i = 0; i < limit; ++i)
-    if (mbar_try_wait(bar, parity)) return i + 1;
-  return 0;   // gave up
-}
+// Bounded wait: one that runs out is counted (sub_pipeline_timeouts) and the
+// kernel goes on with wrong numbers instead of hanging.
 __device__ __forceinline__ void mbar_wait(uint32_t bar, uint32_t parity) {
   if (!mbar_wait_polls(bar, parity, 1u << 20)) atomicAdd(&g_tma_timeouts, 1u);
-}
-
-// 2-D tiled TMA load of one box at (x, y) (x in elements of the innermost
-// dimension) into shared memory, completing bytes on the mbarrier.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
-
-// 3-D tiled TMA load: coordinates (x, y, z), innermost first.
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            int z, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
-      : "memory");
-}
-
-// Pull a tensor-map descriptor into the TMA unit's cache ahead of first use.
-__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
 __device__ __forceinline__ void consumer_sync() {
@@ -709,8 +643,6 @@ int32_t gemv_init() {
   return SUB_OK;
 }
 
-namespace {
-
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -738,6 +670,8 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* ptr
             swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+namespace {
 
 template <bool W4, int MT, int EPI>
 cudaError_t tma_attr() {

@@ -718,6 +718,9 @@ extern "C" int32_t sub_model_create(const sub_model_desc* desc, sub_model** out)
       CREATE_CUDA(cudaEventCreate(&m->ev_tstaged[j]));
     }
   }
+  CREATE_CUDA(cudaMemset(m->xn, 0, R * H * 2));
+  CREATE_CUDA(cudaMemset(m->attn, 0, R * m->q_dim * 2));
+  CREATE_CUDA(cudaMemset(m->act, 0, R * F * 2));
   CREATE_CUDA(cudaDeviceSynchronize());
   *out = m;
   return SUB_OK;
