@@ -9,6 +9,8 @@ than the 129 MB L2):
   gemv_w4     int4 weights 37888x3584, M = 8 (a substitute gate+up pair)
   attn_draft  8 tree queries, 28/4 heads, d 128, 640 committed keys
   attn_verify 385 tree queries, same heads and keys
+  attn32      the Qwen2.5-32B attention sweep (40/8 heads; 385 or 8 queries over 1k, 4k
+              and 16k committed keys)
   gemm_bf16   bf16 weights 18944x3584, M = 385 (a verify FFN matrix, tcgen05)
   gemm_w4     int4 weights 18944x3584, M = 385 (tcgen05 with the dequantising stage)
   gemv_{bf16,w4}_{down,o}  down projection 3584x18944 / o projection 3584x3584, M = 8
@@ -170,6 +172,33 @@ def main():
                                            depth=dp), a.iters)
         byt = (n_prefix + n_tree) * hkv * d * 4 + 2 * nq * hq * d * 2
         res.update(ms=ms, gbs=byt / ms / 1e6)
+    elif a.case == "attn32":
+        # the Qwen2.5-32B attention sweep of bench.py: 40/8 heads, d 128, a
+        # depth-48 width-8 tree over 1k/4k/16k committed keys, 385 or 8 queries,
+        # key/value copies rotated over at least 4x L2
+        import math
+        hq, hkv, d = 40, 8, 128
+        tok, par, dep = synthetic.random_tree(48, 8, 3, 1000)
+        anc = synthetic.ancestors(par, dep, 48).to(dev)
+        dep = dep.to(dev)
+        n_tree = len(par)
+        for lkv in (1024, 4096, 16384):
+            kv_bytes = (lkv + n_tree) * hkv * d * 4
+            nc = max(2, math.ceil(4 * 129 * 2 ** 20 / kv_bytes))
+            caches = []
+            for _ in range(nc):
+                kv, keep = sub.make_kv(1, hkv, d, lkv + n_tree + 64)
+                keep[0].normal_()
+                keep[1].normal_()
+                caches.append((kv, keep))
+            for nq, tag in ((n_tree, "verify385"), (8, "draft8")):
+                q = torch.randn(nq, hq, d, device=dev).to(torch.bfloat16)
+                an, dp = anc[-nq:].contiguous(), dep[-nq:].contiguous()
+                ms = _time(lambda i: sub.tree_attn(q, caches[i % nc][0], 0, lkv, lkv, n_tree,
+                                                   anc=an, depth=dp), max(a.iters, nc))
+                byt = kv_bytes + 4 * nq * hq * d
+                res[f"{tag}_kv{lkv}"] = dict(ms=round(ms, 5), gbs=round(byt / ms / 1e6, 1))
+            del caches
     elif a.case in ("draft_level", "verify_pass"):
         res.update(_model_pass(a.case))
     else:
