@@ -45,9 +45,17 @@ def generate_plain(cfg, glob, layers, prompt, n_new, mode="greedy", temp=1.0, se
     return out
 
 
-def draft_tree(cfg, glob, draft_layers, root_token, n, ks, vs, depth, width, draft_temp):
+def draft_tree(cfg, glob, draft_layers, root_token, n, ks, vs, depth, width, draft_temp,
+               stop_logp=None):
     """Build the static tree for one cycle.  Returns (tokens, parent, depth,
-    draft logits per level).  ks/vs: the target's committed KV, length n."""
+    draft logits per level).  ks/vs: the target's committed KV, length n.
+
+    Adaptive depth (stop_logp not None): after a level is added, drafting stops
+    when the best cumulative sharpened log-probability among its nodes is below
+    stop_logp -- deeper nodes would hang below a path the draft itself finds
+    unlikely ("Low-Bit Shadow" report 3.7 and 10.1 (3): the back half of the
+    48-level tree rarely pays off).  The tree then has fewer than `depth`
+    levels; everything downstream (verify, accept) takes it as it is."""
     tokens = [int(root_token)]
     parent = [-1]
     dep = [0]
@@ -83,6 +91,8 @@ def draft_tree(cfg, glob, draft_layers, root_token, n, ks, vs, depth, width, dra
             parent.append(int(pa))
             dep.append(dep[pa] + 1)
             score.append(float(s))
+        if stop_logp is not None and max(sc) < stop_logp:
+            break
     return (np.array(tokens, np.int64), np.array(parent, np.int64),
             np.array(dep, np.int64), level_logits)
 
@@ -95,8 +105,10 @@ def verify_tree(cfg, glob, layers, tokens, parent, dep, n, ks, vs):
 
 
 def generate_subspec(cfg, glob, target_layers, draft_layers, prompt, n_new, depth, width,
-                     draft_temp=0.2, mode="greedy", temp=1.0, seed=0, record=None):
-    """SubSpec decoding; returns (tokens, per-cycle emitted counts)."""
+                     draft_temp=0.2, mode="greedy", temp=1.0, seed=0, record=None,
+                     stop_logp=None):
+    """SubSpec decoding; returns (tokens, per-cycle emitted counts).  With
+    stop_logp the tree depth adapts per cycle (see draft_tree)."""
     prompt = np.asarray(prompt, np.int64)
     n = len(prompt)
     logits, ks, vs = prefill(cfg, glob, target_layers, prompt)
@@ -105,7 +117,7 @@ def generate_subspec(cfg, glob, target_layers, draft_layers, prompt, n_new, dept
     emitted = []
     while len(out) < n_new:
         tokens, parent, dep, dl = draft_tree(cfg, glob, draft_layers, root, n, ks, vs,
-                                             depth, width, draft_temp)
+                                             depth, width, draft_temp, stop_logp)
         lg, nk, nv = verify_tree(cfg, glob, target_layers, tokens, parent, dep, n, ks, vs)
         choice = _choose(lg, mode, temp, seed, n + dep + 1)
         acc, bonus = accept_walk(tokens, parent, choice)

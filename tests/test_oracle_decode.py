@@ -93,3 +93,40 @@ def test_check_stream_catches_a_wrong_token(tiny):
     # the planted token is caught; later positions see a changed context
     assert r["mismatch"][:1] == [6]
     assert decode.check_stream(CFG, glob, layers, prompt, ref, gap=1e-6)["mismatch"] == []
+
+
+# ---- adaptive draft depth ("Low-Bit Shadow" report 3.7, 10.1 (3)) ----
+@pytest.mark.parametrize("stop", [-1.0, -4.0, -12.0])
+@pytest.mark.parametrize("mode,temp", [("greedy", 1.0), ("gumbel", 0.6)])
+def test_adaptive_depth_is_lossless(tiny, stop, mode, temp):
+    glob, layers, draft, prompt = tiny
+    ref = decode.generate_plain(CFG, glob, layers, prompt, 24, mode, temp, seed=7)
+    got, emitted = decode.generate_subspec(CFG, glob, layers, draft, prompt, 24, 8, 2, 0.2, mode,
+                                           temp, seed=7, stop_logp=stop)
+    assert got == ref
+    assert all(1 <= e <= 9 for e in emitted)
+
+
+def test_adaptive_depth_limits(tiny):
+    """A threshold below every score changes nothing; one above every score
+    (log-probabilities are <= 0) drafts exactly one level per cycle; a higher
+    threshold never drafts deeper trees."""
+    glob, layers, draft, prompt = tiny
+    recs = {}
+    for stop in (None, -1e9, -6.0, -2.0, 1.0):
+        rec = []
+        out, _ = decode.generate_subspec(CFG, glob, layers, draft, prompt, 20, 6, 2,
+                                         record=rec, stop_logp=stop)
+        recs[stop] = (out, rec)
+    base_out, base_rec = recs[None]
+    out, rec = recs[-1e9]
+    assert out == base_out
+    assert all(np.array_equal(a["tokens"], b["tokens"]) and np.array_equal(a["parent"], b["parent"])
+               for a, b in zip(rec, base_rec))
+    _, rec1 = recs[1.0]
+    assert all(len(r["tokens"]) == 1 + 2 and int(max(r["depth"])) == 1 for r in rec1)
+
+    def mean_depth(rec):
+        return np.mean([int(max(r["depth"])) for r in rec])
+    assert mean_depth(recs[-2.0][1]) <= mean_depth(recs[-6.0][1]) <= mean_depth(base_rec)
+    assert mean_depth(recs[-6.0][1]) < 6   # the threshold does stop some cycles early
