@@ -287,6 +287,17 @@ typedef struct {
   float target_temp;
   uint64_t seed;
   int32_t use_graph;      /* capture one decode cycle as a CUDA graph */
+  /* Adaptive depth ("Low-Bit Shadow" report 3.7 and 10.1 (3)): after each
+   * level is added, drafting stops when the best cumulative sharpened
+   * log-probability among its nodes is below stop_logp; the cycle then
+   * verifies the tree with the levels drafted so far, and the accept walk
+   * stops at the last of them.  Only a finite negative value turns this on:
+   * 0 (a zero-filled config), -INFINITY and NaN draft all `depth` levels.
+   * The decision is taken on the device in fp32.  In a captured cycle
+   * (use_graph) the levels after the first are conditional graph nodes, so
+   * a level not drafted launches nothing; without use_graph the host reads
+   * the decision after every level (one synchronisation per level). */
+  float stop_logp;
 } sub_decode_cfg;
 
 typedef struct {
@@ -314,6 +325,8 @@ typedef struct {
    * logits / T + Gumbel noise) differed by less than 1e-2 on the device: the
    * positions where a rounding difference could pick another token */
   int64_t near_tie_events;
+  /* draft levels run over all cycles (cycles * depth without adaptive depth) */
+  int64_t drafted_levels;
 } sub_stats;
 
 /* Step-wise decoding (the pieces sub_generate is made of).

@@ -67,7 +67,8 @@ class ModelDesc(C.Structure):
 
 class DecodeCfg(C.Structure):
     _fields_ = [("depth", _i32), ("width", _i32), ("draft_temp", _f32), ("mode", _i32),
-                ("target_temp", _f32), ("seed", _u64), ("use_graph", _i32)]
+                ("target_temp", _f32), ("seed", _u64), ("use_graph", _i32),
+                ("stop_logp", _f32)]
 
 
 class Stats(C.Structure):
@@ -75,7 +76,7 @@ class Stats(C.Structure):
                 ("t_prefill_ms", C.c_double), ("t_decode_ms", C.c_double),
                 ("accept_hist", _i64 * 65), ("t_draft_ms", C.c_double),
                 ("t_verify_ms", C.c_double), ("t_copy_unhidden_ms", C.c_double),
-                ("near_tie_events", _i64)]
+                ("near_tie_events", _i64), ("drafted_levels", _i64)]
 
 
 def _decl(name, args):
@@ -384,8 +385,10 @@ class Model:
 
     @staticmethod
     def decode_cfg(depth, width, draft_temp=0.2, mode=0, target_temp=1.0, seed=0,
-                   use_graph=True) -> DecodeCfg:
-        return DecodeCfg(depth, width, draft_temp, mode, target_temp, seed, int(use_graph))
+                   use_graph=True, stop_logp=None) -> DecodeCfg:
+        """stop_logp: None (every level drafted) or a negative threshold for adaptive depth."""
+        return DecodeCfg(depth, width, draft_temp, mode, target_temp, seed, int(use_graph),
+                         0.0 if stop_logp is None else float(stop_logp))
 
     def prefill(self, prompt, cfg: DecodeCfg, stream=None):
         self._prompt = prompt.to(torch.int32).contiguous()
@@ -408,11 +411,12 @@ class Model:
         return k.value, b.value
 
     def generate(self, prompt, n_new: int, depth: int, width: int, draft_temp=0.2, mode=0,
-                 target_temp=1.0, seed=0, use_graph=True):
+                 target_temp=1.0, seed=0, use_graph=True, stop_logp=None):
         """prompt: int32 CPU tensor -> (int32 CPU tensor [n_new], Stats)."""
         p = prompt.to(torch.int32).contiguous()
         out = torch.zeros(n_new, dtype=torch.int32)
-        cfg = DecodeCfg(depth, width, draft_temp, mode, target_temp, seed, int(use_graph))
+        cfg = self.decode_cfg(depth, width, draft_temp, mode, target_temp, seed, use_graph,
+                              stop_logp)
         st = Stats()
         _check(_generate(self.handle, C.c_void_p(p.data_ptr()), p.numel(), n_new, C.byref(cfg),
                          C.c_void_p(out.data_ptr()), C.byref(st)))

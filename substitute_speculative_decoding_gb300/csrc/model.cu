@@ -33,7 +33,13 @@ struct Matrices {
 };
 
 // Decode state on the device (one int each).
-enum { ST_N = 0, ST_EMITTED = 1, ST_NACC = 2, ST_BONUS = 3, ST_TIES = 4, ST_COUNT = 8 };
+enum {
+  ST_N = 0, ST_EMITTED = 1, ST_NACC = 2, ST_BONUS = 3, ST_TIES = 4,
+  ST_DLIM = 5,     // adaptive depth: levels drafted this cycle
+  ST_CONT = 6,     // adaptive depth: 1 while drafting goes on
+  ST_LEVELS = 7,   // adaptive depth: levels drafted since the prefill
+  ST_COUNT = 8
+};
 
 // Emitted tokens whose top-2 choice scores differ by less than this are
 // counted as near-ties (sub_stats.near_tie_events).
@@ -93,6 +99,8 @@ struct sub_model {
   size_t mat_bytes[7] = {};
   std::vector<uint16_t*> slots;
   cudaStream_t s_main = nullptr, s_copy = nullptr;
+  cudaStream_t s_cond = nullptr;   // captures the bodies of conditional draft levels
+  int64_t cond_kernels = 0;         // kernel nodes inside them (last capture)
   std::vector<cudaEvent_t> ev_staged, ev_free;
   // timing (recorded as graph event nodes inside a captured cycle): cycle
   // start, draft end, verify end; per offloaded layer, the compute stream
@@ -159,6 +167,7 @@ static void free_model(sub_model* m) {
     if (e) cudaEventDestroy(e);
   if (m->s_main) cudaStreamDestroy(m->s_main);
   if (m->s_copy) cudaStreamDestroy(m->s_copy);
+  if (m->s_cond) cudaStreamDestroy(m->s_cond);
   if (m->host_state) cudaFreeHost(m->host_state);
   if (m->host_prompt) cudaFreeHost(m->host_prompt);
   if (m->host_out) cudaFreeHost(m->host_out);
@@ -521,6 +530,39 @@ static int32_t forward(sub_model* m, bool draft, const FwdRows& r, float* logits
 }
 
 // ------------------------------------------------------------ tiny kernels --
+// Kernel nodes at the top level of a graph.
+static int64_t count_kernels(cudaGraph_t g) {
+  size_t n = 0;
+  if (cudaGraphGetNodes(g, nullptr, &n) != cudaSuccess || n == 0) return 0;
+  std::vector<cudaGraphNode_t> nodes(n);
+  if (cudaGraphGetNodes(g, nodes.data(), &n) != cudaSuccess) return 0;
+  int64_t k = 0;
+  for (auto nd : nodes) {
+    cudaGraphNodeType t;
+    if (cudaGraphNodeGetType(nd, &t) == cudaSuccess && t == cudaGraphNodeTypeKernel) ++k;
+  }
+  return k;
+}
+
+// Adaptive depth, after the expansion of level `level`: the new nodes (depth
+// level + 1) are slots s0 .. s0 + k - 1.  Drafting goes on -- the next level's
+// conditional node runs -- when their best cumulative score is >= stop.
+__global__ void adapt_kernel(const float* score, int s0, int k, float stop, int32_t* state,
+                             int level, cudaGraphConditionalHandle next, int has_next) {
+  pdl_wait();
+  pdl_trigger();
+  float mx = -INFINITY;
+  for (int i = threadIdx.x; i < k; i += 32) mx = fmaxf(mx, score[s0 + i]);
+  mx = warp_max(mx);
+  if (threadIdx.x == 0) {
+    const unsigned go = mx >= stop ? 1u : 0u;
+    state[ST_DLIM] = level + 1;
+    state[ST_CONT] = (int)go;
+    state[ST_LEVELS] += 1;
+    if (has_next) cudaGraphSetConditional(next, go);
+  }
+}
+
 // After accept: committed length += accepted + 1, the bonus becomes the root.
 __global__ void advance_kernel(int32_t* state, int32_t* root_token) {
   pdl_wait();
@@ -583,6 +625,7 @@ extern "C" int32_t sub_model_create(const sub_model_desc* desc, sub_model** out)
   CREATE_TRY(attn_init());
   CREATE_CUDA(cudaStreamCreateWithFlags(&m->s_main, cudaStreamNonBlocking));
   CREATE_CUDA(cudaStreamCreateWithFlags(&m->s_copy, cudaStreamNonBlocking));
+  CREATE_CUDA(cudaStreamCreateWithFlags(&m->s_cond, cudaStreamNonBlocking));
   for (cudaEvent_t* e : {&m->ev_fork, &m->ev_join})
     CREATE_CUDA(cudaEventCreateWithFlags(e, cudaEventDisableTiming));
   CREATE_CUDA(cudaEventCreateWithFlags(&m->ev_t0, cudaEventDisableTiming));
@@ -790,6 +833,12 @@ extern "C" int32_t sub_model_forward(sub_model* m, int32_t which, const int32_t*
 }
 
 // ----------------------------------------------------------------- generate --
+// Adaptive depth is on for a finite negative stop_logp (0, a zero-filled
+// config, -inf and NaN all draft every level).
+static bool adaptive(const sub_decode_cfg& c) {
+  return c.depth > 0 && c.stop_logp < 0.f && c.stop_logp > -INFINITY;
+}
+
 static int32_t accept_args(sub_model* m, const sub_decode_cfg& c, int n_nodes, AcceptArgs& a) {
   a = AcceptArgs{};
   a.logits = m->logits;
@@ -816,6 +865,7 @@ static int32_t accept_args(sub_model* m, const sub_decode_cfg& c, int n_nodes, A
   a.part_key2 = m->part_key2;
   a.near_ties = m->state + ST_TIES;
   a.tie_gap = NEAR_TIE_GAP;
+  a.depth_limit = adaptive(c) ? m->state + ST_DLIM : nullptr;
   return SUB_OK;
 }
 
@@ -832,7 +882,9 @@ static int32_t enqueue_cycle(sub_model* m, const sub_decode_cfg& c) {
   SUB_CUDA_TRY(mark(m->ev_cyc[0], m->s_main));
   SUB_TRY(begin_target_pass(m));
   // ---- draft ----
-  for (int lvl = 0; lvl < D; ++lvl) {
+  // one level: the draft forward over its rows, the expansion into the next
+  // level and, with adaptive depth, the decision to go on
+  auto level = [&](int lvl, cudaGraphConditionalHandle next, int has_next) -> int32_t {
     const int s0 = lvl == 0 ? 0 : 1 + (lvl - 1) * k;
     const int M = lvl == 0 ? 1 : k;
     FwdRows r{};
@@ -862,6 +914,63 @@ static int32_t enqueue_cycle(sub_model* m, const sub_decode_cfg& c) {
     e.part_sum = m->part_f + parts;
     e.counter = m->counters;
     SUB_TRY(launch_expand(e, m->s_main));
+    if (adaptive(c))
+      SUB_CUDA_TRY(launch_k(adapt_kernel, dim3(1), dim3(32), 0, m->s_main, (const float*)tr.score,
+                            1 + lvl * k, k, c.stop_logp, m->state, lvl, next, has_next));
+    return SUB_OK;
+  };
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  SUB_CUDA_TRY(cudaStreamIsCapturing(m->s_main, &cs));
+  const bool captured = cs == cudaStreamCaptureStatusActive;
+  if (!adaptive(c)) {
+    for (int lvl = 0; lvl < D; ++lvl) SUB_TRY(level(lvl, 0, 0));
+  } else if (!captured) {
+    // eager: ask the device after every level whether to go on
+    for (int lvl = 0; lvl < D; ++lvl) {
+      SUB_TRY(level(lvl, 0, 0));
+      if (lvl + 1 == D) break;
+      SUB_CUDA_TRY(cudaMemcpyAsync(m->host_state, m->state, ST_COUNT * 4, cudaMemcpyDeviceToHost,
+                                   m->s_main));
+      SUB_CUDA_TRY(cudaStreamSynchronize(m->s_main));
+      if (!m->host_state[ST_CONT]) break;
+    }
+  } else {
+    // captured: levels 1 .. D-1 are conditional (IF) nodes of the cycle's graph;
+    // each level's adapt kernel opens or closes the next one (handles default to
+    // closed at every launch), and a level's body is captured on a side stream
+    cudaGraph_t g = nullptr;
+    SUB_CUDA_TRY(cudaStreamGetCaptureInfo(m->s_main, &cs, nullptr, &g, nullptr, nullptr, nullptr));
+    std::vector<cudaGraphConditionalHandle> h(D, 0);
+    for (int lvl = 1; lvl < D; ++lvl)
+      SUB_CUDA_TRY(cudaGraphConditionalHandleCreate(&h[lvl], g, 0, cudaGraphCondAssignDefault));
+    SUB_TRY(level(0, D > 1 ? h[1] : 0, D > 1));
+    for (int lvl = 1; lvl < D; ++lvl) {
+      const cudaGraphNode_t* deps = nullptr;
+      size_t nd = 0;
+      SUB_CUDA_TRY(cudaStreamGetCaptureInfo(m->s_main, &cs, nullptr, &g, &deps, nullptr, &nd));
+      cudaGraphNodeParams p{};
+      p.type = cudaGraphNodeTypeConditional;
+      p.conditional.handle = h[lvl];
+      p.conditional.type = cudaGraphCondTypeIf;
+      p.conditional.size = 1;
+      cudaGraphNode_t node = nullptr;
+      SUB_CUDA_TRY(cudaGraphAddNode(&node, g, deps, nullptr, nd, &p));
+      SUB_CUDA_TRY(cudaStreamUpdateCaptureDependencies(m->s_main, &node, nullptr, 1,
+                                                       cudaStreamSetCaptureDependencies));
+      cudaGraph_t body = p.conditional.phGraph_out[0];
+      SUB_CUDA_TRY(cudaStreamBeginCaptureToGraph(m->s_cond, body, nullptr, nullptr, 0,
+                                                 cudaStreamCaptureModeRelaxed));
+      std::swap(m->s_main, m->s_cond);
+      const int32_t st_level = level(lvl, lvl + 1 < D ? h[lvl + 1] : 0, lvl + 1 < D);
+      std::swap(m->s_main, m->s_cond);
+      cudaGraph_t out = nullptr;
+      const cudaError_t ee = cudaStreamEndCapture(m->s_cond, &out);
+      SUB_TRY(st_level);
+      if (ee != cudaSuccess)
+        return fail(SUB_ECUDA, std::string("capture of a conditional draft level: ") +
+                                   cudaGetErrorString(ee));
+      m->cond_kernels += count_kernels(out);
+    }
   }
   // ---- verify ----
   SUB_CUDA_TRY(mark(m->ev_cyc[1], m->s_main));
@@ -902,7 +1011,8 @@ static int32_t enqueue_cycle(sub_model* m, const sub_decode_cfg& c) {
 
 static bool same_cfg(const sub_decode_cfg& a, const sub_decode_cfg& b) {
   return a.depth == b.depth && a.width == b.width && a.draft_temp == b.draft_temp &&
-         a.mode == b.mode && a.target_temp == b.target_temp && a.seed == b.seed;
+         a.mode == b.mode && a.target_temp == b.target_temp && a.seed == b.seed &&
+         std::memcmp(&a.stop_logp, &b.stop_logp, sizeof(float)) == 0;
 }
 
 static int32_t check_cfg(const sub_model* m, const sub_decode_cfg& c) {
@@ -923,6 +1033,7 @@ static int32_t ensure_graph(sub_model* m, const sub_decode_cfg& c) {
     m->graph = nullptr;
   }
   cudaGraph_t g = nullptr;
+  m->cond_kernels = 0;
   SUB_CUDA_TRY(cudaStreamBeginCapture(m->s_main, cudaStreamCaptureModeThreadLocal));
   const int32_t s = enqueue_cycle(m, c);
   const cudaError_t e = cudaStreamEndCapture(m->s_main, &g);
@@ -931,17 +1042,8 @@ static int32_t ensure_graph(sub_model* m, const sub_decode_cfg& c) {
     return s;
   }
   if (e != cudaSuccess) return fail(SUB_ECUDA, std::string("end capture: ") + cudaGetErrorString(e));
-  size_t n_nodes = 0;
-  cudaGraphGetNodes(g, nullptr, &n_nodes);
-  std::vector<cudaGraphNode_t> nodes(n_nodes);
-  int64_t kernels = 0;
-  if (n_nodes) {
-    cudaGraphGetNodes(g, nodes.data(), &n_nodes);
-    for (auto nd : nodes) {
-      cudaGraphNodeType t;
-      if (cudaGraphNodeGetType(nd, &t) == cudaSuccess && t == cudaGraphNodeTypeKernel) ++kernels;
-    }
-  }
+  // with adaptive depth: the count when every conditional level runs
+  const int64_t kernels = count_kernels(g) + m->cond_kernels;
   const cudaError_t ie = cudaGraphInstantiate(&m->graph, g, 0);
   cudaGraphDestroy(g);
   if (ie != cudaSuccess) {
@@ -1157,6 +1259,7 @@ extern "C" int32_t sub_generate(sub_model* m, const int32_t* prompt_host, int32_
     stats->t_verify_ms = t_verify >= 0.0 ? t_verify : -1.0;
     stats->t_copy_unhidden_ms = t_unhidden >= 0.0 ? t_unhidden : -1.0;
     stats->near_tie_events = m->host_state[ST_TIES];
+    stats->drafted_levels = adaptive(c) ? m->host_state[ST_LEVELS] : m->cycles * c.depth;
   }
   return check_timeouts(m);
 }

@@ -361,8 +361,10 @@ __global__ void __launch_bounds__(ACC_THREADS) accept_kernel(AcceptArgs a) {
   if (threadIdx.x == 0) {
     const int k = a.tree.width;
     int cur = 0, n_acc = 0;
+    const int dlim = a.depth_limit ? *a.depth_limit : 0x7fffffff;
     while (true) {
       const int d = a.tree.depth[cur];
+      if (d >= dlim) break;   // no drafted level below this node
       const int lo = 1 + d * k, hi = min(a.n_nodes, lo + k);
       int next = -1;
       for (int s = lo; s < hi; ++s)

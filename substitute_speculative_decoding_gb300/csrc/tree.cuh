@@ -53,6 +53,9 @@ struct AcceptArgs {
   unsigned long long* part_key2;
   int32_t* near_ties;
   float tie_gap;
+  // adaptive depth: tree levels deeper than *depth_limit were not drafted
+  // this cycle (their slots hold an earlier cycle's nodes); null = no limit
+  const int32_t* depth_limit;
 };
 size_t accept_scratch_bytes(int n_nodes, int n_chunks);
 int accept_pick_chunks(int n_nodes, int64_t V);

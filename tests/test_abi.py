@@ -63,3 +63,39 @@ def test_model_desc_validation(lib):
     h = C.c_void_p()
     assert s._model_create(C.byref(d), C.byref(h)) == s.SUB_EINVAL
     assert b"head_dim" in s._lib.sub_last_error()
+
+
+def test_struct_layouts_match_the_header(lib, tmp_path):
+    """Every ctypes mirror of a struct in include/sub_api.h has the C layout:
+    a small C program compiled against the header prints sizeof and the
+    offset of each field, and the binding must agree field by field."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    s = lib
+    mirrors = {"sub_kv_cache": s.KVCache, "sub_tree": s.Tree, "sub_w4": s.W4,
+               "sub_layer_desc": s.LayerDesc, "sub_model_desc": s.ModelDesc,
+               "sub_decode_cfg": s.DecodeCfg, "sub_stats": s.Stats}
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "sub_api.h"',
+             "int main(void) {"]
+    for cname, py in mirrors.items():
+        lines.append(f'  printf("{cname} size %zu\\n", sizeof({cname}));')
+        for f in py._fields_:
+            lines.append(f'  printf("{cname} {f[0]} %zu\\n", offsetof({cname}, {f[0]}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    subprocess.run([gcc, "-std=c11", "-I", inc, str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout
+    got = {}
+    for ln in out.splitlines():
+        cname, field, val = ln.split()
+        got[(cname, field)] = int(val)
+    for cname, py in mirrors.items():
+        assert got[(cname, "size")] == C.sizeof(py), cname
+        for f in py._fields_:
+            assert got[(cname, f[0])] == getattr(py, f[0]).offset, (cname, f[0])
