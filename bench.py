@@ -47,6 +47,11 @@ import synthetic  # noqa: E402
 
 METRIC = "generated tokens/s and τ (1 GB300); W4 GEMM + tree-attn GB/s vs 8 TB/s"
 DEPTH, WIDTH, DRAFT_T = 48, 8, 0.2
+# adaptive-depth thresholds (cumulative sharpened log-probability) and the
+# tokens each of their decodes generates
+ADAPTIVE_STOPS, ADAPTIVE_NEW = (-0.5, -2.0, -6.0, -16.0), 128
+# fixed tree depths of the depth sweep (the model is built for the deepest)
+DEPTH_SWEEP = (8, 16, 32, 48, 64)
 L2_BYTES = 129 * 2 ** 20
 ROTATE_BYTES = 4 * L2_BYTES      # operand sets rotated per timed sweep point
 
@@ -474,7 +479,7 @@ def run_reference(args, world, rank):
 # ------------------------------------------------------------------ main --
 def build_model(sub, cfg, wl, dev, max_seq):
     weights = synthetic.make_model(cfg, device=dev)
-    model = sub.Model(cfg, weights, max_seq=max_seq, max_depth=DEPTH, max_width=WIDTH,
+    model = sub.Model(cfg, weights, max_seq=max_seq, max_depth=max(DEPTH_SWEEP), max_width=WIDTH,
                       max_prompt=cfg.prompt_len, staging_layers=wl["staging"],
                       embed_on_host=wl["embed_on_host"])
     # the substitutes' device tensors, for the kernel measurement
@@ -518,7 +523,8 @@ def main():
     dev = torch.device("cuda", torch.cuda.current_device())
     pk = peaks()
     t_setup = time.perf_counter()
-    max_seq = cfg.prompt_len + max(e2e_new, (args.warmup + args.steps + 2) * (DEPTH + 1)) + 64
+    max_seq = cfg.prompt_len + max(e2e_new, (args.warmup + args.steps + 2) * (DEPTH + 1),
+                                   ADAPTIVE_NEW + max(DEPTH_SWEEP) + 1) + 64
     weights, model = build_model(sub, cfg, wl, dev, max_seq)
     t_setup = time.perf_counter() - t_setup
     timeouts0 = sub.pipeline_timeouts()
@@ -586,6 +592,30 @@ def main():
                        "device-to-host bytes (state reads, tokens) over its cycles; "
                        "draft_over_target is the denominator term D*t_draft/t_target"}
 
+    # adaptive depth: the same decode with drafting stopped per cycle once the
+    # best cumulative sharpened log-probability of a new level falls below a
+    # threshold (decode tokens/s over the cycles, prefill excluded)
+    adaptive = depth_sweep = None
+    if not args.quick:
+        depth_sweep = []
+        for dd in DEPTH_SWEEP:
+            _, sd = model.generate(prompt, ADAPTIVE_NEW, dd, WIDTH, DRAFT_T, mode=mode,
+                                   target_temp=cfg.target_temp, seed=cfg.seed)
+            cyc_d = max(int(sd.cycles), 1)
+            depth_sweep.append({"depth": dd,
+                                "decode_tokens_per_s": (ADAPTIVE_NEW - 1) / (sd.t_decode_ms / 1e3),
+                                "tau": sd.tau, "cycle_ms": sd.t_decode_ms / cyc_d,
+                                "cycles": sd.cycles})
+        adaptive = []
+        for stop in ADAPTIVE_STOPS:
+            _, sa = model.generate(prompt, ADAPTIVE_NEW, DEPTH, WIDTH, DRAFT_T, mode=mode,
+                                   target_temp=cfg.target_temp, seed=cfg.seed, stop_logp=stop)
+            cyc_a = max(int(sa.cycles), 1)
+            adaptive.append({"stop_logp": stop,
+                             "decode_tokens_per_s": (ADAPTIVE_NEW - 1) / (sa.t_decode_ms / 1e3),
+                             "tau": sa.tau, "mean_depth": sa.drafted_levels / cyc_a,
+                             "cycle_ms": sa.t_decode_ms / cyc_a, "cycles": sa.cycles})
+
     g = kern["w4_gemv_m8"]
     traffic = profile_traffic("gemv_w4")
     roof = {"kernel": "gemv_tma_kernel (int4 substitutes, M=8: the draft's substitute layers)",
@@ -639,6 +669,7 @@ def main():
         "frac_of_bound": value / world / bound["tokens_per_s"] if bound["tokens_per_s"] else None,
         "host_link_gbs": round(link, 1),
         "roofline": roof, "kernels": kern, "cpu_baseline": cpu, "e2e": e2e,
+        "adaptive": adaptive, "depth_sweep": depth_sweep,
         "gpu_launches": kernels_per_cycle * args.steps, "kernels_per_cycle": kernels_per_cycle,
         "clocks": clk, "setup_s": round(t_setup, 1),
         "model_device_bytes": model.device_bytes(),
