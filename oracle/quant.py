@@ -78,3 +78,114 @@ def w4_dequant(q, s, z, k: int) -> np.ndarray:
 def w4_gemm(x, q, s, z, k: int) -> np.ndarray:
     """Y[M, N] = X[M, K] . deq(W)^T, accumulated in float64, rounded to fp32."""
     return mm(x, w4_dequant(q, s, z, k))
+
+
+# ---------------------------------------------------------------------------
+# 2-, 3- and 4-bit substitutes (lower and mixed precision for the draft's
+# substitute layers: "Low-Bit Shadow" report 5.1 point 2 and 10.1 (2), which
+# leave 2/3-bit substitutes untested, and Critique (10), per-layer precision
+# chosen by sensitivity).  The quantiser is the min-max one above with
+# L = 2^bits - 1 levels in place of 15:
+#   s = bf16(fp32(hi - lo) / L); if s == 0 then s = 1;  z = bf16(fp32(-lo) / s)
+#   q = clamp(rint_even(fp32(w / s) + z), 0, L);   deq = bf16((q - z) * s)
+# Code layout of one 64-element group (8 * bits bytes, groups contiguous):
+#   bits 4: 32 bytes, byte j = element 2j (low nibble) | element 2j+1 << 4
+#   bits 2: 16 bytes, byte j = elements 4j .. 4j+3 at bits 0-1, 2-3, 4-5, 6-7
+#   bits 3: 24 bytes, bytes 0..15 the 2-bit layout of (code & 3), bytes
+#           16..23 the high bits: bit i of byte 16 + j = code(8j + i) >> 2
+# Codes past K are 0.
+# ---------------------------------------------------------------------------
+BITS = (2, 3, 4)
+
+
+def group_bytes(bits: int) -> int:
+    return 8 * bits
+
+
+def wq_codes(w, bits: int) -> tuple:
+    """w: float32 [N, K] of bf16 values -> (codes uint8 [N, K], s, z float32
+    [N, G] holding bf16 values), the min-max quantiser with 2^bits - 1 levels."""
+    assert bits in BITS
+    w = np.asarray(w, dtype=np.float32)
+    n, k = w.shape
+    g_count = n_groups(k)
+    levels = np.float32(2 ** bits - 1)
+    codes = np.zeros((n, k), dtype=np.uint8)
+    s_all = np.zeros((n, g_count), dtype=np.float32)
+    z_all = np.zeros((n, g_count), dtype=np.float32)
+    for g in range(g_count):
+        c0, c1 = g * GROUP, min(k, (g + 1) * GROUP)
+        blk = w[:, c0:c1]
+        lo = blk.min(axis=1)
+        hi = blk.max(axis=1)
+        s = round_bf16((hi - lo) / levels)
+        s = np.where(s == 0, np.float32(1.0), s).astype(np.float32)
+        z = round_bf16((-lo) / s)
+        t = (blk / s[:, None]) + z[:, None]          # two fp32 ops, each rounded
+        codes[:, c0:c1] = np.clip(np.rint(t), 0, levels).astype(np.uint8)
+        s_all[:, g] = s
+        z_all[:, g] = z
+    return codes, s_all, z_all
+
+
+def wq_pack_codes(codes, bits: int) -> np.ndarray:
+    """codes uint8 [N, K] (each < 2^bits) -> packed uint8 [N, G * 8 * bits]."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    n, k = codes.shape
+    g_count = n_groups(k)
+    full = np.zeros((n, g_count * GROUP), dtype=np.uint8)
+    full[:, :k] = codes
+    grp = full.reshape(n, g_count, GROUP)
+    if bits == 4:
+        out = grp[:, :, 0::2] | (grp[:, :, 1::2] << 4)
+    else:
+        lo2 = grp & 3
+        out = lo2[:, :, 0::4] | (lo2[:, :, 1::4] << 2) | (lo2[:, :, 2::4] << 4) | (lo2[:, :, 3::4] << 6)
+        if bits == 3:
+            hb = (grp >> 2) & 1
+            plane = np.zeros((n, g_count, 8), dtype=np.uint8)
+            for i in range(8):
+                plane |= (hb[:, :, i::8] << i).astype(np.uint8)
+            out = np.concatenate([out, plane], axis=2)
+    return out.reshape(n, g_count * group_bytes(bits)).astype(np.uint8)
+
+
+def wq_unpack_codes(q, k: int, bits: int) -> np.ndarray:
+    """packed uint8 [N, G * 8 * bits] -> codes [N, K]."""
+    q = np.asarray(q, dtype=np.uint8)
+    n = q.shape[0]
+    gb = group_bytes(bits)
+    g_count = q.shape[1] // gb
+    grp = q.reshape(n, g_count, gb)
+    codes = np.zeros((n, g_count, GROUP), dtype=np.uint8)
+    if bits == 4:
+        codes[:, :, 0::2] = grp & 0xF
+        codes[:, :, 1::2] = grp >> 4
+    else:
+        for i in range(4):
+            codes[:, :, i::4] = (grp[:, :, :16] >> (2 * i)) & 3
+        if bits == 3:
+            for i in range(8):
+                codes[:, :, i::8] |= ((grp[:, :, 16:24] >> i) & 1) << 2
+    return codes.reshape(n, g_count * GROUP)[:, :k]
+
+
+def wq_pack(w, bits: int) -> tuple:
+    """w: float32 [N, K] of bf16 values -> (q uint8 [N, G * 8 * bits], s, z)."""
+    codes, s, z = wq_codes(w, bits)
+    return wq_pack_codes(codes, bits), s, z
+
+
+def wq_dequant(q, s, z, k: int, bits: int) -> np.ndarray:
+    """bf16((q - z) * s) per element, as float32 [N, K] (exact before the
+    rounding, as for 4 bits: fewer code bits only shorten q - z)."""
+    codes = wq_unpack_codes(q, k, bits).astype(np.float64)
+    gidx = np.arange(k) // GROUP
+    s64 = np.asarray(s, np.float64)[:, gidx]
+    z64 = np.asarray(z, np.float64)[:, gidx]
+    return round_bf16(((codes - z64) * s64).astype(np.float32))
+
+
+def wq_gemm(x, q, s, z, k: int, bits: int) -> np.ndarray:
+    """Y[M, N] = X[M, K] . deq(W)^T, accumulated in float64, rounded to fp32."""
+    return mm(x, wq_dequant(q, s, z, k, bits))

@@ -16,18 +16,24 @@ def oracle_model(model: dict):
     return glob, layers
 
 
-def oracle_draft_layers(cfg, layers):
+def oracle_draft_layers(cfg, layers, bits=4):
     """Draft weights: resident layers shared, the rest replaced by the
-    dequantised int4 substitutes (oracle quantiser)."""
+    dequantised substitutes (oracle quantiser); bits: 2, 3 or 4 for every
+    substitute, or a list with one entry per layer (mixed precision)."""
     out = []
     for i, lw in enumerate(layers):
         if i < cfg.n_resident:
             out.append(lw)
             continue
+        b = bits[i] if isinstance(bits, (list, tuple)) else bits
         d = dict(lw)
         for name in synthetic.LAYER_TENSORS:
             w = lw[name]
-            q, s, z = quant.w4_pack(w)
-            d[name] = quant.w4_dequant(q, s, z, w.shape[1])
+            if b == 4:
+                q, s, z = quant.w4_pack(w)
+                d[name] = quant.w4_dequant(q, s, z, w.shape[1])
+            else:
+                q, s, z = quant.wq_pack(w, b)
+                d[name] = quant.wq_dequant(q, s, z, w.shape[1], b)
         out.append(d)
     return out
