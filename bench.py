@@ -316,6 +316,33 @@ def kernel_measurements(sub, cfg, weights, model, pk, dev, quick):
     del xv, yv
     if quick:
         return out
+    # --- 2-, 3- and 4-bit substitutes at M=8 on this workload's o/gate/up/down
+    # shapes (random bf16 weights packed on the device), rotated over >= 4x L2
+    h, f = cfg.hidden, cfg.ffn
+    low = {}
+    for bits in (2, 3, 4):
+        mats_b = []
+        for n, k in ((h, h), (f, h), (f, h), (h, f)):
+            wbytes = n * ((k + 63) // 64) * (8 * bits + 4)
+            for c in range(copies_for(wbytes)):
+                w = (torch.randn(n, k, device=dev) * 0.02).to(torch.bfloat16)
+                mats_b.append((*sub.wq_pack(w, bits), n, k))
+                del w
+        xb = {k: torch.randn(WIDTH, k, device=dev).to(torch.bfloat16) for *_, k in mats_b}
+        yb = {n: torch.empty(WIDTH, n, device=dev, dtype=torch.bfloat16) for *_, n, _k in mats_b}
+
+        def run_b(i, bits=bits, mats_b=mats_b, xb=xb, yb=yb):
+            q, s_, z, n, k = mats_b[i % len(mats_b)]
+            sub.wq_gemm(xb[k], q, s_, z, n, k, bits, out=yb[n])
+        msb = time_launches(run_b, len(mats_b), st)
+        bb = sum(q.numel() + s_.numel() * 2 + z.numel() * 2 + WIDTH * (n + k) * 2
+                 for q, s_, z, n, k in mats_b) / len(mats_b)
+        low[f"bits{bits}"] = dict(ms_per_launch=round(msb, 5), bytes_per_launch=int(bb),
+                                  gbs=round(bb / (msb / 1e3) / 1e9, 1),
+                                  frac_hbm=round(bb / (msb / 1e3) / 1e9 / pk["hbm"], 3),
+                                  kernel="gemv_tma_kernel" if bits == 4 else "gemv_kernel")
+        del mats_b, xb, yb
+    out["wq_gemv_m8"] = low
     # --- int4 sweep on Qwen2.5-32B layer shapes, operands rotated over >= 4x L2
     shapes = {"qkv": (7168, 5120), "o": (5120, 5120), "gate_up": (55296, 5120),
               "down": (5120, 27648)}
@@ -599,6 +626,9 @@ def main():
     if not args.quick:
         depth_sweep = []
         for dd in DEPTH_SWEEP:
+            # capture the cycle graph first: the decode time is then steady-state
+            model.cycle_info(sub.Model.decode_cfg(dd, WIDTH, DRAFT_T, mode=mode,
+                                                  target_temp=cfg.target_temp, seed=cfg.seed))
             _, sd = model.generate(prompt, ADAPTIVE_NEW, dd, WIDTH, DRAFT_T, mode=mode,
                                    target_temp=cfg.target_temp, seed=cfg.seed)
             cyc_d = max(int(sd.cycles), 1)
@@ -608,6 +638,9 @@ def main():
                                 "cycles": sd.cycles})
         adaptive = []
         for stop in ADAPTIVE_STOPS:
+            model.cycle_info(sub.Model.decode_cfg(DEPTH, WIDTH, DRAFT_T, mode=mode,
+                                                  target_temp=cfg.target_temp, seed=cfg.seed,
+                                                  stop_logp=stop))
             _, sa = model.generate(prompt, ADAPTIVE_NEW, DEPTH, WIDTH, DRAFT_T, mode=mode,
                                    target_temp=cfg.target_temp, seed=cfg.seed, stop_logp=stop)
             cyc_a = max(int(sa.cycles), 1)
@@ -651,6 +684,40 @@ def main():
         else:
             cpu["one_thread"] = one
 
+    model_bytes = model.device_bytes()
+    device_total = int(torch.cuda.memory_allocated() + model_bytes)
+    # lower and mixed-precision substitutes: the same workload rebuilt with
+    # 3-bit, 2-bit and half-and-half (first half of the substituted layers
+    # 4-bit, the rest 2-bit) substitutes; decode tokens/s, tau and the draft's
+    # share, at the fixed depth and with adaptive depth at stop_logp -6
+    lowbit = None
+    if not args.quick:
+        model.close()
+        model = None
+        torch.cuda.empty_cache()
+        n_sub = cfg.n_layers - cfg.n_resident
+        mixed = [4] * cfg.n_resident + [4 if j < n_sub // 2 else 2 for j in range(n_sub)]
+        lowbit = []
+        for tag, bits in (("3-bit", 3), ("2-bit", 2), ("4/2-bit mixed", mixed)):
+            mb = sub.Model(cfg, weights, max_seq=max_seq, max_depth=max(DEPTH_SWEEP),
+                           max_width=WIDTH, max_prompt=cfg.prompt_len,
+                           staging_layers=wl["staging"], embed_on_host=wl["embed_on_host"],
+                           bits=bits)
+            entry = {"substitutes": tag}
+            for key, stop in (("fixed", None), ("adaptive_m6", -6.0)):
+                mb.cycle_info(sub.Model.decode_cfg(DEPTH, WIDTH, DRAFT_T, mode=mode,
+                                                   target_temp=cfg.target_temp, seed=cfg.seed,
+                                                   stop_logp=stop))
+                _, sb = mb.generate(prompt, ADAPTIVE_NEW, DEPTH, WIDTH, DRAFT_T, mode=mode,
+                                    target_temp=cfg.target_temp, seed=cfg.seed, stop_logp=stop)
+                cb = max(int(sb.cycles), 1)
+                entry[key] = {"decode_tokens_per_s": (ADAPTIVE_NEW - 1) / (sb.t_decode_ms / 1e3),
+                              "tau": sb.tau, "mean_depth": sb.drafted_levels / cb,
+                              "draft_ms_per_level": sb.t_draft_ms / max(sb.drafted_levels, 1)}
+            mb.close()
+            lowbit.append(entry)
+            torch.cuda.empty_cache()
+
     timeouts = sub.pipeline_timeouts() - timeouts0
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -669,16 +736,17 @@ def main():
         "frac_of_bound": value / world / bound["tokens_per_s"] if bound["tokens_per_s"] else None,
         "host_link_gbs": round(link, 1),
         "roofline": roof, "kernels": kern, "cpu_baseline": cpu, "e2e": e2e,
-        "adaptive": adaptive, "depth_sweep": depth_sweep,
+        "adaptive": adaptive, "depth_sweep": depth_sweep, "lowbit": lowbit,
         "gpu_launches": kernels_per_cycle * args.steps, "kernels_per_cycle": kernels_per_cycle,
         "clocks": clk, "setup_s": round(t_setup, 1),
-        "model_device_bytes": model.device_bytes(),
-        "device_bytes_total": int(torch.cuda.memory_allocated() + model.device_bytes()),
+        "model_device_bytes": model_bytes,
+        "device_bytes_total": device_total,
         "pipeline_timeouts": timeouts, "valid": timeouts == 0,
     }
     if rank == 0:
         print(json.dumps(line))
-    model.close()
+    if model is not None:
+        model.close()
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

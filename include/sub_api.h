@@ -114,6 +114,34 @@ int32_t sub_bf16_gemm(const sub_bf16* X, int64_t M, const sub_bf16* W, int64_t N
                       sub_bf16* Y, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* 2-, 3- and 4-bit substitutes (lower and per-layer mixed precision for the
+ * substitute layers: "Low-Bit Shadow" report 5.1 point 2 and 10.1 (2), which
+ * leave 2/3-bit substitutes untested; Critique (10), precision per layer by
+ * sensitivity).  The same quantiser with L = 2^bits - 1 levels in place of 15:
+ * s = bf16(fp32(hi-lo)/L) (1 if that is 0), z = bf16(fp32(-lo)/s),
+ * q = clamp(rint_even(fp32(w/s) + z), 0, L), dequantised bf16((q - z) * s).
+ * q is uint8 [N, ceil(K/64) * 8 * bits]; per 64-element group:
+ *   bits 4: 32 bytes, the int4 layout above (sub_w4_* are these calls at 4);
+ *   bits 2: 16 bytes, byte j holds elements 4j..4j+3 at bits 0-1, 2-3, 4-5, 6-7;
+ *   bits 3: 24 bytes, bytes 0..15 the 2-bit layout of (q & 3), then bit i of
+ *           byte 16 + j is q(8j + i) >> 2.
+ * Codes past K are 0; scale and zero are bf16 [N, ceil(K/64)].  Arguments,
+ * alignment and errors as for the sub_w4_* calls; bits outside {2, 3, 4}
+ * returns SUB_EINVAL. */
+int32_t sub_wq_pack(const sub_bf16* W, int64_t N, int64_t K, int32_t group, int32_t bits,
+                    uint8_t* q, sub_bf16* scale, sub_bf16* zero, void* stream);
+int32_t sub_wq_dequant(const uint8_t* q, const sub_bf16* scale, const sub_bf16* zero, int64_t N,
+                       int64_t K, int32_t group, int32_t bits, sub_bf16* W_out, void* stream);
+/* Y[M, N] (bf16) = X[M, K] . deq(W)^T.  M <= 16: the warp-level GEMV with the
+ * zero point and scale folded into fp32 sums (2- and 3-bit codes are spread
+ * into the int4 word layout in registers).  Larger M at 2 or 3 bits:
+ * dequantise into stream-ordered scratch (N * K * 2 bytes, SUB_ENOMEM if it
+ * cannot be had) and run the bf16 tensor-core GEMM; at 4 bits as sub_w4_gemm. */
+int32_t sub_wq_gemm(const sub_bf16* X, int64_t M, const uint8_t* q, const sub_bf16* scale,
+                    const sub_bf16* zero, int64_t N, int64_t K, int32_t group, int32_t bits,
+                    sub_bf16* Y, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Shared paged KV cache.  The draft attends over the target's committed KV
  * ("Low-Bit Shadow" report 4.1 point 2: draft and target see the same
  * attention context; card, measured effects: shared KV-cache).
@@ -230,6 +258,9 @@ typedef struct {
   const uint8_t* q;
   const sub_bf16* scale;
   const sub_bf16* zero;
+  int32_t bits;   /* code bits: 2, 3 or 4 (0 means 4); see sub_wq_pack.  A layer's
+                     q/k/v substitutes share one width, and so do gate and up;
+                     draft forwards over more than 16 rows need 4 bits */
 } sub_w4;
 
 typedef struct {

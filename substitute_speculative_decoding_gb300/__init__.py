@@ -47,7 +47,7 @@ class Tree(C.Structure):
 
 
 class W4(C.Structure):
-    _fields_ = [("q", _vp), ("scale", _vp), ("zero", _vp)]
+    _fields_ = [("q", _vp), ("scale", _vp), ("zero", _vp), ("bits", _i32)]
 
 
 class LayerDesc(C.Structure):
@@ -97,6 +97,9 @@ _w4_pack = _decl("sub_w4_pack", [_vp, _i64, _i64, _i32, _vp, _vp, _vp, _vp])
 _w4_dequant = _decl("sub_w4_dequant", [_vp, _vp, _vp, _i64, _i64, _i32, _vp, _vp])
 _w4_gemm = _decl("sub_w4_gemm", [_vp, _i64, _vp, _vp, _vp, _i64, _i64, _i32, _vp, _vp])
 _bf16_gemm = _decl("sub_bf16_gemm", [_vp, _i64, _vp, _i64, _i64, _vp, _vp])
+_wq_pack = _decl("sub_wq_pack", [_vp, _i64, _i64, _i32, _i32, _vp, _vp, _vp, _vp])
+_wq_dequant = _decl("sub_wq_dequant", [_vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp, _vp])
+_wq_gemm = _decl("sub_wq_gemm", [_vp, _i64, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp, _vp])
 _tree_attn = _decl("sub_tree_attn", [_vp, _i32, _i32, C.POINTER(KVCache), _i32, _i64, _i64, _i32,
                                      _vp, _i32, _vp, _f32, _vp, _vp])
 _draft_expand = _decl("sub_draft_expand", [_vp, _i64, _f32, C.POINTER(Tree), _i32, _vp])
@@ -122,6 +125,7 @@ _cycle_info = _decl("sub_cycle_info", [_vp, C.POINTER(DecodeCfg), C.POINTER(_i64
 
 EXPORTED = ["sub_last_error", "sub_version", "sub_pipeline_timeouts", "sub_bounded_wait_check",
             "sub_w4_pack", "sub_w4_dequant", "sub_w4_gemm",
+            "sub_wq_pack", "sub_wq_dequant", "sub_wq_gemm",
             "sub_bf16_gemm", "sub_tree_attn", "sub_draft_expand", "sub_verify_accept",
             "sub_verify_accept_static",
             "sub_kv_compact", "sub_model_create", "sub_model_destroy", "sub_model_memory",
@@ -188,6 +192,33 @@ def w4_gemm(x, q, s, z, n: int, k: int, out=None, stream=None):
     m = x.shape[0]
     y = out if out is not None else torch.empty((m, n), dtype=torch.bfloat16, device=x.device)
     _check(_w4_gemm(_p(_bf16(x)), m, _p(q), _p(s), _p(z), n, k, 64, _p(y), _stream(stream)))
+    return y
+
+
+def wq_pack(w: torch.Tensor, bits: int, stream=None):
+    """Group-64 min-max pack with 2, 3 or 4 code bits of a bf16 [N, K] device
+    matrix -> (q uint8 [N, G * 8 * bits], scale, zero)."""
+    n, k = w.shape
+    g = (k + 63) // 64
+    q = torch.empty((n, g * 8 * bits), dtype=torch.uint8, device=w.device)
+    s = torch.empty((n, g), dtype=torch.bfloat16, device=w.device)
+    z = torch.empty((n, g), dtype=torch.bfloat16, device=w.device)
+    _check(_wq_pack(_p(_bf16(w)), n, k, 64, bits, _p(q), _p(s), _p(z), _stream(stream)))
+    return q, s, z
+
+
+def wq_dequant(q, s, z, k: int, bits: int, stream=None):
+    n = q.shape[0]
+    out = torch.empty((n, k), dtype=torch.bfloat16, device=q.device)
+    _check(_wq_dequant(_p(q), _p(s), _p(z), n, k, 64, bits, _p(out), _stream(stream)))
+    return out
+
+
+def wq_gemm(x, q, s, z, n: int, k: int, bits: int, out=None, stream=None):
+    m = x.shape[0]
+    y = out if out is not None else torch.empty((m, n), dtype=torch.bfloat16, device=x.device)
+    _check(_wq_gemm(_p(_bf16(x)), m, _p(q), _p(s), _p(z), n, k, 64, bits, _p(y),
+                    _stream(stream)))
     return y
 
 
@@ -297,7 +328,9 @@ class Model:
 
     def __init__(self, cfg, weights: dict, max_seq: int, max_depth: int, max_width: int,
                  max_prompt: int | None = None, staging_layers: int = 0, device="cuda",
-                 embed_on_host: bool = False):
+                 embed_on_host: bool = False, bits=4):
+        """bits: code bits of the substitutes (2, 3 or 4), or one entry per
+        layer (entries of resident layers are ignored) for mixed precision."""
         self.cfg = cfg
         self.keep = []          # tensors the library points into
         self.w4 = {}            # (layer, name) -> (q, scale, zero) device substitutes
@@ -320,10 +353,11 @@ class Model:
                 if i < cfg.n_resident:
                     setattr(L, name, dev_t(w).data_ptr())
                 else:
+                    b = bits[i] if isinstance(bits, (list, tuple)) else bits
                     wd = w.to(dev).contiguous()
-                    q, s, z = w4_pack(wd)
+                    q, s, z = w4_pack(wd) if b == 4 else wq_pack(wd, b)
                     self.w4[(i, name)] = (q, s, z)
-                    setattr(L, qn, W4(q.data_ptr(), s.data_ptr(), z.data_ptr()))
+                    setattr(L, qn, W4(q.data_ptr(), s.data_ptr(), z.data_ptr(), b))
                     host = w.to("cpu").contiguous().pin_memory()
                     self.keep.append(host)
                     setattr(L, name, host.data_ptr())

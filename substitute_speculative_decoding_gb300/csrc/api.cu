@@ -89,7 +89,7 @@ extern "C" int32_t sub_bounded_wait_check(uint32_t max_polls) {
 
 static int32_t matmul_public(const sub_bf16* X, int64_t M, bool w4, const void* W,
                              const sub_bf16* scale, const sub_bf16* zero, int64_t N, int64_t K,
-                             sub_bf16* Y, void* stream) {
+                             sub_bf16* Y, void* stream, int bits = 4) {
   SUB_CHECK_ARG(X && W && Y, "null pointer");
   SUB_CHECK_ARG(M >= 1 && N >= 1 && K >= 8 && K % 8 == 0, "bad sizes (K % 8 == 0 required)");
   SUB_CHECK_ARG(M < (1 << 24) && N < (1 << 30) && K < (1 << 30), "sizes too large");
@@ -107,6 +107,7 @@ static int32_t matmul_public(const sub_bf16* X, int64_t M, bool w4, const void* 
   a.N = (int)N;
   a.Y = Y;
   a.ldy = (int)N;
+  a.bits = w4 ? bits : 0;
   const cudaStream_t st = as_stream(stream);
   StreamScratch scratch(st);
   // split scratch: partial sums of K splits (register-streamed kernel) or of
@@ -133,6 +134,24 @@ extern "C" int32_t sub_w4_gemm(const sub_bf16* X, int64_t M, const uint8_t* q,
   if (group != 64) return fail(SUB_EUNSUPPORTED, "group must be 64");
   SUB_CHECK_ARG(scale && zero, "null pointer");
   return matmul_public(X, M, true, q, scale, zero, N, K, Y, stream);
+}
+
+extern "C" int32_t sub_wq_gemm(const sub_bf16* X, int64_t M, const uint8_t* q,
+                               const sub_bf16* scale, const sub_bf16* zero, int64_t N, int64_t K,
+                               int32_t group, int32_t bits, sub_bf16* Y, void* stream) {
+  if (group != 64) return fail(SUB_EUNSUPPORTED, "group must be 64");
+  SUB_CHECK_ARG(bits == 2 || bits == 3 || bits == 4, "bits must be 2, 3 or 4");
+  SUB_CHECK_ARG(X && q && scale && zero && Y, "null pointer");
+  if (M <= 16 || bits == 4) return matmul_public(X, M, true, q, scale, zero, N, K, Y, stream, bits);
+  // wider products of 2- and 3-bit codes: dequantise into scratch, then the
+  // bf16 tensor-core GEMM (the same bf16((q - z) * s) values the oracle uses)
+  SUB_CHECK_ARG(N >= 1 && K >= 8 && K % 8 == 0 && N < (1 << 30) && K < (1 << 30), "bad sizes");
+  const cudaStream_t st = as_stream(stream);
+  StreamScratch deq(st);
+  SUB_TRY(deq.alloc((size_t)N * (size_t)K * 2));
+  sub_bf16* Wd = reinterpret_cast<sub_bf16*>(deq.p);
+  SUB_TRY(sub_wq_dequant(q, scale, zero, N, K, group, bits, Wd, stream));
+  return matmul_public(X, M, false, Wd, nullptr, nullptr, N, K, Y, stream);
 }
 
 extern "C" int32_t sub_bf16_gemm(const sub_bf16* X, int64_t M, const sub_bf16* W, int64_t N,

@@ -22,8 +22,12 @@ size_t gemm_tc_scratch_floats(const GemvArgs& a, bool is_w4, int epi);
 int32_t gemm_tc_timeouts(unsigned int* out);
 
 // Dispatch on M: GEMV for M <= 16, tiled GEMM otherwise.
+// 2- and 3-bit codes have the GEMV only (the draft's tree levels, M <= 16).
 inline int32_t launch_matmul(const GemvArgs& a, bool is_w4, int epi, cudaStream_t stream) {
-  return a.M <= 16 ? launch_gemv(a, is_w4, epi, stream) : launch_gemm(a, is_w4, epi, stream);
+  if (a.M <= 16) return launch_gemv(a, is_w4, epi, stream);
+  if (is_w4 && code_bits(a) != 4)
+    return fail(SUB_EUNSUPPORTED, "2- and 3-bit weights: M must be <= 16 here");
+  return launch_gemm(a, is_w4, epi, stream);
 }
 
 }  // namespace sub

@@ -76,7 +76,43 @@ __host__ __device__ inline int split_units(int K, int ks) {
   return ((total + ks - 1) / ks + U - 1) / U * U;
 }
 
-template <bool W4, int MT, int RT, int EPI, int U>
+// Codes of 2- and 3-bit substitutes spread into the int4 word layout (code i
+// of a lane's run of 8 at bits 4i .. 4i+3), so one unpack serves all widths.
+// spread2: eight 2-bit fields at stride 2 -> stride 4 (bit interleave by
+// shift-or-mask); spread1: eight bits at stride 1 -> stride 4.
+__device__ __forceinline__ uint32_t spread2(uint32_t v) {
+  v &= 0xffffu;
+  v = (v | (v << 8)) & 0x00ff00ffu;
+  v = (v | (v << 4)) & 0x0f0f0f0fu;
+  return (v | (v << 2)) & 0x33333333u;
+}
+__device__ __forceinline__ uint32_t spread1(uint32_t v) {
+  v &= 0xffu;
+  v = (v | (v << 12)) & 0x000f000fu;
+  v = (v | (v << 6)) & 0x03030303u;
+  return (v | (v << 3)) & 0x11111111u;
+}
+
+// One lane's 16 codes of group gi (elements 16 * tig .. 16 * tig + 15 of the
+// group) as two int4-layout words; row points at the row's first group.
+template <int QB>
+__device__ __forceinline__ uint2 load_codes(const char* row, int gi, int tig) {
+  const char* grp = row + (int64_t)gi * (8 * QB);
+  if constexpr (QB == 4) {
+    return ldg_nc_v2(grp + tig * 8);
+  } else {
+    const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(grp + tig * 4));
+    uint2 r = make_uint2(spread2(w), spread2(w >> 16));
+    if constexpr (QB == 3) {
+      const uint32_t h = __ldg(reinterpret_cast<const uint16_t*>(grp + 16 + tig * 2));
+      r.x |= spread1(h) << 2;
+      r.y |= spread1(h >> 8) << 2;
+    }
+    return r;
+  }
+}
+
+template <bool W4, int MT, int RT, int EPI, int U, int QB = 4>
 __global__ void __launch_bounds__(WK * 32)
 gemv_kernel(GemvArgs a) {
   constexpr bool GLU = (EPI == EPI_GLU);
@@ -109,8 +145,8 @@ gemv_kernel(GemvArgs a) {
     const int r1 = min(tr.hi + g, nrows - 1);
     const char* base = reinterpret_cast<const char*>(a.W[tr.seg]);
     if constexpr (W4) {
-      rp0[t] = base + (int64_t)r0 * G * 32 + tig * 8;
-      rp1[t] = base + (int64_t)r1 * G * 32 + tig * 8;
+      rp0[t] = base + (int64_t)r0 * G * (8 * QB);
+      rp1[t] = base + (int64_t)r1 * G * (8 * QB);
       sp0[t] = a.S[tr.seg] + (int64_t)r0 * G;
       sp1[t] = a.S[tr.seg] + (int64_t)r1 * G;
       zp0[t] = a.Z[tr.seg] + (int64_t)r0 * G;
@@ -192,8 +228,8 @@ gemv_kernel(GemvArgs a) {
       const bool ok = gi < u_end;
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
-        q0[u][t] = ok ? ldg_nc_v2(rp0[t] + (int64_t)gi * 32) : make_uint2(0, 0);
-        q1[u][t] = ok ? ldg_nc_v2(rp1[t] + (int64_t)gi * 32) : make_uint2(0, 0);
+        q0[u][t] = ok ? load_codes<QB>(rp0[t], gi, tig) : make_uint2(0, 0);
+        q1[u][t] = ok ? load_codes<QB>(rp1[t], gi, tig) : make_uint2(0, 0);
         if (!sz_vec) {
           ss0[u][t] = ok ? __ldg(sp0[t] + gi) : 0;
           ss1[u][t] = ok ? __ldg(sp1[t] + gi) : 0;
@@ -491,7 +527,7 @@ int gemv_ksplit(const GemvArgs& a, bool is_w4, int epi) {
   return pick_ksplit(a, is_w4, gemv_grid(a, epi));
 }
 
-template <bool W4, int MT, int RT, int EPI>
+template <bool W4, int MT, int RT, int EPI, int QB>
 static int32_t launch_cfg(const GemvArgs& a_in, cudaStream_t st) {
   constexpr int U = 4;
   constexpr int NT = (EPI == EPI_GLU) ? 2 * RT : RT;
@@ -501,36 +537,45 @@ static int32_t launch_cfg(const GemvArgs& a_in, cudaStream_t st) {
   int ks = (a.split_part && a.split_cnt) ? pick_ksplit(a, W4, units) : 1;
   while (ks > 1 && ((size_t)units * ks * PER > a.split_cap || units > a.split_cnt_cap)) --ks;
   a.ksplit = ks;
-  SUB_CUDA_TRY(launch_k(gemv_kernel<W4, MT, RT, EPI, U>, dim3(units, ks), dim3(WK * 32), 0, st, a));
+  SUB_CUDA_TRY(launch_k(gemv_kernel<W4, MT, RT, EPI, U, QB>, dim3(units, ks), dim3(WK * 32), 0, st,
+                        a));
   return SUB_OK;
 }
 
-template <bool W4, int MT, int EPI>
+// 2- and 3-bit codes (QB) run one row tile per warp only.
+template <bool W4, int MT, int EPI, int QB>
 static int32_t launch_rt(const GemvArgs& a, cudaStream_t st) {
-  if constexpr (EPI == EPI_GLU || EPI == EPI_QKV) {
-    return launch_cfg<W4, MT, 1, EPI>(a, st);
+  if constexpr (EPI == EPI_GLU || EPI == EPI_QKV || QB != 4) {
+    return launch_cfg<W4, MT, 1, EPI, QB>(a, st);
   } else {
-    if (pick_rt(a, EPI) == 2) return launch_cfg<W4, MT, 2, EPI>(a, st);
-    return launch_cfg<W4, MT, 1, EPI>(a, st);
+    if (pick_rt(a, EPI) == 2) return launch_cfg<W4, MT, 2, EPI, QB>(a, st);
+    return launch_cfg<W4, MT, 1, EPI, QB>(a, st);
   }
 }
 
-template <bool W4, int EPI>
+template <bool W4, int EPI, int QB>
 static int32_t launch_mt(const GemvArgs& a, cudaStream_t st) {
-  if (a.M <= 8) return launch_rt<W4, 1, EPI>(a, st);
-  return launch_rt<W4, 2, EPI>(a, st);
+  if (a.M <= 8) return launch_rt<W4, 1, EPI, QB>(a, st);
+  return launch_rt<W4, 2, EPI, QB>(a, st);
 }
 
-template <bool W4>
+template <bool W4, int QB>
 static int32_t launch_epi(const GemvArgs& a, int epi, cudaStream_t st) {
   switch (epi) {
-    case EPI_BF16: return launch_mt<W4, EPI_BF16>(a, st);
-    case EPI_F32: return launch_mt<W4, EPI_F32>(a, st);
-    case EPI_RESID: return launch_mt<W4, EPI_RESID>(a, st);
-    case EPI_GLU: return launch_mt<W4, EPI_GLU>(a, st);
-    case EPI_QKV: return launch_mt<W4, EPI_QKV>(a, st);
+    case EPI_BF16: return launch_mt<W4, EPI_BF16, QB>(a, st);
+    case EPI_F32: return launch_mt<W4, EPI_F32, QB>(a, st);
+    case EPI_RESID: return launch_mt<W4, EPI_RESID, QB>(a, st);
+    case EPI_GLU: return launch_mt<W4, EPI_GLU, QB>(a, st);
+    case EPI_QKV: return launch_mt<W4, EPI_QKV, QB>(a, st);
   }
   return fail(SUB_EINVAL, "bad gemv epilogue");
+}
+
+static int32_t launch_bf16_or_tma(const GemvArgs& a, int epi, cudaStream_t st) {
+  bool done = false;
+  SUB_TRY(launch_gemv_tma(a, false, epi, st, &done));
+  if (done) return SUB_OK;
+  return launch_epi<false, 4>(a, epi, st);
 }
 
 int32_t launch_gemv(const GemvArgs& a, bool is_w4, int epi, cudaStream_t st) {
@@ -555,10 +600,15 @@ int32_t launch_gemv(const GemvArgs& a, bool is_w4, int epi, cudaStream_t st) {
   if (epi == EPI_RESID && a.norm.xn)
     SUB_CHECK_ARG(a.norm.partial && a.norm.gain && a.ldy == a.N && a.n_seg == 1,
                   "gemv: norm epilogue needs partial, gain, one segment and ldy == N");
+  const int bits = code_bits(a);
+  SUB_CHECK_ARG(!is_w4 || bits == 2 || bits == 3 || bits == 4, "gemv: code bits must be 2, 3 or 4");
+  if (!is_w4) return launch_bf16_or_tma(a, epi, st);
+  if (bits == 2) return launch_epi<true, 2>(a, epi, st);
+  if (bits == 3) return launch_epi<true, 3>(a, epi, st);
   bool done = false;
-  SUB_TRY(launch_gemv_tma(a, is_w4, epi, st, &done));
+  SUB_TRY(launch_gemv_tma(a, true, epi, st, &done));
   if (done) return SUB_OK;
-  return is_w4 ? launch_epi<true>(a, epi, st) : launch_epi<false>(a, epi, st);
+  return launch_epi<true, 4>(a, epi, st);
 }
 
 }  // namespace sub

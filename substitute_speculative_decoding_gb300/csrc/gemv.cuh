@@ -126,9 +126,15 @@ struct GemvArgs {
   size_t split_cap;
   int split_cnt_cap;
   int ksplit;            // set by launch_gemv
+  int bits;              // quantised weights: code bits 2, 3 or 4 (0 means 4)
 };
 
-// Launch: int4 (is_w4) or bf16 weights, epilogue, M <= 16.
+// Code bits of a quantised product (0 in GemvArgs means 4).
+inline int code_bits(const GemvArgs& a) { return a.bits ? a.bits : 4; }
+
+// Launch: quantised (is_w4; a.bits code bits) or bf16 weights, epilogue, M <= 16.
+// 2- and 3-bit codes run the register-streamed kernel; 4-bit codes and bf16
+// weights take the TMA variant when it fits.
 int32_t launch_gemv(const GemvArgs& a, bool is_w4, int epi, cudaStream_t stream);
 // Row units (CTAs along grid.x) a launch uses; NormOut::partial holds 16 floats per unit.
 int gemv_grid(const GemvArgs& a, int epi);

@@ -27,9 +27,10 @@
 namespace sub {
 
 struct Matrices {
-  const void* w[7];   // wq wk wv wo wg wu wd (bf16 or packed int4)
+  const void* w[7];   // wq wk wv wo wg wu wd (bf16 or packed codes)
   const uint16_t* s[7];
   const uint16_t* z[7];
+  int bits[7];        // code bits of the substitutes (0 for bf16)
 };
 
 // Decode state on the device (one int each).
@@ -193,6 +194,7 @@ static Matrices layer_mats(const sub_model* m, int l, bool draft) {
       r.w[i] = w4[i]->q;
       r.s[i] = w4[i]->scale;
       r.z[i] = w4[i]->zero;
+      r.bits[i] = w4[i]->bits ? w4[i]->bits : 4;
     }
   } else if (off) {
     const uint8_t* base = reinterpret_cast<const uint8_t*>(m->slots[(l - m->d.n_resident) % m->ring]);
@@ -325,6 +327,7 @@ static GemvArgs mm_args(const void* X, int M, int K, const Matrices& W, const in
   a.N = acc;
   a.Y = Y;
   a.ldy = ldy;
+  a.bits = W.bits[idx[0]];   // segments of one launch share their width (checked at create)
   return a;
 }
 
@@ -612,11 +615,22 @@ extern "C" int32_t sub_model_create(const sub_model_desc* desc, sub_model** out)
     }
     if (l >= d.n_resident) {
       const sub_w4* w4[7] = {&L.q4, &L.k4, &L.v4, &L.o4, &L.g4, &L.u4, &L.d4};
-      for (auto* w : w4)
+      for (auto* w : w4) {
         if (!(w->q && w->scale && w->zero)) {
           fail(SUB_EINVAL, "layer " + std::to_string(l) + ": null int4 substitute");
           return bail(SUB_EINVAL);
         }
+        if (!(w->bits == 0 || w->bits == 2 || w->bits == 3 || w->bits == 4)) {
+          fail(SUB_EINVAL, "layer " + std::to_string(l) + ": substitute bits must be 2, 3 or 4");
+          return bail(SUB_EINVAL);
+        }
+      }
+      auto b = [](const sub_w4& w) { return w.bits ? w.bits : 4; };
+      if (b(L.q4) != b(L.k4) || b(L.q4) != b(L.v4) || b(L.g4) != b(L.u4)) {
+        fail(SUB_EINVAL, "layer " + std::to_string(l) +
+                             ": q/k/v substitutes must share one width, and so must gate/up");
+        return bail(SUB_EINVAL);
+      }
     }
   }
   CREATE_TRY(gemm_init());
@@ -1218,10 +1232,13 @@ extern "C" int32_t sub_generate(sub_model* m, const int32_t* prompt_host, int32_
   SUB_CHECK_ARG(n_new >= 1 && (int64_t)n_prompt + n_new <= d.max_seq, "n_prompt + n_new > max_seq");
   const cudaStream_t st = m->s_main;
   SUB_CUDA_TRY(cudaStreamSynchronize(st));
+  // a new configuration's cycle graph is captured before the timed spans, so
+  // t_prefill_ms and t_decode_ms are device time only
+  SUB_TRY(check_cfg(m, c));
+  if (c.use_graph) SUB_TRY(ensure_graph(m, c));
   SUB_CUDA_TRY(cudaEventRecord(m->ev_g0, st));
   SUB_TRY(prefill_impl(m, prompt_host, n_prompt, c));
   SUB_CUDA_TRY(cudaEventRecord(m->ev_g1, st));
-  if (c.use_graph) SUB_TRY(ensure_graph(m, c));
   SUB_TRY(read_state(m));
   int emitted = m->host_state[ST_EMITTED];
   double t_draft = 0.0, t_verify = 0.0, t_unhidden = 0.0;

@@ -1,25 +1,35 @@
-// Int4 substitute construction: group-64 min-max pack and dequant.
+// Low-bit substitute construction: group-64 min-max pack and dequant for
+// 4-bit codes (the pages' substitutes) and 2- or 3-bit codes (the lower and
+// mixed precisions they leave open).
 //
-// The draft's substitute layers are data-free 4-bit copies of the offloaded
+// The draft's substitute layers are data-free low-bit copies of the offloaded
 // target layers ("SubSpec: Using the Target Model's Own Low-Bit Shadow as Its
-// Draft Model", 2.2 Step 4; "Speculate Deep and Accurate" card, Approach).
-// Quantiser (per row and 64-element group along K, all steps single IEEE fp32
-// operations, no fast-math):
-//   s = bf16((hi - lo) / 15), s = 1 if that rounds to 0;  z = bf16(-lo / s)
-//   q = clamp(rint(w / s + z), 0, 15);   deq = bf16((q - z) * s)
-// One warp owns one (row, group): lane l holds elements 2l, 2l+1 and writes
-// byte l of the group (element 2l in the low nibble).
+// Draft Model", 2.2 Step 4, 5.1 point 2, 10.1 (2); "Speculate Deep and
+// Accurate" card, Approach).  Quantiser with L = 2^bits - 1 levels (per row
+// and 64-element group along K, all steps single IEEE fp32 operations, no
+// fast-math):
+//   s = bf16((hi - lo) / L), s = 1 if that rounds to 0;  z = bf16(-lo / s)
+//   q = clamp(rint(w / s + z), 0, L);   deq = bf16((q - z) * s)
+// Code layout of a group (8 * bits bytes):
+//   4 bits: byte j = element 2j (low nibble) | element 2j+1 << 4
+//   2 bits: byte j = elements 4j .. 4j+3 at bits 0-1, 2-3, 4-5, 6-7
+//   3 bits: bytes 0..15 the 2-bit layout of (q & 3); bit i of byte 16 + j is
+//           q(8j + i) >> 2
+// One warp owns one (row, group): lane l holds elements 2l and 2l + 1.
 #include "common.cuh"
 
 namespace sub {
 
-__global__ void w4_pack_kernel(const uint16_t* __restrict__ W, int64_t N, int64_t K,
+template <int BITS>
+__global__ void wq_pack_kernel(const uint16_t* __restrict__ W, int64_t N, int64_t K,
                                uint8_t* __restrict__ q, uint16_t* __restrict__ scale,
                                uint16_t* __restrict__ zero) {
+  constexpr int GB = 8 * BITS;                 // bytes per group
+  constexpr float LEVELS = (float)((1 << BITS) - 1);
   const int64_t G = (K + 63) / 64;
   const int64_t warp = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
-  if (warp >= N * G) return;
+  if (warp >= N * G) return;   // uniform per warp
   const int64_t row = warp / G, g = warp % G;
   const int64_t k = g * 64 + 2 * lane;
   const bool valid = k < K;  // K % 8 == 0: both elements of the pair agree
@@ -36,7 +46,7 @@ __global__ void w4_pack_kernel(const uint16_t* __restrict__ W, int64_t N, int64_
     lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
     hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
   }
-  const float s32 = __fdiv_rn(__fsub_rn(hi, lo), 15.0f);
+  const float s32 = __fdiv_rn(__fsub_rn(hi, lo), LEVELS);
   uint16_t sb = f32_to_bf16_bits(s32);
   float s = bf16_bits_to_f32(sb);
   if (s == 0.0f) { s = 1.0f; sb = 0x3f80; }
@@ -44,32 +54,66 @@ __global__ void w4_pack_kernel(const uint16_t* __restrict__ W, int64_t N, int64_
   const float z = bf16_bits_to_f32(zb);
   uint32_t c0 = 0, c1 = 0;
   if (valid) {
-    c0 = (uint32_t)fminf(fmaxf(rintf(__fadd_rn(__fdiv_rn(w0, s), z)), 0.f), 15.f);
-    c1 = (uint32_t)fminf(fmaxf(rintf(__fadd_rn(__fdiv_rn(w1, s), z)), 0.f), 15.f);
+    c0 = (uint32_t)fminf(fmaxf(rintf(__fadd_rn(__fdiv_rn(w0, s), z)), 0.f), LEVELS);
+    c1 = (uint32_t)fminf(fmaxf(rintf(__fadd_rn(__fdiv_rn(w1, s), z)), 0.f), LEVELS);
   }
-  q[row * G * 32 + g * 32 + lane] = (uint8_t)(c0 | (c1 << 4));
+  uint8_t* grp = q + row * G * GB + g * GB;
+  if constexpr (BITS == 4) {
+    grp[lane] = (uint8_t)(c0 | (c1 << 4));
+  } else {
+    // low two bits: lanes 2j and 2j + 1 make byte j
+    const uint32_t pair = (c0 & 3u) | ((c1 & 3u) << 2);
+    const uint32_t next = __shfl_down_sync(0xffffffffu, pair, 1);
+    if ((lane & 1) == 0) grp[lane >> 1] = (uint8_t)(pair | (next << 4));
+    if constexpr (BITS == 3) {
+      // high bits: element e = 2l + t has its bit in ballot t at position l
+      const uint32_t m0 = __ballot_sync(0xffffffffu, (c0 >> 2) & 1u);
+      const uint32_t m1 = __ballot_sync(0xffffffffu, (c1 >> 2) & 1u);
+      if (lane < 8) {
+        uint32_t byte = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t m = (i & 1) ? m1 : m0;
+          byte |= ((m >> (4 * lane + (i >> 1))) & 1u) << i;
+        }
+        grp[16 + lane] = (uint8_t)byte;
+      }
+    }
+  }
   if (lane == 0) {
     scale[row * G + g] = sb;
     zero[row * G + g] = zb;
   }
 }
 
-__global__ void w4_dequant_kernel(const uint8_t* __restrict__ q, const uint16_t* __restrict__ scale,
+// Code of element j (0..63) of a group.
+template <int BITS>
+__device__ __forceinline__ uint32_t code_of(const uint8_t* grp, int j) {
+  if constexpr (BITS == 4) return (grp[j >> 1] >> (4 * (j & 1))) & 15u;
+  uint32_t c = (grp[j >> 2] >> (2 * (j & 3))) & 3u;
+  if constexpr (BITS == 3) c |= ((grp[16 + (j >> 3)] >> (j & 7)) & 1u) << 2;
+  return c;
+}
+
+template <int BITS>
+__global__ void wq_dequant_kernel(const uint8_t* __restrict__ q, const uint16_t* __restrict__ scale,
                                   const uint16_t* __restrict__ zero, int64_t N, int64_t K,
                                   uint16_t* __restrict__ out) {
+  constexpr int GB = 8 * BITS;
   const int64_t G = (K + 63) / 64;
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;   // one byte = 2 elements
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;   // one element pair
   if (i >= N * G * 32) return;
   const int64_t row = i / (G * 32), rem = i % (G * 32);
   const int64_t g = rem / 32;
-  const int64_t k = g * 64 + 2 * (rem % 32);
+  const int j = 2 * (int)(rem % 32);
+  const int64_t k = g * 64 + j;
   if (k >= K) return;
-  const uint8_t b = q[i];
+  const uint8_t* grp = q + row * G * GB + g * GB;
   const float s = bf16_bits_to_f32(scale[row * G + g]);
   const float z = bf16_bits_to_f32(zero[row * G + g]);
   // (q - z) and its product with s are exact in fp32; one rounding to bf16.
-  const float d0 = __fmul_rn(__fsub_rn((float)(b & 15), z), s);
-  const float d1 = __fmul_rn(__fsub_rn((float)(b >> 4), z), s);
+  const float d0 = __fmul_rn(__fsub_rn((float)code_of<BITS>(grp, j), z), s);
+  const float d1 = __fmul_rn(__fsub_rn((float)code_of<BITS>(grp, j + 1), z), s);
   *reinterpret_cast<uint32_t*>(out + row * K + k) = pack_bf16x2(d0, d1);
 }
 
@@ -84,30 +128,63 @@ int32_t w4_check(int64_t N, int64_t K, int32_t group) {
 
 using namespace sub;
 
-extern "C" int32_t sub_w4_pack(const sub_bf16* W, int64_t N, int64_t K, int32_t group,
-                               uint8_t* q, sub_bf16* scale, sub_bf16* zero, void* stream) {
+static int32_t wq_pack(const sub_bf16* W, int64_t N, int64_t K, int32_t group, int32_t bits,
+                       uint8_t* q, sub_bf16* scale, sub_bf16* zero, void* stream) {
   SUB_TRY(w4_check(N, K, group));
+  SUB_CHECK_ARG(bits == 2 || bits == 3 || bits == 4, "bits must be 2, 3 or 4");
   SUB_CHECK_ARG(W && q && scale && zero, "null pointer");
   SUB_CHECK_ARG(aligned16(W), "W must be 16-byte aligned");
   const int64_t warps = N * ((K + 63) / 64);
   const int threads = 256;
   const int64_t blocks = cdiv(warps, threads / 32);
   SUB_CHECK_ARG(blocks < (1ll << 31), "matrix too large");
-  w4_pack_kernel<<<(unsigned)blocks, threads, 0, as_stream(stream)>>>(W, N, K, q, scale, zero);
-  return check_launch("w4_pack");
+  const cudaStream_t st = as_stream(stream);
+  if (bits == 4) wq_pack_kernel<4><<<(unsigned)blocks, threads, 0, st>>>(W, N, K, q, scale, zero);
+  if (bits == 3) wq_pack_kernel<3><<<(unsigned)blocks, threads, 0, st>>>(W, N, K, q, scale, zero);
+  if (bits == 2) wq_pack_kernel<2><<<(unsigned)blocks, threads, 0, st>>>(W, N, K, q, scale, zero);
+  return check_launch("wq_pack");
+}
+
+static int32_t wq_dequant(const uint8_t* q, const sub_bf16* scale, const sub_bf16* zero,
+                          int64_t N, int64_t K, int32_t group, int32_t bits, sub_bf16* W_out,
+                          void* stream) {
+  SUB_TRY(w4_check(N, K, group));
+  SUB_CHECK_ARG(bits == 2 || bits == 3 || bits == 4, "bits must be 2, 3 or 4");
+  SUB_CHECK_ARG(W_out && q && scale && zero, "null pointer");
+  SUB_CHECK_ARG(aligned16(W_out), "W_out must be 16-byte aligned");
+  const int64_t pairs = N * ((K + 63) / 64) * 32;
+  const int threads = 256;
+  const int64_t blocks = cdiv(pairs, threads);
+  SUB_CHECK_ARG(blocks < (1ll << 31), "matrix too large");
+  const cudaStream_t st = as_stream(stream);
+  if (bits == 4)
+    wq_dequant_kernel<4><<<(unsigned)blocks, threads, 0, st>>>(q, scale, zero, N, K, W_out);
+  if (bits == 3)
+    wq_dequant_kernel<3><<<(unsigned)blocks, threads, 0, st>>>(q, scale, zero, N, K, W_out);
+  if (bits == 2)
+    wq_dequant_kernel<2><<<(unsigned)blocks, threads, 0, st>>>(q, scale, zero, N, K, W_out);
+  return check_launch("wq_dequant");
+}
+
+extern "C" int32_t sub_w4_pack(const sub_bf16* W, int64_t N, int64_t K, int32_t group,
+                               uint8_t* q, sub_bf16* scale, sub_bf16* zero, void* stream) {
+  return wq_pack(W, N, K, group, 4, q, scale, zero, stream);
 }
 
 extern "C" int32_t sub_w4_dequant(const uint8_t* q, const sub_bf16* scale, const sub_bf16* zero,
                                   int64_t N, int64_t K, int32_t group, sub_bf16* W_out,
                                   void* stream) {
-  SUB_TRY(w4_check(N, K, group));
-  SUB_CHECK_ARG(W_out && q && scale && zero, "null pointer");
-  SUB_CHECK_ARG(aligned16(W_out), "W_out must be 16-byte aligned");
-  const int64_t bytes = N * ((K + 63) / 64) * 32;
-  const int threads = 256;
-  const int64_t blocks = cdiv(bytes, threads);
-  SUB_CHECK_ARG(blocks < (1ll << 31), "matrix too large");
-  w4_dequant_kernel<<<(unsigned)blocks, threads, 0, as_stream(stream)>>>(q, scale, zero, N, K,
-                                                                          W_out);
-  return check_launch("w4_dequant");
+  return wq_dequant(q, scale, zero, N, K, group, 4, W_out, stream);
+}
+
+extern "C" int32_t sub_wq_pack(const sub_bf16* W, int64_t N, int64_t K, int32_t group,
+                               int32_t bits, uint8_t* q, sub_bf16* scale, sub_bf16* zero,
+                               void* stream) {
+  return wq_pack(W, N, K, group, bits, q, scale, zero, stream);
+}
+
+extern "C" int32_t sub_wq_dequant(const uint8_t* q, const sub_bf16* scale, const sub_bf16* zero,
+                                  int64_t N, int64_t K, int32_t group, int32_t bits,
+                                  sub_bf16* W_out, void* stream) {
+  return wq_dequant(q, scale, zero, N, K, group, bits, W_out, stream);
 }
