@@ -189,3 +189,107 @@ def wq_dequant(q, s, z, k: int, bits: int) -> np.ndarray:
 def wq_gemm(x, q, s, z, k: int, bits: int) -> np.ndarray:
     """Y[M, N] = X[M, K] . deq(W)^T, accumulated in float64, rounded to fp32."""
     return mm(x, wq_dequant(q, s, z, k, bits))
+
+
+# ---------------------------------------------------------------------------
+# HQQ zero-point optimisation (the pages build their substitutes with HQQ,
+# "Low-Bit Shadow" report Critique 3 and 6.2, and give none of its steps).
+# Restated here from the published half-quadratic method: keep the min-max
+# scale s and, per group, alternate
+#   q  = clamp(rint(w / s + z), 0, L)            codes for the current zero
+#   r  = w - s (q - z)                            the residual
+#   e  = sign(r) max(|r| - |r|^(p-1) / beta, 0)   the l_p shrinkage of r
+#   z  = mean(q - (w - e) / s)                    the zero minimising
+#                                                 sum (w - e - s (q - z))^2
+#   beta = beta * kappa
+# for a fixed number of iterations, keeping the zero with the smallest
+# sum |r| seen (the first one, the min-max zero, included; ties keep the
+# earlier).  Parameters: p = 1/2 (HQQ's default is 0.7; at 1/2,
+# |r|^(p-1) = 1 / sqrt|r| is two correctly rounded fp32 operations),
+# beta = 10, kappa = 1.01, 20 iterations (HQQ's defaults).  The kept zero is
+# rounded to bf16 and the codes are formed with it, as in the min-max rule.
+# All arithmetic is fp32, each operation rounded; the sums over a group run
+# in one fixed pairwise order (pair_sum64), and the mean divides by the
+# group's element count.
+# ---------------------------------------------------------------------------
+HQQ_ITERS, HQQ_BETA, HQQ_KAPPA, HQQ_P = 20, 10.0, 1.01, 0.5
+
+
+def pair_sum64(x) -> np.ndarray:
+    """Sum over the last axis (64 entries) in a fixed order: a_l = x[2l] +
+    x[2l+1], then five rounds of a_l = a_l + a_(l xor o), o = 16, 8, 4, 2, 1;
+    the result is a_0.  fp32, every addition rounded."""
+    x = np.asarray(x, np.float32)
+    a = x[..., 0::2] + x[..., 1::2]
+    idx = np.arange(32)
+    for o in (16, 8, 4, 2, 1):
+        a = a + a[..., idx ^ o]
+    return a[..., 0]
+
+
+def shrink_lp(r, beta, p=HQQ_P) -> np.ndarray:
+    """sign(r) max(|r| - |r|^(p-1) / beta, 0) in fp32; 0 where r == 0."""
+    r = np.asarray(r, np.float32)
+    ar = np.abs(r)
+    safe = np.where(ar > 0, ar, np.float32(1))
+    if p == 0.5:
+        pw = np.float32(1) / np.sqrt(safe)
+    else:
+        pw = np.power(safe, np.float32(p - 1)).astype(np.float32)
+    th = np.where(ar > 0, pw / np.float32(beta), np.float32(0)).astype(np.float32)
+    return (np.sign(r) * np.maximum(ar - th, np.float32(0))).astype(np.float32)
+
+
+def hqq_codes(w, bits: int, iters=HQQ_ITERS, beta0=HQQ_BETA, kappa=HQQ_KAPPA, p=HQQ_P) -> tuple:
+    """w: float32 [N, K] of bf16 values -> (codes uint8 [N, K], s, z) with the
+    min-max scale and the HQQ-optimised zero (see above)."""
+    assert bits in BITS and iters >= 1
+    w = np.asarray(w, dtype=np.float32)
+    n, k = w.shape
+    g_count = n_groups(k)
+    levels = np.float32(2 ** bits - 1)
+    codes = np.zeros((n, k), dtype=np.uint8)
+    s_all = np.zeros((n, g_count), dtype=np.float32)
+    z_all = np.zeros((n, g_count), dtype=np.float32)
+    for g in range(g_count):
+        c0, c1 = g * GROUP, min(k, (g + 1) * GROUP)
+        cnt = c1 - c0
+        blk = np.zeros((n, GROUP), np.float32)
+        blk[:, :cnt] = w[:, c0:c1]
+        valid = np.zeros(GROUP, bool)
+        valid[:cnt] = True
+        lo = blk[:, :cnt].min(axis=1)
+        hi = blk[:, :cnt].max(axis=1)
+        s = round_bf16((hi - lo) / levels)
+        s = np.where(s == 0, np.float32(1.0), s).astype(np.float32)
+        z = ((-lo) / s).astype(np.float32)
+        beta = np.float32(beta0)
+        best_z, best_err = z.copy(), None
+        for _ in range(iters):
+            q = np.clip(np.rint((blk / s[:, None]) + z[:, None]), 0, levels).astype(np.float32)
+            r = (blk - s[:, None] * (q - z[:, None])).astype(np.float32)
+            r = np.where(valid, r, np.float32(0))
+            err = pair_sum64(np.abs(r))
+            if best_err is None:
+                best_err = err
+            else:
+                better = err < best_err
+                best_err = np.where(better, err, best_err)
+                best_z = np.where(better, z, best_z)
+            e = shrink_lp(r, beta, p)
+            t = np.where(valid, q - (blk - e) / s[:, None], np.float32(0)).astype(np.float32)
+            z = (pair_sum64(t) / np.float32(cnt)).astype(np.float32)
+            beta = np.float32(beta * np.float32(kappa))
+        zb = round_bf16(best_z)
+        t = (blk[:, :cnt] / s[:, None]) + zb[:, None]
+        codes[:, c0:c1] = np.clip(np.rint(t), 0, levels).astype(np.uint8)
+        s_all[:, g] = s
+        z_all[:, g] = zb
+    return codes, s_all, z_all
+
+
+def wq_pack_hqq(w, bits: int, iters=HQQ_ITERS) -> tuple:
+    """HQQ-zero substitutes in the wq layouts: (q, s, z); dequantise with
+    wq_dequant like any other."""
+    codes, s, z = hqq_codes(w, bits, iters)
+    return wq_pack_codes(codes, bits), s, z
