@@ -343,6 +343,14 @@ def kernel_measurements(sub, cfg, weights, model, pk, dev, quick):
                                   kernel="gemv_tma_kernel" if bits == 4 else "gemv_kernel")
         del mats_b, xb, yb
     out["wq_gemv_m8"] = low
+    # --- substitute construction: min-max and HQQ (20 iterations) packing of
+    # one gate matrix, 4 bits
+    wg = (torch.randn(f, h, device=dev) * 0.02).to(torch.bfloat16)
+    ms_mm = time_launches(lambda i: sub.wq_pack(wg, 4), 4, st)
+    ms_hq = time_launches(lambda i: sub.wq_pack_hqq(wg, 4, 20), 4, st)
+    out["pack_gate_4bit"] = dict(shape=[f, h], minmax_ms=round(ms_mm, 4), hqq20_ms=round(ms_hq, 4),
+                                 hqq20_gweights_per_s=round(f * h / (ms_hq / 1e3) / 1e9, 2))
+    del wg
     # --- int4 sweep on Qwen2.5-32B layer shapes, operands rotated over >= 4x L2
     shapes = {"qkv": (7168, 5120), "o": (5120, 5120), "gate_up": (55296, 5120),
               "down": (5120, 27648)}
@@ -635,7 +643,7 @@ def main():
             depth_sweep.append({"depth": dd,
                                 "decode_tokens_per_s": (ADAPTIVE_NEW - 1) / (sd.t_decode_ms / 1e3),
                                 "tau": sd.tau, "cycle_ms": sd.t_decode_ms / cyc_d,
-                                "cycles": sd.cycles})
+                                "cycles": sd.cycles, **phase_ms(sd)})
         adaptive = []
         for stop in ADAPTIVE_STOPS:
             model.cycle_info(sub.Model.decode_cfg(DEPTH, WIDTH, DRAFT_T, mode=mode,
@@ -647,7 +655,8 @@ def main():
             adaptive.append({"stop_logp": stop,
                              "decode_tokens_per_s": (ADAPTIVE_NEW - 1) / (sa.t_decode_ms / 1e3),
                              "tau": sa.tau, "mean_depth": sa.drafted_levels / cyc_a,
-                             "cycle_ms": sa.t_decode_ms / cyc_a, "cycles": sa.cycles})
+                             "cycle_ms": sa.t_decode_ms / cyc_a, "cycles": sa.cycles,
+                             **phase_ms(sa)})
 
     g = kern["w4_gemv_m8"]
     traffic = profile_traffic("gemv_w4")
@@ -657,6 +666,43 @@ def main():
             "traffic": traffic, "peak_source": pk["src"] + " (burst copy)",
             "bytes_per_launch": int(g["bytes_per_launch"])}
 
+    model_bytes = model.device_bytes()
+    device_total = int(torch.cuda.memory_allocated() + model_bytes)
+    # lower and mixed-precision substitutes: the same workload rebuilt with
+    # 3-bit, 2-bit and half-and-half (first half of the substituted layers
+    # 4-bit, the rest 2-bit) substitutes; decode tokens/s, tau and the draft's
+    # share, at the fixed depth and with adaptive depth at stop_logp -6
+    lowbit = None
+    if not args.quick:
+        model.close()
+        model = None
+        torch.cuda.empty_cache()
+        n_sub = cfg.n_layers - cfg.n_resident
+        mixed = [4] * cfg.n_resident + [4 if j < n_sub // 2 else 2 for j in range(n_sub)]
+        lowbit = []
+        for tag, bits, hq in (("4-bit HQQ zeros", 4, 20), ("3-bit", 3, 0), ("2-bit", 2, 0),
+                              ("4/2-bit mixed", mixed, 0)):
+            mb = sub.Model(cfg, weights, max_seq=max_seq, max_depth=max(DEPTH_SWEEP),
+                           max_width=WIDTH, max_prompt=cfg.prompt_len,
+                           staging_layers=wl["staging"], embed_on_host=wl["embed_on_host"],
+                           bits=bits, hqq_iters=hq)
+            entry = {"substitutes": tag}
+            for key, stop in (("fixed", None), ("adaptive_m6", -6.0)):
+                mb.cycle_info(sub.Model.decode_cfg(DEPTH, WIDTH, DRAFT_T, mode=mode,
+                                                   target_temp=cfg.target_temp, seed=cfg.seed,
+                                                   stop_logp=stop))
+                _, sb = mb.generate(prompt, ADAPTIVE_NEW, DEPTH, WIDTH, DRAFT_T, mode=mode,
+                                    target_temp=cfg.target_temp, seed=cfg.seed, stop_logp=stop)
+                cb = max(int(sb.cycles), 1)
+                entry[key] = {"decode_tokens_per_s": (ADAPTIVE_NEW - 1) / (sb.t_decode_ms / 1e3),
+                              "tau": sb.tau, "mean_depth": sb.drafted_levels / cb,
+                              "draft_ms_per_level": sb.t_draft_ms / max(sb.drafted_levels, 1),
+                              **phase_ms(sb)}
+            mb.close()
+            lowbit.append(entry)
+            torch.cuda.empty_cache()
+
+    # the oracle baseline last: its host memory and threads touch no GPU measurement
     cpu = None
     if rank == 0 and world == 1 and not args.quick:
         # one full token through every layer and the head on all host cores,
@@ -683,40 +729,6 @@ def main():
                                            f"layers scaled to {cfg.n_layers}"}
         else:
             cpu["one_thread"] = one
-
-    model_bytes = model.device_bytes()
-    device_total = int(torch.cuda.memory_allocated() + model_bytes)
-    # lower and mixed-precision substitutes: the same workload rebuilt with
-    # 3-bit, 2-bit and half-and-half (first half of the substituted layers
-    # 4-bit, the rest 2-bit) substitutes; decode tokens/s, tau and the draft's
-    # share, at the fixed depth and with adaptive depth at stop_logp -6
-    lowbit = None
-    if not args.quick:
-        model.close()
-        model = None
-        torch.cuda.empty_cache()
-        n_sub = cfg.n_layers - cfg.n_resident
-        mixed = [4] * cfg.n_resident + [4 if j < n_sub // 2 else 2 for j in range(n_sub)]
-        lowbit = []
-        for tag, bits in (("3-bit", 3), ("2-bit", 2), ("4/2-bit mixed", mixed)):
-            mb = sub.Model(cfg, weights, max_seq=max_seq, max_depth=max(DEPTH_SWEEP),
-                           max_width=WIDTH, max_prompt=cfg.prompt_len,
-                           staging_layers=wl["staging"], embed_on_host=wl["embed_on_host"],
-                           bits=bits)
-            entry = {"substitutes": tag}
-            for key, stop in (("fixed", None), ("adaptive_m6", -6.0)):
-                mb.cycle_info(sub.Model.decode_cfg(DEPTH, WIDTH, DRAFT_T, mode=mode,
-                                                   target_temp=cfg.target_temp, seed=cfg.seed,
-                                                   stop_logp=stop))
-                _, sb = mb.generate(prompt, ADAPTIVE_NEW, DEPTH, WIDTH, DRAFT_T, mode=mode,
-                                    target_temp=cfg.target_temp, seed=cfg.seed, stop_logp=stop)
-                cb = max(int(sb.cycles), 1)
-                entry[key] = {"decode_tokens_per_s": (ADAPTIVE_NEW - 1) / (sb.t_decode_ms / 1e3),
-                              "tau": sb.tau, "mean_depth": sb.drafted_levels / cb,
-                              "draft_ms_per_level": sb.t_draft_ms / max(sb.drafted_levels, 1)}
-            mb.close()
-            lowbit.append(entry)
-            torch.cuda.empty_cache()
 
     timeouts = sub.pipeline_timeouts() - timeouts0
     line = {
@@ -752,6 +764,14 @@ def main():
         dist.destroy_process_group()
     if timeouts:
         raise SystemExit(f"{timeouts} bounded pipeline wait(s) ran out: the numbers are invalid")
+
+
+def phase_ms(st):
+    """Per-cycle device time of a generate call's phases (sub_stats)."""
+    c = max(int(st.cycles), 1)
+    return {"per_cycle_ms": {"draft": round(st.t_draft_ms / c, 3),
+                             "verify": round(st.t_verify_ms / c, 3),
+                             "copy_unhidden": round(st.t_copy_unhidden_ms / c, 3)}}
 
 
 def profile_traffic(kernel):

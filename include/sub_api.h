@@ -132,6 +132,23 @@ int32_t sub_wq_pack(const sub_bf16* W, int64_t N, int64_t K, int32_t group, int3
                     uint8_t* q, sub_bf16* scale, sub_bf16* zero, void* stream);
 int32_t sub_wq_dequant(const uint8_t* q, const sub_bf16* scale, const sub_bf16* zero, int64_t N,
                        int64_t K, int32_t group, int32_t bits, sub_bf16* W_out, void* stream);
+/* sub_wq_pack with the zero point optimised by HQQ (the pages' quantiser:
+ * "Low-Bit Shadow" report Critique 3 and 6.2; their steps are not given
+ * there, these follow the published half-quadratic method).  The min-max
+ * scale is kept; per group, starting from the min-max zero z (unrounded),
+ * `iters` steps of
+ *   q = clamp(rint(w/s + z), 0, L),  r = w - s (q - z),
+ *   e = sign(r) max(|r| - |r|^(-1/2) / beta, 0),  z = mean(q - (w - e)/s),
+ *   beta = beta * 1.01   (beta starts at 10)
+ * keep the zero with the smallest sum |r| (ties: the earlier); it is rounded
+ * to bf16 and the codes are formed with it.  Every step is one IEEE fp32
+ * operation and the group sums run in one fixed pairwise order, so the
+ * result is reproducible bit for bit.  The output is in the sub_wq layouts
+ * and dequantises with the same rule.  iters in [1, 1000]; iters = 1 gives
+ * the min-max quantiser. */
+int32_t sub_wq_pack_hqq(const sub_bf16* W, int64_t N, int64_t K, int32_t group, int32_t bits,
+                        int32_t iters, uint8_t* q, sub_bf16* scale, sub_bf16* zero,
+                        void* stream);
 /* Y[M, N] (bf16) = X[M, K] . deq(W)^T.  M <= 16: the warp-level GEMV with the
  * zero point and scale folded into fp32 sums (2- and 3-bit codes are spread
  * into the int4 word layout in registers).  Larger M at 2 or 3 bits:

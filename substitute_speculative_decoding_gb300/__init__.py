@@ -99,6 +99,7 @@ _w4_gemm = _decl("sub_w4_gemm", [_vp, _i64, _vp, _vp, _vp, _i64, _i64, _i32, _vp
 _bf16_gemm = _decl("sub_bf16_gemm", [_vp, _i64, _vp, _i64, _i64, _vp, _vp])
 _wq_pack = _decl("sub_wq_pack", [_vp, _i64, _i64, _i32, _i32, _vp, _vp, _vp, _vp])
 _wq_dequant = _decl("sub_wq_dequant", [_vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp, _vp])
+_wq_pack_hqq = _decl("sub_wq_pack_hqq", [_vp, _i64, _i64, _i32, _i32, _i32, _vp, _vp, _vp, _vp])
 _wq_gemm = _decl("sub_wq_gemm", [_vp, _i64, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp, _vp])
 _tree_attn = _decl("sub_tree_attn", [_vp, _i32, _i32, C.POINTER(KVCache), _i32, _i64, _i64, _i32,
                                      _vp, _i32, _vp, _f32, _vp, _vp])
@@ -125,7 +126,7 @@ _cycle_info = _decl("sub_cycle_info", [_vp, C.POINTER(DecodeCfg), C.POINTER(_i64
 
 EXPORTED = ["sub_last_error", "sub_version", "sub_pipeline_timeouts", "sub_bounded_wait_check",
             "sub_w4_pack", "sub_w4_dequant", "sub_w4_gemm",
-            "sub_wq_pack", "sub_wq_dequant", "sub_wq_gemm",
+            "sub_wq_pack", "sub_wq_dequant", "sub_wq_gemm", "sub_wq_pack_hqq",
             "sub_bf16_gemm", "sub_tree_attn", "sub_draft_expand", "sub_verify_accept",
             "sub_verify_accept_static",
             "sub_kv_compact", "sub_model_create", "sub_model_destroy", "sub_model_memory",
@@ -204,6 +205,18 @@ def wq_pack(w: torch.Tensor, bits: int, stream=None):
     s = torch.empty((n, g), dtype=torch.bfloat16, device=w.device)
     z = torch.empty((n, g), dtype=torch.bfloat16, device=w.device)
     _check(_wq_pack(_p(_bf16(w)), n, k, 64, bits, _p(q), _p(s), _p(z), _stream(stream)))
+    return q, s, z
+
+
+def wq_pack_hqq(w: torch.Tensor, bits: int, iters: int = 20, stream=None):
+    """wq_pack with the HQQ-optimised zero point -> (q, scale, zero)."""
+    n, k = w.shape
+    g = (k + 63) // 64
+    q = torch.empty((n, g * 8 * bits), dtype=torch.uint8, device=w.device)
+    s = torch.empty((n, g), dtype=torch.bfloat16, device=w.device)
+    z = torch.empty((n, g), dtype=torch.bfloat16, device=w.device)
+    _check(_wq_pack_hqq(_p(_bf16(w)), n, k, 64, bits, iters, _p(q), _p(s), _p(z),
+                        _stream(stream)))
     return q, s, z
 
 
@@ -328,9 +341,10 @@ class Model:
 
     def __init__(self, cfg, weights: dict, max_seq: int, max_depth: int, max_width: int,
                  max_prompt: int | None = None, staging_layers: int = 0, device="cuda",
-                 embed_on_host: bool = False, bits=4):
+                 embed_on_host: bool = False, bits=4, hqq_iters: int = 0):
         """bits: code bits of the substitutes (2, 3 or 4), or one entry per
-        layer (entries of resident layers are ignored) for mixed precision."""
+        layer (entries of resident layers are ignored) for mixed precision.
+        hqq_iters > 0 packs them with the HQQ-optimised zero point."""
         self.cfg = cfg
         self.keep = []          # tensors the library points into
         self.w4 = {}            # (layer, name) -> (q, scale, zero) device substitutes
@@ -355,7 +369,10 @@ class Model:
                 else:
                     b = bits[i] if isinstance(bits, (list, tuple)) else bits
                     wd = w.to(dev).contiguous()
-                    q, s, z = w4_pack(wd) if b == 4 else wq_pack(wd, b)
+                    if hqq_iters > 0:
+                        q, s, z = wq_pack_hqq(wd, b, hqq_iters)
+                    else:
+                        q, s, z = w4_pack(wd) if b == 4 else wq_pack(wd, b)
                     self.w4[(i, name)] = (q, s, z)
                     setattr(L, qn, W4(q.data_ptr(), s.data_ptr(), z.data_ptr(), b))
                     host = w.to("cpu").contiguous().pin_memory()
@@ -389,9 +406,13 @@ class Model:
         self.handle = h
 
     def close(self):
+        """Destroy the model and drop the tensors it pointed into (the pinned
+        originals and the device substitutes)."""
         if getattr(self, "handle", None) and self.handle.value:
             _model_destroy(self.handle)
             self.handle = _vp()
+        self.keep = []
+        self.w4 = {}
 
     def __del__(self):
         try:

@@ -16,10 +16,11 @@ def oracle_model(model: dict):
     return glob, layers
 
 
-def oracle_draft_layers(cfg, layers, bits=4):
+def oracle_draft_layers(cfg, layers, bits=4, hqq_iters=0):
     """Draft weights: resident layers shared, the rest replaced by the
     dequantised substitutes (oracle quantiser); bits: 2, 3 or 4 for every
-    substitute, or a list with one entry per layer (mixed precision)."""
+    substitute, or a list with one entry per layer (mixed precision);
+    hqq_iters > 0: HQQ-optimised zero points."""
     out = []
     for i, lw in enumerate(layers):
         if i < cfg.n_resident:
@@ -29,7 +30,10 @@ def oracle_draft_layers(cfg, layers, bits=4):
         d = dict(lw)
         for name in synthetic.LAYER_TENSORS:
             w = lw[name]
-            if b == 4:
+            if hqq_iters > 0:
+                q, s, z = quant.wq_pack_hqq(w, b, hqq_iters)
+                d[name] = quant.wq_dequant(q, s, z, w.shape[1], b)
+            elif b == 4:
                 q, s, z = quant.w4_pack(w)
                 d[name] = quant.w4_dequant(q, s, z, w.shape[1])
             else:

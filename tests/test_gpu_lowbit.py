@@ -1,9 +1,9 @@
 """2- and 3-bit and per-layer mixed-precision substitutes on the device
-("Low-Bit Shadow" report 5.1 point 2, 10.1 (2); Critique (10)) against the
-oracle: packed codes, scales, zeros and dequantised values bit-exact; the
-GEMV and the wide product within the bf16 output rounding; draft logits of
-mixed-precision models within the stated tolerance; and decoding that stays
-lossless with any substitute width."""
+("Low-Bit Shadow" report 5.1 point 2, 10.1 (2); Critique (10)), and HQQ zero
+points (Critique 3, 6.2), against the oracle: packed codes, scales, zeros
+and dequantised values bit-exact; the GEMV and the wide product within the
+bf16 output rounding; draft logits of mixed-precision and HQQ models within
+the stated tolerance; and decoding that stays lossless with any of them."""
 import numpy as np
 import pytest
 import torch
@@ -80,6 +80,21 @@ def test_wq_gemm_identity_is_exact_dequant(sub, bits):
     assert torch.equal(y.t().contiguous(), deq)
 
 
+@pytest.mark.parametrize("bits", [2, 3, 4])
+@pytest.mark.parametrize("iters", [1, 20])
+@pytest.mark.parametrize("n,k", [(48, 688), (64, 3584), (40, 200)])
+def test_hqq_pack_bit_exact(sub, bits, iters, n, k):
+    """HQQ zero optimisation: codes, scales and zeros equal the oracle's bit
+    for bit (fp32 steps and one summation order on both sides)."""
+    w = synthetic.randn_bf16((n, k), n + k + bits, std=0.02)
+    w[3, :64] = 0.25                       # a constant group
+    q, s, z = sub.wq_pack_hqq(w.to(DEV), bits, iters)
+    rq, rs, rz = quant.wq_pack_hqq(np32(w), bits, iters)
+    assert np.array_equal(np32(s), rs)
+    assert np.array_equal(np32(z), rz)
+    assert np.array_equal(q.cpu().numpy(), rq)
+
+
 def test_bad_bits_rejected(sub):
     w = torch.zeros((16, 64), dtype=torch.bfloat16, device=DEV)
     with pytest.raises(sub.SubError):
@@ -94,20 +109,22 @@ TMA4 = synthetic.DecoderConfig("tma4", n_layers=4, hidden=512, n_heads_q=8, n_he
                                n_resident=1, prompt_len=32, n_new=48, depth=6, width=3)
 TINY = synthetic.CONFIGS["tiny"]
 CASES = {
-    "tiny-2bit": (TINY, 2),
-    "tiny-3bit": (TINY, 3),
-    "tma4-mixed": (TMA4, [4, 4, 2, 3]),   # layer 0 resident; substitutes 4, 2, 3 bits
+    "tiny-2bit": (TINY, 2, 0),
+    "tiny-3bit": (TINY, 3, 0),
+    "tma4-mixed": (TMA4, [4, 4, 2, 3], 0),   # layer 0 resident; substitutes 4, 2, 3 bits
+    "tma4-hqq": (TMA4, 4, 20),               # 4-bit substitutes with HQQ zero points
 }
 
 
 @pytest.fixture(scope="module", params=sorted(CASES))
 def lowbit(sub, request):
-    cfg, bits = CASES[request.param]
+    cfg, bits, hqq = CASES[request.param]
     w = synthetic.make_model(cfg, norm_gain_std=0.1)
     glob, layers = oracle_model(w)
-    draft = oracle_draft_layers(cfg, layers, bits)
+    draft = oracle_draft_layers(cfg, layers, bits, hqq_iters=hqq)
     prompt = synthetic.make_prompt(cfg)
-    model = sub.Model(cfg, w, max_seq=256, max_depth=8, max_width=3, max_prompt=64, bits=bits)
+    model = sub.Model(cfg, w, max_seq=256, max_depth=8, max_width=3, max_prompt=64, bits=bits,
+                      hqq_iters=hqq)
     yield dict(cfg=cfg, glob=glob, layers=layers, draft=draft, prompt=prompt, model=model)
     model.close()
 
@@ -150,8 +167,18 @@ def test_generate_is_lossless(lowbit, mode, temp):
 
 def test_wide_draft_needs_four_bits(sub, lowbit):
     """A draft forward over more than 16 rows with 2- or 3-bit substitutes is
-    refused (those widths have the GEMV only on the model path)."""
+    refused (those widths have the GEMV only on the model path); with 4-bit
+    HQQ substitutes it runs the tensor-core GEMM and matches the oracle."""
     p = lowbit["prompt"].to(DEV)
+    if lowbit["model"].w4 and all(q.shape[1] * 2 == 64 * s.shape[1]
+                                  for q, s, _ in lowbit["model"].w4.values()):
+        lg = torch.empty((len(p), lowbit["cfg"].vocab), dtype=torch.float32, device=DEV)
+        lowbit["model"].forward(1, p, 0, 0, logits=lg)
+        torch.cuda.synchronize()
+        ref, _, _ = prefill(lowbit["cfg"], lowbit["glob"], lowbit["draft"],
+                            lowbit["prompt"].numpy())
+        close(lg.cpu().numpy(), ref)
+        return
     lg = torch.empty((len(p), lowbit["cfg"].vocab), dtype=torch.float32, device=DEV)
     with pytest.raises(sub.SubError):
         lowbit["model"].forward(1, p, 0, 0, logits=lg)
