@@ -597,10 +597,6 @@ def main():
     tokens_all = reduce(world, tokens, "sum")
     value = tokens_all / (ms_max / 1e3)
 
-    link = measure_link(dev)
-    bound = cycle_bound(cfg, pk, tau, cfg.prompt_len + tokens, link, wl["staging"])
-    kern = kernel_measurements(sub, cfg, weights, model, pk, dev, args.quick)
-
     # e2e: the public call with host buffers, prefill included
     e2e = None
     if not args.quick:
@@ -657,6 +653,29 @@ def main():
                              "tau": sa.tau, "mean_depth": sa.drafted_levels / cyc_a,
                              "cycle_ms": sa.t_decode_ms / cyc_a, "cycles": sa.cycles,
                              **phase_ms(sa)})
+
+    # verify reuse of the draft's leading (resident) layers, fixed depth and
+    # adaptive depth at stop_logp -6
+    reuse = None
+    if not args.quick:
+        reuse = []
+        for stop in (None, -6.0):
+            model.cycle_info(sub.Model.decode_cfg(DEPTH, WIDTH, DRAFT_T, mode=mode,
+                                                  target_temp=cfg.target_temp, seed=cfg.seed,
+                                                  stop_logp=stop, verify_reuse=True))
+            _, sr = model.generate(prompt, ADAPTIVE_NEW, DEPTH, WIDTH, DRAFT_T, mode=mode,
+                                   target_temp=cfg.target_temp, seed=cfg.seed, stop_logp=stop,
+                                   verify_reuse=True)
+            cr = max(int(sr.cycles), 1)
+            reuse.append({"stop_logp": stop,
+                          "decode_tokens_per_s": (ADAPTIVE_NEW - 1) / (sr.t_decode_ms / 1e3),
+                          "tau": sr.tau, "mean_depth": sr.drafted_levels / cr,
+                          "cycle_ms": sr.t_decode_ms / cr, **phase_ms(sr)})
+
+    # host link and kernel measurements come after this model's decode runs
+    link = measure_link(dev)
+    bound = cycle_bound(cfg, pk, tau, cfg.prompt_len + tokens, link, wl["staging"])
+    kern = kernel_measurements(sub, cfg, weights, model, pk, dev, args.quick)
 
     g = kern["w4_gemv_m8"]
     traffic = profile_traffic("gemv_w4")
@@ -748,7 +767,7 @@ def main():
         "frac_of_bound": value / world / bound["tokens_per_s"] if bound["tokens_per_s"] else None,
         "host_link_gbs": round(link, 1),
         "roofline": roof, "kernels": kern, "cpu_baseline": cpu, "e2e": e2e,
-        "adaptive": adaptive, "depth_sweep": depth_sweep, "lowbit": lowbit,
+        "adaptive": adaptive, "depth_sweep": depth_sweep, "lowbit": lowbit, "verify_reuse": reuse,
         "gpu_launches": kernels_per_cycle * args.steps, "kernels_per_cycle": kernels_per_cycle,
         "clocks": clk, "setup_s": round(t_setup, 1),
         "model_device_bytes": model_bytes,

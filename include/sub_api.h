@@ -346,6 +346,16 @@ typedef struct {
    * a level not drafted launches nothing; without use_graph the host reads
    * the decision after every level (one synchronisation per level). */
   float stop_logp;
+  /* Verify reuse of the draft's leading layers (layer and KV sharing, "Low-Bit
+   * Shadow" report 4.1 point 2): layers [0, n_resident) are the target's own,
+   * so the draft's residual stream after them is the target's for the same
+   * node.  Nonzero: every tree node's leading part runs once, in the draft
+   * (the deepest level's nodes get it right after their expansion), and the
+   * verify starts at layer n_resident from it; the K/V of those layers are
+   * the draft's.  The draft's kernels (M <= 16 GEMV) and the verify's (tiled
+   * GEMM) round differently, so the verify logits move by that rounding
+   * noise; the emitted tokens stay the target's up to near-ties. */
+  int32_t verify_reuse;
 } sub_decode_cfg;
 
 typedef struct {

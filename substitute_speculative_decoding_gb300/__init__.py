@@ -68,7 +68,7 @@ class ModelDesc(C.Structure):
 class DecodeCfg(C.Structure):
     _fields_ = [("depth", _i32), ("width", _i32), ("draft_temp", _f32), ("mode", _i32),
                 ("target_temp", _f32), ("seed", _u64), ("use_graph", _i32),
-                ("stop_logp", _f32)]
+                ("stop_logp", _f32), ("verify_reuse", _i32)]
 
 
 class Stats(C.Structure):
@@ -440,10 +440,11 @@ class Model:
 
     @staticmethod
     def decode_cfg(depth, width, draft_temp=0.2, mode=0, target_temp=1.0, seed=0,
-                   use_graph=True, stop_logp=None) -> DecodeCfg:
-        """stop_logp: None (every level drafted) or a negative threshold for adaptive depth."""
+                   use_graph=True, stop_logp=None, verify_reuse=False) -> DecodeCfg:
+        """stop_logp: None (every level drafted) or a negative threshold for adaptive
+        depth; verify_reuse: the verify starts from the draft's leading layers."""
         return DecodeCfg(depth, width, draft_temp, mode, target_temp, seed, int(use_graph),
-                         0.0 if stop_logp is None else float(stop_logp))
+                         0.0 if stop_logp is None else float(stop_logp), int(verify_reuse))
 
     def prefill(self, prompt, cfg: DecodeCfg, stream=None):
         self._prompt = prompt.to(torch.int32).contiguous()
@@ -466,12 +467,12 @@ class Model:
         return k.value, b.value
 
     def generate(self, prompt, n_new: int, depth: int, width: int, draft_temp=0.2, mode=0,
-                 target_temp=1.0, seed=0, use_graph=True, stop_logp=None):
+                 target_temp=1.0, seed=0, use_graph=True, stop_logp=None, verify_reuse=False):
         """prompt: int32 CPU tensor -> (int32 CPU tensor [n_new], Stats)."""
         p = prompt.to(torch.int32).contiguous()
         out = torch.zeros(n_new, dtype=torch.int32)
         cfg = self.decode_cfg(depth, width, draft_temp, mode, target_temp, seed, use_graph,
-                              stop_logp)
+                              stop_logp, verify_reuse)
         st = Stats()
         _check(_generate(self.handle, C.c_void_p(p.data_ptr()), p.numel(), n_new, C.byref(cfg),
                          C.c_void_p(out.data_ptr()), C.byref(st)))

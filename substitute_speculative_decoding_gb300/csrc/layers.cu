@@ -51,6 +51,61 @@ int32_t launch_embed(const uint16_t* embed, int hidden, const RowSet& rs, int ro
   return SUB_OK;
 }
 
+// Rows that enter a forward part-way (the verify from a layer the draft has
+// already computed for the same nodes): x = src row, and the first layer's
+// RMSNorm input exactly as embed_kernel forms it from an embedding row.
+__global__ void rows_in_kernel(const float* __restrict__ src, int hidden,
+                               float* __restrict__ x, const uint16_t* __restrict__ gain, float eps,
+                               uint16_t* __restrict__ xn, float* __restrict__ ss_out) {
+  __shared__ float s_part[32];
+  pdl_wait();
+  pdl_trigger();
+  const int r = blockIdx.x;
+  const float* sr = src + (int64_t)r * hidden;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < hidden; i += blockDim.x) {
+    const float v = sr[i];
+    x[(int64_t)r * hidden + i] = v;
+    ss = fmaf(v, v, ss);
+  }
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) s_part[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += s_part[w];
+  const float inv = rsqrtf(tot / (float)hidden + eps);
+  if (ss_out && threadIdx.x == 0) ss_out[r] = tot;
+  const float scale = ss_out ? 1.0f : inv;
+  for (int i = threadIdx.x; i < hidden; i += blockDim.x)
+    reinterpret_cast<__nv_bfloat16*>(xn)[(int64_t)r * hidden + i] =
+        __float2bfloat16_rn(sr[i] * scale * bf16_bits_to_f32(gain[i]));
+}
+
+int32_t launch_rows_in(const float* src, int hidden, int rows, float* x, const uint16_t* gain,
+                       float eps, uint16_t* xn, float* ss_out, cudaStream_t st) {
+  if (rows <= 0) return SUB_OK;
+  SUB_CUDA_TRY(launch_k(rows_in_kernel, dim3(rows), dim3(256), 0, st, src, hidden, x, gain, eps,
+                        xn, ss_out));
+  return SUB_OK;
+}
+
+// dst[r, :] = x[r, :] for `rows` rows of `hidden` floats (16-byte aligned rows).
+__global__ void rows_out_kernel(const float4* __restrict__ x, int n4, float4* __restrict__ dst) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n4) dst[i] = x[i];
+}
+
+int32_t launch_rows_out(const float* x, int hidden, int rows, float* dst, cudaStream_t st) {
+  if (rows <= 0) return SUB_OK;
+  SUB_CHECK_ARG(hidden % 4 == 0 && aligned16(x) && aligned16(dst), "rows_out: alignment");
+  const int n4 = rows * hidden / 4;
+  SUB_CUDA_TRY(launch_k(rows_out_kernel, dim3((n4 + 255) / 256), dim3(256), 0, st,
+                        reinterpret_cast<const float4*>(x), n4, reinterpret_cast<float4*>(dst)));
+  return SUB_OK;
+}
+
 // y = bf16(x * rsqrt(mean(x^2) + eps) * gain); one CTA per row, fixed-order sum.
 __global__ void rmsnorm_kernel(const float* __restrict__ x, const uint16_t* __restrict__ gain,
                                int hidden, float eps, uint16_t* __restrict__ out) {

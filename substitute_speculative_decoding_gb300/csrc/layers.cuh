@@ -20,6 +20,11 @@ struct RowSet {
 // x[r]^2, one part of the consumer's RowScale).
 int32_t launch_embed(const uint16_t* embed, int hidden, const RowSet& rs, int rows, float* x,
                      const uint16_t* gain, float eps, uint16_t* xn, float* ss_out, cudaStream_t st);
+// Rows entering a forward at a later layer: x = src, xn (and ss_out) as launch_embed forms them.
+int32_t launch_rows_in(const float* src, int hidden, int rows, float* x, const uint16_t* gain,
+                       float eps, uint16_t* xn, float* ss_out, cudaStream_t st);
+// dst = x for rows x hidden floats (the residual stream handed to a later forward).
+int32_t launch_rows_out(const float* x, int hidden, int rows, float* dst, cudaStream_t st);
 int32_t launch_rmsnorm(const float* x, const uint16_t* gain, int rows, int hidden, float eps,
                        uint16_t* out, cudaStream_t st);
 

@@ -66,6 +66,7 @@ struct sub_model {
   int max_pos = 0;
   // activations
   float* x = nullptr;        // [rows, H]
+  float* xsave = nullptr;    // [tree slots, H]: residual stream at layer n_resident (verify reuse)
   uint16_t* xn = nullptr;    // [rows, H]
   float* qkv = nullptr;      // [rows, qkv_dim]
   uint16_t* q = nullptr;     // [rows, Hq*D]
@@ -300,6 +301,13 @@ struct FwdRows {
   int64_t base;            // committed length (host) ...
   const int32_t* base_dev; // ... or on the device
   int64_t keys_hint;       // for the split heuristic
+  // layer range [layer0, layer_end) (layer_end 0: all layers, then the head);
+  // x_in / x_out: per-slot residual streams [slots, hidden] fp32 to start
+  // from (instead of the embedding) and to leave at layer_end
+  int layer0;
+  int layer_end;
+  const float* x_in;
+  float* x_out;
 };
 
 static GemvArgs mm_args(const void* X, int M, int K, const Matrices& W, const int* idx, int nseg,
@@ -361,8 +369,13 @@ static int32_t forward(sub_model* m, bool draft, const FwdRows& r, float* logits
     r_attn = RowScale{m->norm_partial, 1, H, d.rms_eps, 0};   // the embedding: one part
     r_ffn = RowScale{m->norm_partial + m->norm_parts, tiles, H, d.rms_eps, 0};
   }
-  SUB_TRY(launch_embed(d.embed, H, rs, M, m->x, m->layers[0].attn_norm, d.rms_eps, m->xn,
-                       fuse_norm ? m->norm_partial : nullptr, st));
+  const int l0 = r.layer0, l1 = r.layer_end ? r.layer_end : d.n_layers;
+  if (r.x_in)
+    SUB_TRY(launch_rows_in(r.x_in + (size_t)r.slot0 * H, H, M, m->x, m->layers[l0].attn_norm,
+                           d.rms_eps, m->xn, fuse_norm ? m->norm_partial : nullptr, st));
+  else
+    SUB_TRY(launch_embed(d.embed, H, rs, M, m->x, m->layers[0].attn_norm, d.rms_eps, m->xn,
+                         fuse_norm ? m->norm_partial : nullptr, st));
 
   AttnArgs at{};
   at.Q = m->q;
@@ -438,7 +451,7 @@ static int32_t forward(sub_model* m, bool draft, const FwdRows& r, float* logits
   const int gu_idx[2] = {4, 5};
   const int dn_idx[1] = {6};
 
-  for (int l = 0; l < d.n_layers; ++l) {
+  for (int l = l0; l < l1; ++l) {
     const sub_layer_desc& L = m->layers[l];
     const bool off = l >= d.n_resident;
     const bool w4 = off && draft;
@@ -452,14 +465,14 @@ static int32_t forward(sub_model* m, bool draft, const FwdRows& r, float* logits
 
     trace_mark(m, w4 ? "qkv_w4" : "qkv_bf16");
     if (fuse_qkv) {
-      if (!fuse_norm && l > 0) SUB_TRY(launch_rmsnorm(m->x, L.attn_norm, M, H, d.rms_eps, m->xn, st));
+      if (!fuse_norm && l > l0) SUB_TRY(launch_rmsnorm(m->x, L.attn_norm, M, H, d.rms_eps, m->xn, st));
       GemvArgs qa = mm_args(m->xn, M, H, W, qkv_idx, 3, qkv_rows, nullptr, 0, m);
       qa.xscale = r_attn;
       qo.layer = l;
       qa.qkv = qo;
       SUB_TRY(launch_gemv(qa, w4, EPI_QKV, st));
     } else {
-      if (l > 0 && !fuse_norm) SUB_TRY(launch_rmsnorm(m->x, L.attn_norm, M, H, d.rms_eps, m->xn, st));
+      if (l > l0 && !fuse_norm) SUB_TRY(launch_rmsnorm(m->x, L.attn_norm, M, H, d.rms_eps, m->xn, st));
       GemvArgs qa = mm_args(m->xn, M, H, W, qkv_idx, 3, qkv_rows, m->qkv, m->qkv_dim, m);
       qa.xscale = r_attn;
       SUB_TRY(launch_matmul(qa, w4, EPI_F32, st));
@@ -508,6 +521,8 @@ static int32_t forward(sub_model* m, bool draft, const FwdRows& r, float* logits
       }
     }
   }
+  if (r.x_out) SUB_TRY(launch_rows_out(m->x, H, M, r.x_out + (size_t)r.slot0 * H, st));
+  if (l1 < d.n_layers) return SUB_OK;   // a leading part: no head
   // final norm (already in xn on the fused path) + lm_head
   const int first = last_only ? M - 1 : 0;
   const int nrow = last_only ? 1 : M;
@@ -687,6 +702,11 @@ extern "C" int32_t sub_model_create(const sub_model_desc* desc, sub_model** out)
   }
   const size_t R = m->rows_max;
   CREATE_TRY(dalloc_t(m, &m->x, R * H));
+  if (d.n_resident > 0 && d.max_depth > 0) {
+    const size_t n_tree = 1 + (size_t)d.max_depth * d.max_width;
+    CREATE_TRY(dalloc_t(m, &m->xsave, n_tree * H));
+    CREATE_CUDA(cudaMemset(m->xsave, 0, n_tree * H * 4));
+  }
   CREATE_TRY(dalloc_t(m, &m->xn, R * H));
   CREATE_TRY(dalloc_t(m, &m->qkv, R * m->qkv_dim));
   CREATE_TRY(dalloc_t(m, &m->q, R * m->q_dim));
@@ -849,6 +869,11 @@ extern "C" int32_t sub_model_forward(sub_model* m, int32_t which, const int32_t*
 // ----------------------------------------------------------------- generate --
 // Adaptive depth is on for a finite negative stop_logp (0, a zero-filled
 // config, -inf and NaN all draft every level).
+// Verify reuse needs resident layers to share and a tree.
+static bool reuses(const sub_model* m, const sub_decode_cfg& c) {
+  return c.verify_reuse && c.depth > 0 && m->d.n_resident > 0 && m->xsave;
+}
+
 static bool adaptive(const sub_decode_cfg& c) {
   return c.depth > 0 && c.stop_logp < 0.f && c.stop_logp > -INFINITY;
 }
@@ -898,7 +923,14 @@ static int32_t enqueue_cycle(sub_model* m, const sub_decode_cfg& c) {
   // ---- draft ----
   // one level: the draft forward over its rows, the expansion into the next
   // level and, with adaptive depth, the decision to go on
-  auto level = [&](int lvl, cudaGraphConditionalHandle next, int has_next) -> int32_t {
+  // With verify reuse the draft forward of a level is split at layer R =
+  // n_resident: the new nodes' leading part (layers < R, the resident layers
+  // the target shares) runs right after the expansion that made them and
+  // leaves their residual stream in xsave, and the level's own pass starts
+  // from there.  The verify then starts at layer R too.
+  const bool reuse = reuses(m, c);
+  const int R = d.n_resident;
+  auto rows_of = [&](int lvl) {
     const int s0 = lvl == 0 ? 0 : 1 + (lvl - 1) * k;
     const int M = lvl == 0 ? 1 : k;
     FwdRows r{};
@@ -911,6 +943,22 @@ static int32_t enqueue_cycle(sub_model* m, const sub_decode_cfg& c) {
     r.n_slots = s0 + M;
     r.base_dev = m->state + ST_N;
     r.keys_hint = d.max_seq;
+    return r;
+  };
+  auto lead = [&](int lvl) -> int32_t {   // layers [0, R) of level lvl's rows into xsave
+    FwdRows r = rows_of(lvl);
+    r.layer_end = R;
+    r.x_out = m->xsave;
+    return forward(m, true, r, nullptr, false);
+  };
+  if (reuse) SUB_TRY(lead(0));
+  auto level = [&](int lvl, cudaGraphConditionalHandle next, int has_next) -> int32_t {
+    const int M = lvl == 0 ? 1 : k;
+    FwdRows r = rows_of(lvl);
+    if (reuse) {
+      r.layer0 = R;
+      r.x_in = m->xsave;
+    }
     SUB_TRY(forward(m, true, r, m->logits, false));
     ExpandArgs e{};
     e.logits = m->logits;
@@ -928,6 +976,7 @@ static int32_t enqueue_cycle(sub_model* m, const sub_decode_cfg& c) {
     e.part_sum = m->part_f + parts;
     e.counter = m->counters;
     SUB_TRY(launch_expand(e, m->s_main));
+    if (reuse) SUB_TRY(lead(lvl + 1));
     if (adaptive(c))
       SUB_CUDA_TRY(launch_k(adapt_kernel, dim3(1), dim3(32), 0, m->s_main, (const float*)tr.score,
                             1 + lvl * k, k, c.stop_logp, m->state, lvl, next, has_next));
@@ -998,6 +1047,10 @@ static int32_t enqueue_cycle(sub_model* m, const sub_decode_cfg& c) {
   v.n_slots = n_tree;
   v.base_dev = m->state + ST_N;
   v.keys_hint = d.max_seq;
+  if (reuse) {   // layers < R of every tree node were computed by the draft
+    v.layer0 = R;
+    v.x_in = m->xsave;
+  }
   SUB_TRY(forward(m, false, v, m->logits, false));
   SUB_TRY(end_target_pass(m));
   SUB_CUDA_TRY(mark(m->ev_cyc[2], m->s_main));
@@ -1026,7 +1079,8 @@ static int32_t enqueue_cycle(sub_model* m, const sub_decode_cfg& c) {
 static bool same_cfg(const sub_decode_cfg& a, const sub_decode_cfg& b) {
   return a.depth == b.depth && a.width == b.width && a.draft_temp == b.draft_temp &&
          a.mode == b.mode && a.target_temp == b.target_temp && a.seed == b.seed &&
-         std::memcmp(&a.stop_logp, &b.stop_logp, sizeof(float)) == 0;
+         std::memcmp(&a.stop_logp, &b.stop_logp, sizeof(float)) == 0 &&
+         (a.verify_reuse != 0) == (b.verify_reuse != 0);
 }
 
 static int32_t check_cfg(const sub_model* m, const sub_decode_cfg& c) {
