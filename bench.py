@@ -614,7 +614,10 @@ def main():
                "decode_ms": st.t_decode_ms, "tau": st.tau, "cycles": st.cycles,
                "per_cycle_ms": {"draft": st.t_draft_ms / cycles,
                                 "verify": st.t_verify_ms / cycles,
-                                "copy_unhidden": st.t_copy_unhidden_ms / cycles},
+                                "copy_unhidden": st.t_copy_unhidden_ms / cycles,
+                                "copy": st.t_copy_ms / cycles},
+               "h2d_gbs": (h2d_per_cycle * cycles / (st.t_copy_ms / 1e3) / 1e9
+                           if st.t_copy_ms > 0 else None),
                "draft_over_target": (st.t_draft_ms / st.t_verify_ms
                                      if st.t_verify_ms > 0 else None),
                "near_tie_events": st.near_tie_events,
@@ -639,7 +642,7 @@ def main():
             depth_sweep.append({"depth": dd,
                                 "decode_tokens_per_s": (ADAPTIVE_NEW - 1) / (sd.t_decode_ms / 1e3),
                                 "tau": sd.tau, "cycle_ms": sd.t_decode_ms / cyc_d,
-                                "cycles": sd.cycles, **phase_ms(sd)})
+                                "cycles": sd.cycles, **phase_ms(sd, h2d_per_cycle)})
         adaptive = []
         for stop in ADAPTIVE_STOPS:
             model.cycle_info(sub.Model.decode_cfg(DEPTH, WIDTH, DRAFT_T, mode=mode,
@@ -652,7 +655,7 @@ def main():
                              "decode_tokens_per_s": (ADAPTIVE_NEW - 1) / (sa.t_decode_ms / 1e3),
                              "tau": sa.tau, "mean_depth": sa.drafted_levels / cyc_a,
                              "cycle_ms": sa.t_decode_ms / cyc_a, "cycles": sa.cycles,
-                             **phase_ms(sa)})
+                             **phase_ms(sa, h2d_per_cycle)})
 
     # verify reuse of the draft's leading (resident) layers, fixed depth and
     # adaptive depth at stop_logp -6
@@ -670,7 +673,7 @@ def main():
             reuse.append({"stop_logp": stop,
                           "decode_tokens_per_s": (ADAPTIVE_NEW - 1) / (sr.t_decode_ms / 1e3),
                           "tau": sr.tau, "mean_depth": sr.drafted_levels / cr,
-                          "cycle_ms": sr.t_decode_ms / cr, **phase_ms(sr)})
+                          "cycle_ms": sr.t_decode_ms / cr, **phase_ms(sr, h2d_per_cycle)})
 
     # host link and kernel measurements come after this model's decode runs
     link = measure_link(dev)
@@ -716,7 +719,7 @@ def main():
                 entry[key] = {"decode_tokens_per_s": (ADAPTIVE_NEW - 1) / (sb.t_decode_ms / 1e3),
                               "tau": sb.tau, "mean_depth": sb.drafted_levels / cb,
                               "draft_ms_per_level": sb.t_draft_ms / max(sb.drafted_levels, 1),
-                              **phase_ms(sb)}
+                              **phase_ms(sb, h2d_per_cycle)}
             mb.close()
             lowbit.append(entry)
             torch.cuda.empty_cache()
@@ -785,12 +788,17 @@ def main():
         raise SystemExit(f"{timeouts} bounded pipeline wait(s) ran out: the numbers are invalid")
 
 
-def phase_ms(st):
-    """Per-cycle device time of a generate call's phases (sub_stats)."""
+def phase_ms(st, h2d_per_cycle=None):
+    """Per-cycle device time of a generate call's phases (sub_stats), and the
+    host link rate its streamed copies got."""
     c = max(int(st.cycles), 1)
-    return {"per_cycle_ms": {"draft": round(st.t_draft_ms / c, 3),
-                             "verify": round(st.t_verify_ms / c, 3),
-                             "copy_unhidden": round(st.t_copy_unhidden_ms / c, 3)}}
+    out = {"per_cycle_ms": {"draft": round(st.t_draft_ms / c, 3),
+                            "verify": round(st.t_verify_ms / c, 3),
+                            "copy_unhidden": round(st.t_copy_unhidden_ms / c, 3),
+                            "copy": round(st.t_copy_ms / c, 3)}}
+    if h2d_per_cycle and st.t_copy_ms > 0:
+        out["h2d_gbs"] = round(h2d_per_cycle * c / (st.t_copy_ms / 1e3) / 1e9, 1)
+    return out
 
 
 def profile_traffic(kernel):

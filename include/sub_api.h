@@ -385,6 +385,10 @@ typedef struct {
   int64_t near_tie_events;
   /* draft levels run over all cycles (cycles * depth without adaptive depth) */
   int64_t drafted_levels;
+  /* device time from each cycle's start to the last offloaded original
+   * landing in the staging ring, summed over cycles (0 without offloaded
+   * layers): streamed bytes / t_copy_ms is the host link rate the cycles got */
+  double t_copy_ms;
 } sub_stats;
 
 /* Step-wise decoding (the pieces sub_generate is made of).

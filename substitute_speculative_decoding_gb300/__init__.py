@@ -76,7 +76,7 @@ class Stats(C.Structure):
                 ("t_prefill_ms", C.c_double), ("t_decode_ms", C.c_double),
                 ("accept_hist", _i64 * 65), ("t_draft_ms", C.c_double),
                 ("t_verify_ms", C.c_double), ("t_copy_unhidden_ms", C.c_double),
-                ("near_tie_events", _i64), ("drafted_levels", _i64)]
+                ("near_tie_events", _i64), ("drafted_levels", _i64), ("t_copy_ms", C.c_double)]
 
 
 def _decl(name, args):
@@ -355,12 +355,27 @@ class Model:
             self.keep.append(t)
             return t
 
+        # the offloaded originals live in one pinned host arena (one large
+        # page-locked allocation), each matrix 256-byte aligned inside it
+        names = ("wq", "wk", "wv", "wo", "wg", "wu", "wd")
+        off_mats = [(i, n) for i in range(cfg.n_resident, cfg.n_layers) for n in names]
+        sizes = [weights["layers"][i][n].numel() * 2 for i, n in off_mats]
+        total = sum((b + 255) // 256 * 256 for b in sizes)
+        arena = torch.empty(max(total, 256), dtype=torch.uint8, pin_memory=True)
+        self.keep.append(arena)
+        host_of, pos = {}, 0
+        for (i, n), b in zip(off_mats, sizes):
+            w = weights["layers"][i][n]
+            view = arena[pos:pos + b].view(torch.bfloat16).view(w.shape)
+            view.copy_(w)
+            host_of[(i, n)] = view
+            pos += (b + 255) // 256 * 256
+
         layers = (LayerDesc * cfg.n_layers)()
         for i, lw in enumerate(weights["layers"]):
             L = layers[i]
             L.attn_norm = dev_t(lw["attn_norm"]).data_ptr()
             L.ffn_norm = dev_t(lw["ffn_norm"]).data_ptr()
-            names = ("wq", "wk", "wv", "wo", "wg", "wu", "wd")
             w4n = ("q4", "k4", "v4", "o4", "g4", "u4", "d4")
             for name, qn in zip(names, w4n):
                 w = lw[name]
@@ -375,9 +390,7 @@ class Model:
                         q, s, z = w4_pack(wd) if b == 4 else wq_pack(wd, b)
                     self.w4[(i, name)] = (q, s, z)
                     setattr(L, qn, W4(q.data_ptr(), s.data_ptr(), z.data_ptr(), b))
-                    host = w.to("cpu").contiguous().pin_memory()
-                    self.keep.append(host)
-                    setattr(L, name, host.data_ptr())
+                    setattr(L, name, host_of[(i, name)].data_ptr())
                     del wd
         torch.cuda.synchronize(dev)
         d = ModelDesc()

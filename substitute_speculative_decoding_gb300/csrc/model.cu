@@ -1295,7 +1295,7 @@ extern "C" int32_t sub_generate(sub_model* m, const int32_t* prompt_host, int32_
   SUB_CUDA_TRY(cudaEventRecord(m->ev_g1, st));
   SUB_TRY(read_state(m));
   int emitted = m->host_state[ST_EMITTED];
-  double t_draft = 0.0, t_verify = 0.0, t_unhidden = 0.0;
+  double t_draft = 0.0, t_verify = 0.0, t_unhidden = 0.0, t_copy = 0.0;
   while (emitted < n_new) {
     SUB_TRY(decode_impl(m, c, 1));
     SUB_TRY(read_state(m));
@@ -1303,6 +1303,10 @@ extern "C" int32_t sub_generate(sub_model* m, const int32_t* prompt_host, int32_
     // this cycle's phase times (the marks of the cycle just synchronised)
     t_draft += span_ms(m->ev_cyc[0], m->ev_cyc[1]);
     t_verify += span_ms(m->ev_cyc[1], m->ev_cyc[2]);
+    if (m->n_off > 0) {
+      const double c = span_ms(m->ev_cyc[0], m->ev_tstaged[m->n_off - 1]);
+      t_copy = (c < -1e29 || t_copy < 0.0) ? -1.0 : t_copy + c;
+    }
     for (int j = 0; j < m->n_off; ++j) {
       const double w = span_ms(m->ev_ready[j], m->ev_tstaged[j]);   // < 0: copy was early
       t_unhidden = (w < -1e29 || t_unhidden < 0.0) ? -1.0 : t_unhidden + std::max(0.0, w);
@@ -1329,6 +1333,7 @@ extern "C" int32_t sub_generate(sub_model* m, const int32_t* prompt_host, int32_
     stats->t_draft_ms = t_draft >= 0.0 ? t_draft : -1.0;
     stats->t_verify_ms = t_verify >= 0.0 ? t_verify : -1.0;
     stats->t_copy_unhidden_ms = t_unhidden >= 0.0 ? t_unhidden : -1.0;
+    stats->t_copy_ms = t_copy >= 0.0 ? t_copy : -1.0;
     stats->near_tie_events = m->host_state[ST_TIES];
     stats->drafted_levels = adaptive(c) ? m->host_state[ST_LEVELS] : m->cycles * c.depth;
   }

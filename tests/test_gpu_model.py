@@ -130,6 +130,8 @@ def test_generate_greedy_is_lossless(tiny, depth, width):
     else:
         assert st.t_draft_ms > 0.0
     assert st.t_draft_ms + st.t_verify_ms <= st.t_decode_ms * 1.05 + 0.5
+    # the streamed originals of the offloaded layer land within each cycle
+    assert 0.0 < st.t_copy_ms <= st.t_decode_ms * 1.05 + 0.5
     # the device's near-ties (its own top-2 gap < 1e-2) cover every position
     # where it picked another token than the oracle within the tie gap, or more
     assert st.near_tie_events >= 0 and st.near_tie_events <= 64
