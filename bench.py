@@ -67,7 +67,8 @@ WORKLOADS = {
                          "14336, vocab 128256, RoPE theta 5e5), random bf16 init; 8 resident + "
                          "24 int4 g64 substitutes with pinned-host originals; prompt 1024; "
                          "depth 48, width 8, greedy; step = one cycle"),
-    "qwen32b": dict(cfg="qwen32b", staging=2, embed_on_host=True, e2e_new=256,
+    "qwen32b": dict(cfg="qwen32b", staging=2, embed_on_host=True, e2e_new=256, sweep_new=32,
+                    lowbit=False,
                     text="Qwen2.5-32B-shaped decoder (64 layers, hidden 5120, 40/8 heads, FFN "
                          "27648, vocab 152064), random bf16 init, 24 GB device budget: 1 resident "
                          "layer + 63 int4 g64 substitutes, 2-slot staging ring for the pinned-host "
@@ -555,11 +556,12 @@ def main():
     cfg = synthetic.CONFIGS[wl["cfg"]]
     mode = 1 if cfg.mode == "gumbel" else 0
     e2e_new = args.new or wl["e2e_new"]
+    sweep_new = wl.get("sweep_new", ADAPTIVE_NEW)   # tokens per sweep run
     dev = torch.device("cuda", torch.cuda.current_device())
     pk = peaks()
     t_setup = time.perf_counter()
     max_seq = cfg.prompt_len + max(e2e_new, (args.warmup + args.steps + 2) * (DEPTH + 1),
-                                   ADAPTIVE_NEW + max(DEPTH_SWEEP) + 1) + 64
+                                   sweep_new + max(DEPTH_SWEEP) + 1) + 64
     weights, model = build_model(sub, cfg, wl, dev, max_seq)
     t_setup = time.perf_counter() - t_setup
     timeouts0 = sub.pipeline_timeouts()
@@ -636,11 +638,11 @@ def main():
             # capture the cycle graph first: the decode time is then steady-state
             model.cycle_info(sub.Model.decode_cfg(dd, WIDTH, DRAFT_T, mode=mode,
                                                   target_temp=cfg.target_temp, seed=cfg.seed))
-            _, sd = model.generate(prompt, ADAPTIVE_NEW, dd, WIDTH, DRAFT_T, mode=mode,
+            _, sd = model.generate(prompt, sweep_new, dd, WIDTH, DRAFT_T, mode=mode,
                                    target_temp=cfg.target_temp, seed=cfg.seed)
             cyc_d = max(int(sd.cycles), 1)
             depth_sweep.append({"depth": dd,
-                                "decode_tokens_per_s": (ADAPTIVE_NEW - 1) / (sd.t_decode_ms / 1e3),
+                                "decode_tokens_per_s": (sweep_new - 1) / (sd.t_decode_ms / 1e3),
                                 "tau": sd.tau, "cycle_ms": sd.t_decode_ms / cyc_d,
                                 "cycles": sd.cycles, **phase_ms(sd, h2d_per_cycle)})
         adaptive = []
@@ -648,11 +650,11 @@ def main():
             model.cycle_info(sub.Model.decode_cfg(DEPTH, WIDTH, DRAFT_T, mode=mode,
                                                   target_temp=cfg.target_temp, seed=cfg.seed,
                                                   stop_logp=stop))
-            _, sa = model.generate(prompt, ADAPTIVE_NEW, DEPTH, WIDTH, DRAFT_T, mode=mode,
+            _, sa = model.generate(prompt, sweep_new, DEPTH, WIDTH, DRAFT_T, mode=mode,
                                    target_temp=cfg.target_temp, seed=cfg.seed, stop_logp=stop)
             cyc_a = max(int(sa.cycles), 1)
             adaptive.append({"stop_logp": stop,
-                             "decode_tokens_per_s": (ADAPTIVE_NEW - 1) / (sa.t_decode_ms / 1e3),
+                             "decode_tokens_per_s": (sweep_new - 1) / (sa.t_decode_ms / 1e3),
                              "tau": sa.tau, "mean_depth": sa.drafted_levels / cyc_a,
                              "cycle_ms": sa.t_decode_ms / cyc_a, "cycles": sa.cycles,
                              **phase_ms(sa, h2d_per_cycle)})
@@ -666,12 +668,12 @@ def main():
             model.cycle_info(sub.Model.decode_cfg(DEPTH, WIDTH, DRAFT_T, mode=mode,
                                                   target_temp=cfg.target_temp, seed=cfg.seed,
                                                   stop_logp=stop, verify_reuse=True))
-            _, sr = model.generate(prompt, ADAPTIVE_NEW, DEPTH, WIDTH, DRAFT_T, mode=mode,
+            _, sr = model.generate(prompt, sweep_new, DEPTH, WIDTH, DRAFT_T, mode=mode,
                                    target_temp=cfg.target_temp, seed=cfg.seed, stop_logp=stop,
                                    verify_reuse=True)
             cr = max(int(sr.cycles), 1)
             reuse.append({"stop_logp": stop,
-                          "decode_tokens_per_s": (ADAPTIVE_NEW - 1) / (sr.t_decode_ms / 1e3),
+                          "decode_tokens_per_s": (sweep_new - 1) / (sr.t_decode_ms / 1e3),
                           "tau": sr.tau, "mean_depth": sr.drafted_levels / cr,
                           "cycle_ms": sr.t_decode_ms / cr, **phase_ms(sr, h2d_per_cycle)})
 
@@ -695,7 +697,7 @@ def main():
     # 4-bit, the rest 2-bit) substitutes; decode tokens/s, tau and the draft's
     # share, at the fixed depth and with adaptive depth at stop_logp -6
     lowbit = None
-    if not args.quick:
+    if not args.quick and wl.get("lowbit", True):
         model.close()
         model = None
         torch.cuda.empty_cache()
@@ -713,10 +715,10 @@ def main():
                 mb.cycle_info(sub.Model.decode_cfg(DEPTH, WIDTH, DRAFT_T, mode=mode,
                                                    target_temp=cfg.target_temp, seed=cfg.seed,
                                                    stop_logp=stop))
-                _, sb = mb.generate(prompt, ADAPTIVE_NEW, DEPTH, WIDTH, DRAFT_T, mode=mode,
+                _, sb = mb.generate(prompt, sweep_new, DEPTH, WIDTH, DRAFT_T, mode=mode,
                                     target_temp=cfg.target_temp, seed=cfg.seed, stop_logp=stop)
                 cb = max(int(sb.cycles), 1)
-                entry[key] = {"decode_tokens_per_s": (ADAPTIVE_NEW - 1) / (sb.t_decode_ms / 1e3),
+                entry[key] = {"decode_tokens_per_s": (sweep_new - 1) / (sb.t_decode_ms / 1e3),
                               "tau": sb.tau, "mean_depth": sb.drafted_levels / cb,
                               "draft_ms_per_level": sb.t_draft_ms / max(sb.drafted_levels, 1),
                               **phase_ms(sb, h2d_per_cycle)}

@@ -7,6 +7,8 @@ of verify rows, the first draft levels' logits, and the accept walk.  At this
 depth the logit tolerance is calibrated against the oracle run with float32
 GEMM accumulation (tests/fullsize.py explains why); the near-tie counts and
 error statistics are printed."""
+import os
+
 import pytest
 
 import synthetic
@@ -29,4 +31,17 @@ def test_qwen7b_workload_matches_the_oracle(sub):
 def test_llama8b_workload_matches_the_oracle(sub):
     # every 32nd cycle: the 1.5k-row oracle forwards dominate this test's time
     r = fullsize.run(sub, synthetic.CONFIGS["llama8b"], 512, verify_sample=16, every=32)
+    assert r["cycles"] >= 2 and len(r["checked_cycles"]) >= 3
+
+
+@pytest.mark.skipif(os.environ.get("SUB_TEST_QWEN32B") != "1",
+                    reason="its oracle forwards take about a quarter of an hour; set SUB_TEST_QWEN32B=1")
+def test_qwen32b_workload_matches_the_oracle(sub):
+    """The Qwen2.5-32B-shaped workload as the bench runs it: 1 resident layer,
+    63 int4 substitutes, a 2-slot staging ring, the embedding in pinned host
+    memory, Gumbel-max sampling at T = 0.6 with seed 7; 48 generated tokens,
+    cycles 1, 2 and every 16th checked, the oracle's layers built lazily."""
+    r = fullsize.run(sub, synthetic.CONFIGS["qwen32b"], 48, mode="gumbel", temp=0.6, seed=7,
+                     staging=2, embed_on_host=True, draft_levels=2, verify_sample=16,
+                     lazy=True, every=16)
     assert r["cycles"] >= 2 and len(r["checked_cycles"]) >= 3
