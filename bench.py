@@ -599,6 +599,10 @@ def main():
     tokens_all = reduce(world, tokens, "sum")
     value = tokens_all / (ms_max / 1e3)
 
+    # clocks and throttle reasons over the e2e run and the sweeps as well
+    clocks_sweeps = Clocks(gpu_index(local))
+    if not args.quick:
+        clocks_sweeps.start()
     # e2e: the public call with host buffers, prefill included
     e2e = None
     if not args.quick:
@@ -677,6 +681,7 @@ def main():
                           "tau": sr.tau, "mean_depth": sr.drafted_levels / cr,
                           "cycle_ms": sr.t_decode_ms / cr, **phase_ms(sr, h2d_per_cycle)})
 
+    clk_sweeps = clocks_sweeps.stop() if not args.quick else None
     # host link and kernel measurements come after this model's decode runs
     link = measure_link(dev)
     bound = cycle_bound(cfg, pk, tau, cfg.prompt_len + tokens, link, wl["staging"])
@@ -774,7 +779,7 @@ def main():
         "roofline": roof, "kernels": kern, "cpu_baseline": cpu, "e2e": e2e,
         "adaptive": adaptive, "depth_sweep": depth_sweep, "lowbit": lowbit, "verify_reuse": reuse,
         "gpu_launches": kernels_per_cycle * args.steps, "kernels_per_cycle": kernels_per_cycle,
-        "clocks": clk, "setup_s": round(t_setup, 1),
+        "clocks": clk, "clocks_e2e_and_sweeps": clk_sweeps, "setup_s": round(t_setup, 1),
         "model_device_bytes": model_bytes,
         "device_bytes_total": device_total,
         "pipeline_timeouts": timeouts, "valid": timeouts == 0,
