@@ -159,9 +159,11 @@ class Clocks:
             for i, n in enumerate(names):
                 if r[5 + i].lower().startswith("active"):
                     reasons.add(n)
+        pw = [float(r[3]) for r in self.rows if len(r) >= 9 and r[3].replace(".", "").isdigit()]
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "power_w_median": statistics.median(pw) if pw else None,
+                "power_w_max": max(pw) if pw else None}
 
 
 def gpu_index(local):
