@@ -154,7 +154,7 @@ size_t gemv_tma_scratch_floats(const GemvArgs& a, bool is_w4, int epi);
 int32_t gemv_init();
 // Pipeline waits that ran out since load (each one is a bug; never expected).
 int32_t gemv_tma_timeouts(unsigned int* out);
-// The driver's tensor-map encoder (null if unavailable), and a 2-D tiled map
+// The CUDA driver API's tensor-map encoder (null if unavailable), and a 2-D tiled map
 // over a row-major [rows, cols] array with the given row stride and box
 // (128-byte swizzle when swz); false when the encoder or the alignment refuses.
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn();

@@ -79,7 +79,7 @@ def test_static_matches_allocating_accept_twice(sub, mode, vocab, depth, width, 
 
 def _default_pool_high_water():
     """Reset, then read back, the high-water mark of the device's default
-    memory pool (the pool cudaMallocAsync draws from), through the driver."""
+    memory pool (the pool cudaMallocAsync draws from), through the CUDA driver API."""
     drv = C.CDLL("libcuda.so.1")
     dev = C.c_int()
     assert drv.cuDeviceGet(C.byref(dev), torch.cuda.current_device()) == 0
