@@ -22,7 +22,9 @@ Workloads (--workload):
 
 Flags: --gpus N (replicas; one process per GPU under torchrun), --steps K,
 --warmup W, --impl reference (the CPU oracle arm), --quick (skip the kernel
-sweep, e2e and the CPU baseline: for profiler launch lists), --new N.
+sweep, e2e and the CPU baseline: for profiler launch lists), --new N,
+--stop-logp X (adaptive depth for the timed cycles and the e2e run; the
+default line is the fixed-depth workload).
 """
 from __future__ import annotations
 
@@ -546,6 +548,8 @@ def main():
     ap.add_argument("--workload", default="qwen7b", choices=sorted(WORKLOADS))
     ap.add_argument("--new", type=int, default=None, help="tokens generated by the e2e leg")
     ap.add_argument("--quick", action="store_true")
+    ap.add_argument("--stop-logp", type=float, default=None,
+                    help="adaptive depth for the timed cycles and the e2e run (default: off)")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.impl == "reference":
@@ -570,7 +574,7 @@ def main():
 
     prompt = synthetic.make_prompt(cfg)
     dcfg = sub.Model.decode_cfg(DEPTH, WIDTH, DRAFT_T, mode=mode, target_temp=cfg.target_temp,
-                                seed=cfg.seed)
+                                seed=cfg.seed, stop_logp=args.stop_logp)
     kernels_per_cycle, h2d_per_cycle = model.cycle_info(dcfg)
     stream = torch.cuda.current_stream()
     model.prefill(prompt, dcfg, stream)
@@ -610,7 +614,8 @@ def main():
     if not args.quick:
         t0 = time.perf_counter()
         out, st = model.generate(prompt, e2e_new, DEPTH, WIDTH, DRAFT_T, mode=mode,
-                                 target_temp=cfg.target_temp, seed=cfg.seed)
+                                 target_temp=cfg.target_temp, seed=cfg.seed,
+                                 stop_logp=args.stop_logp)
         t_e2e = time.perf_counter() - t0
         cycles = max(int(st.cycles), 1)
         h2d_total = prompt.numel() * 4 + h2d_per_cycle * (st.cycles + 1)
@@ -769,6 +774,9 @@ def main():
         "data": "synthetic",
         "config": {"workload": wl["text"], "prompt": cfg.prompt_len, "depth": DEPTH,
                    "width": WIDTH, "parallelism": f"replicas x{world}",
+                   **({"stop_logp": args.stop_logp,
+                       "gpu_launches": "upper bound: every conditional draft level counted"}
+                      if args.stop_logp is not None else {}),
                    "l2": "inputs larger than L2 (every draft level reads all weights: "
                          f"{bound['level_bytes'] / 1e9:.2f} GB)"},
         "tau": tau, "tokens_timed": tokens_all,
