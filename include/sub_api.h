@@ -116,7 +116,7 @@ int32_t sub_bf16_gemm(const sub_bf16* X, int64_t M, const sub_bf16* W, int64_t N
 /* ------------------------------------------------------------------------ */
 /* 2-, 3- and 4-bit substitutes (lower and per-layer mixed precision for the
  * substitute layers: "Low-Bit Shadow" report 5.1 point 2 and 10.1 (2), which
- * leave 2/3-bit substitutes untested; Critique (10), precision per layer by
+ * leave 2/3-bit substitutes untested; 10.2 (10), precision per layer by
  * sensitivity).  The same quantiser with L = 2^bits - 1 levels in place of 15:
  * s = bf16(fp32(hi-lo)/L) (1 if that is 0), z = bf16(fp32(-lo)/s),
  * q = clamp(rint_even(fp32(w/s) + z), 0, L), dequantised bf16((q - z) * s).

@@ -83,7 +83,7 @@ def w4_gemm(x, q, s, z, k: int) -> np.ndarray:
 # ---------------------------------------------------------------------------
 # 2-, 3- and 4-bit substitutes (lower and mixed precision for the draft's
 # substitute layers: "Low-Bit Shadow" report 5.1 point 2 and 10.1 (2), which
-# leave 2/3-bit substitutes untested, and Critique (10), per-layer precision
+# leave 2/3-bit substitutes untested, and 10.2 (10), per-layer precision
 # chosen by sensitivity).  The quantiser is the min-max one above with
 # L = 2^bits - 1 levels in place of 15:
 #   s = bf16(fp32(hi - lo) / L); if s == 0 then s = 1;  z = bf16(fp32(-lo) / s)

@@ -1,5 +1,5 @@
 """2- and 3-bit and per-layer mixed-precision substitutes on the device
-("Low-Bit Shadow" report 5.1 point 2, 10.1 (2); Critique (10)), and HQQ zero
+("Low-Bit Shadow" report 5.1 point 2, 10.1 (2), 10.2 (10)), and HQQ zero
 points (Critique 3, 6.2), against the oracle: packed codes, scales, zeros
 and dequantised values bit-exact; the GEMV and the wide product within the
 bf16 output rounding; draft logits of mixed-precision and HQQ models within
