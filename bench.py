@@ -81,13 +81,19 @@ WORKLOADS = {
 
 # ------------------------------------------------------------------ setup --
 def dist_setup():
+    """Rank, world size and local rank from the launcher's environment; with
+    more than one rank, a process group (NCCL on GPUs, gloo without them:
+    replicas exchange only their timings and counts, no data)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group("gloo")
     elif torch.cuda.is_available():
         torch.cuda.set_device(0)
     return world, rank, local
@@ -100,12 +106,22 @@ def barrier(world):
 
 
 def reduce(world, value, op):
+    """max or sum of one number over the ranks."""
     if world == 1:
         return value
     import torch.distributed as dist
-    t = torch.tensor([float(value)], device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
     return float(t.item())
+
+
+def aggregate(world, tokens, ms):
+    """Whole-job throughput of N replicas: every rank's tokens over the
+    slowest rank's time -> (tokens over all ranks, max ms, tokens/s)."""
+    ms_max = reduce(world, ms, "max")
+    tokens_all = reduce(world, tokens, "sum")
+    return tokens_all, ms_max, tokens_all / (ms_max / 1e3)
 
 
 def peaks():
@@ -601,9 +617,7 @@ def main():
     _, e1, c1 = model.decode_read()
     tokens = e1 - e0
     tau = tokens / args.steps
-    ms_max = reduce(world, ms, "max")
-    tokens_all = reduce(world, tokens, "sum")
-    value = tokens_all / (ms_max / 1e3)
+    tokens_all, ms_max, value = aggregate(world, tokens, ms)
 
     # clocks and throttle reasons over the e2e run and the sweeps as well
     clocks_sweeps = Clocks(gpu_index(local))
