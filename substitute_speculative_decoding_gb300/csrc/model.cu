@@ -921,8 +921,6 @@ static int32_t enqueue_cycle(sub_model* m, const sub_decode_cfg& c) {
   SUB_CUDA_TRY(mark(m->ev_cyc[0], m->s_main));
   SUB_TRY(begin_target_pass(m));
   // ---- draft ----
-  // one level: the draft forward over its rows, the expansion into the next
-  // level and, with adaptive depth, the decision to go on
   // With verify reuse the draft forward of a level is split at layer R =
   // n_resident: the new nodes' leading part (layers < R, the resident layers
   // the target shares) runs right after the expansion that made them and
@@ -952,6 +950,9 @@ static int32_t enqueue_cycle(sub_model* m, const sub_decode_cfg& c) {
     return forward(m, true, r, nullptr, false);
   };
   if (reuse) SUB_TRY(lead(0));
+  // one level: the draft forward over its rows, the expansion into the next
+  // level and, with adaptive depth, the decision to go on (next: the next
+  // level's conditional node when the cycle is captured)
   auto level = [&](int lvl, cudaGraphConditionalHandle next, int has_next) -> int32_t {
     const int M = lvl == 0 ? 1 : k;
     FwdRows r = rows_of(lvl);
