@@ -49,6 +49,13 @@ def test_bad_arguments_are_rejected_on_the_host(lib):
     assert s._kv_compact(C.byref(kv), 0, None, None, 4, None) == s.SUB_EINVAL
     cfg = s.DecodeCfg(4, 2, 0.2, 0, 1.0, 0, 0)
     assert s._generate(None, None, 0, 0, C.byref(cfg), None, None) == s.SUB_EINVAL
+    # 2/3/4-bit packing: the code width and the HQQ iteration count are checked first
+    assert s._wq_pack(None, 16, 64, 64, 5, None, None, None, None) == s.SUB_EINVAL
+    assert s._wq_pack(None, 16, 64, 64, 1, None, None, None, None) == s.SUB_EINVAL
+    assert s._wq_pack(None, 16, 64, 32, 2, None, None, None, None) == s.SUB_EUNSUPPORTED
+    assert s._wq_pack_hqq(None, 16, 64, 64, 3, 0, None, None, None, None) == s.SUB_EINVAL
+    assert s._wq_dequant(None, None, None, 16, 64, 64, 6, None, None) == s.SUB_EINVAL
+    assert s._wq_gemm(None, 1, None, None, None, 16, 64, 64, 2, None, None) == s.SUB_EINVAL
 
 
 def test_model_desc_validation(lib):
