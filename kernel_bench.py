@@ -16,6 +16,7 @@ than the 129 MB L2):
   gemv_{bf16,w4}_{down,o}  down projection 3584x18944 / o projection 3584x3584, M = 8
   w4_mix      the four int4 substitute matrices of one layer (o, gate, up, down)
               in turn, M = 8
+  wq_mix2, wq_mix3  the same with 2- or 3-bit substitutes (register-streamed GEMV)
   draft_level one draft forward of 8 tree nodes through the whole Qwen2.5-7B-shaped
               model (11 resident + 17 int4 layers, lm_head), inside the NVTX range
               "draft_level" (the second of two runs)
@@ -132,6 +133,22 @@ def main():
             sub.w4_gemm(xs[k], *packs[i % 4], n, k, out=ys[n])
         ms = _time(run, a.iters)
         byt = sum(n * ((k + 63) // 64) * 36 + 8 * (n + k) * 2 for n, k in shapes) / 4
+        res.update(ms=ms, gbs=byt / ms / 1e6, bytes_per_launch=byt)
+    elif a.case in ("wq_mix2", "wq_mix3"):
+        # the same four shapes with 2- or 3-bit substitutes (random bf16 weights
+        # packed on the device; 4 copies of each shape rotate past L2)
+        bits = 2 if a.case == "wq_mix2" else 3
+        shapes = [(3584, 3584), (18944, 3584), (18944, 3584), (3584, 18944)]
+        packs = [sub.wq_pack(synthetic.randn_bf16((n, k), 11 + 4 * i + r, 0.02, dev), bits)
+                 for i, (n, k) in enumerate(shapes) for r in range(4)]
+        xs = {k: torch.randn(8, k, device=dev).to(torch.bfloat16) for _, k in shapes}
+        ys = {n: torch.empty(8, n, device=dev, dtype=torch.bfloat16) for n, _ in shapes}
+
+        def run(i):
+            n, k = shapes[i % 4]
+            sub.wq_gemm(xs[k], *packs[(i % 4) * 4 + (i // 4) % 4], n, k, bits, out=ys[n])
+        ms = _time(run, a.iters)
+        byt = sum(n * ((k + 63) // 64) * (8 * bits + 4) + 8 * (n + k) * 2 for n, k in shapes) / 4
         res.update(ms=ms, gbs=byt / ms / 1e6, bytes_per_launch=byt)
     elif a.case in ("gemv_bf16", "gemm_bf16"):
         m = 8 if a.case == "gemv_bf16" else 385
