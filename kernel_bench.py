@@ -11,6 +11,7 @@ than the 129 MB L2):
   attn_verify 385 tree queries, same heads and keys
   attn32      the Qwen2.5-32B attention sweep (40/8 heads; 385 or 8 queries over 1k, 4k
               and 16k committed keys)
+  attn32_draft16k  its draft-shaped 16k-key point alone
   gemm_bf16   bf16 weights 18944x3584, M = 385 (a verify FFN matrix, tcgen05)
   gemm_w4     int4 weights 18944x3584, M = 385 (tcgen05 with the dequantising stage)
   gemv_{bf16,w4}_{down,o}  down projection 3584x18944 / o projection 3584x3584, M = 8
@@ -216,6 +217,29 @@ def main():
                 byt = kv_bytes + 4 * nq * hq * d
                 res[f"{tag}_kv{lkv}"] = dict(ms=round(ms, 5), gbs=round(byt / ms / 1e6, 1))
             del caches
+    elif a.case == "attn32_draft16k":
+        # one shape of that sweep alone, for a profiler capture: 8 draft
+        # queries of a depth-48 width-8 tree over 16384 committed keys
+        import math
+        hq, hkv, d, lkv = 40, 8, 128, 16384
+        tok, par, dep = synthetic.random_tree(48, 8, 3, 1000)
+        anc = synthetic.ancestors(par, dep, 48).to(dev)
+        dep = dep.to(dev)
+        n_tree = len(par)
+        kv_bytes = (lkv + n_tree) * hkv * d * 4
+        nc = max(2, math.ceil(4 * 129 * 2 ** 20 / kv_bytes))
+        caches = []
+        for _ in range(nc):
+            kv, keep = sub.make_kv(1, hkv, d, lkv + n_tree + 64)
+            keep[0].normal_()
+            keep[1].normal_()
+            caches.append((kv, keep))
+        q = torch.randn(8, hq, d, device=dev).to(torch.bfloat16)
+        an, dp = anc[-8:].contiguous(), dep[-8:].contiguous()
+        ms = _time(lambda i: sub.tree_attn(q, caches[i % nc][0], 0, lkv, lkv, n_tree, anc=an,
+                                           depth=dp), max(a.iters, nc))
+        byt = kv_bytes + 4 * 8 * hq * d
+        res.update(ms=ms, gbs=byt / ms / 1e6)
     elif a.case in ("draft_level", "verify_pass"):
         res.update(_model_pass(a.case))
     else:
