@@ -199,7 +199,18 @@ extern "C" int32_t sub_tree_attn(const sub_bf16* Q, int32_t n_q, int32_t n_heads
   SUB_CHECK_ARG(n_heads_q >= 1 && kv->n_heads_kv >= 1 && n_heads_q % kv->n_heads_kv == 0,
                 "Hq must be a multiple of Hkv");
   const cudaStream_t st = as_stream(stream);
-  const int splits = attn_pick_splits(a, (int)(n_prefix + n_slots));
+  const int splits = attn_pick_splits(a, (int)(n_prefix + n_slots), true);
+  StreamScratch scratch(st);
+  const size_t xf = attn_xpart_floats(a, splits), xc = attn_xcnt_count(a, splits);
+  if (xf) {   // two clusters per row block: their partials and counters
+    SUB_TRY(scratch.alloc(xf * 4 + xc * 4));
+    const size_t rows = xf / (a.head_dim + 2);
+    a.xpart = reinterpret_cast<float*>(scratch.p);
+    a.xm = a.xpart + rows * a.head_dim;
+    a.xl = a.xm + rows;
+    a.xcnt = reinterpret_cast<unsigned int*>(a.xl + rows);
+    SUB_CUDA_TRY(cudaMemsetAsync(a.xcnt, 0, xc * 4, st));
+  }
   return launch_tree_attn(a, splits, st);
 }
 

@@ -17,7 +17,10 @@
 // enters P V as a bf16 pair hi + lo, which keeps it to ~2^-17.  Keys
 // may be split over up to 16 CTAs (grid.z) that form one thread-block cluster;
 // their partial (max, sum, O) are merged in split order through distributed
-// shared memory, so no global scratch and no second launch are needed.
+// shared memory, so no global scratch and no second launch are needed.  Long
+// key ranges with few row blocks take 32 splits: two clusters, each merged as
+// above, whose partials meet in a small global scratch and are folded, in
+// cluster order, by the last CTA of each row slice to arrive.
 #include <mutex>
 #include <cooperative_groups.h>
 #include "attn_core.cuh"
@@ -84,7 +87,8 @@ __global__ void __launch_bounds__(THREADS) tree_attn_kernel(AttnArgs a) {
     }
   }
   cluster.sync();
-  const int S = (int)gridDim.z;
+  const int S = (int)cluster.dim_blocks().z;   // splits of this cluster
+  const int C = (int)gridDim.z / S;            // clusters of this row block (2-level merge if > 1)
   const int rank = (int)cluster.block_rank();
   const int rows_per = (ROWS + S - 1) / S;
   const int r_lo = rank * rows_per, r_hi = min(ROWS, r_lo + rows_per);
@@ -109,7 +113,18 @@ __global__ void __launch_bounds__(THREADS) tree_attn_kernel(AttnArgs a) {
   if (act)
     for (int t2 = 0; t2 < S; ++t2) den += sWl[mi * S + t2];   // in split order
   __syncthreads();
-  if (act) sWl[mi * S + ms2] = w_peer * (den > 0.f ? 1.f / den : 0.f);
+  // one cluster: normalised weights; several: this cluster's unnormalised
+  // partial, its max and its denominator go to the cross-cluster scratch
+  const size_t blk = (size_t)blockIdx.x * gridDim.y + blockIdx.y;
+  const int c_idx = (int)blockIdx.z / S;
+  if (act) sWl[mi * S + ms2] = C > 1 ? w_peer : w_peer * (den > 0.f ? 1.f / den : 0.f);
+  if (C > 1 && act && ms2 == 0) {
+    float mx = -INFINITY;
+    for (int t2 = 0; t2 < S; ++t2) mx = fmaxf(mx, sMl[mi * S + t2]);
+    const size_t xr = (blk * C + c_idx) * ROWS + r_lo + mi;
+    a.xm[xr] = mx;
+    a.xl[xr] = den;
+  }
   __syncthreads();
   for (int idx = tid; idx < (r_hi - r_lo) * (D / 4); idx += THREADS) {
     const int i = idx / (D / 4), c = (idx % (D / 4)) * 4;
@@ -132,9 +147,52 @@ __global__ void __launch_bounds__(THREADS) tree_attn_kernel(AttnArgs a) {
         v3 = fmaf(w, pv[s2].w, v3);
       }
     }
+    if (C > 1) {
+      __stcg(reinterpret_cast<float4*>(a.xpart + ((blk * C + c_idx) * ROWS + r) * D + c),
+             make_float4(v0, v1, v2, v3));
+      continue;
+    }
     const int q = gr / G, hh = gr % G;
     const size_t orow = (size_t)q * a.n_heads_q + kvh * G + hh;
     *reinterpret_cast<uint2*>(a.O + orow * D + c) = make_uint2(pack_bf16x2(v0, v1), pack_bf16x2(v2, v3));
+  }
+  if (C > 1) {
+    // the rank-r CTAs of the C clusters hold the same rows: the last of them
+    // to arrive merges the clusters' partials, in cluster order
+    __shared__ unsigned int s_last;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = atomicAdd(a.xcnt + blk * S + rank, 1u) == (unsigned)C - 1 ? 1u : 0u;
+    __syncthreads();
+    if (s_last) {
+      __threadfence();
+      for (int idx = tid; idx < (r_hi - r_lo) * (D / 4); idx += THREADS) {
+        const int i = idx / (D / 4), c = (idx % (D / 4)) * 4;
+        const int r = r_lo + i;
+        const int gr = row0 + r;
+        if (gr >= n_rows) continue;
+        float M = -INFINITY;
+        for (int cc = 0; cc < C; ++cc) M = fmaxf(M, __ldcg(a.xm + (blk * C + cc) * ROWS + r));
+        float L = 0.f, v0 = 0.f, v1 = 0.f, v2 = 0.f, v3 = 0.f;
+        for (int cc = 0; cc < C; ++cc) {
+          const size_t xr = (blk * C + cc) * ROWS + r;
+          const float mc = __ldcg(a.xm + xr);
+          const float wc = mc == -INFINITY ? 0.f : exp2f(mc - M);
+          const float4 p = __ldcg(reinterpret_cast<const float4*>(a.xpart + xr * D + c));
+          L = fmaf(wc, __ldcg(a.xl + xr), L);
+          v0 = fmaf(wc, p.x, v0);
+          v1 = fmaf(wc, p.y, v1);
+          v2 = fmaf(wc, p.z, v2);
+          v3 = fmaf(wc, p.w, v3);
+        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        const int q = gr / G, hh = gr % G;
+        const size_t orow = (size_t)q * a.n_heads_q + kvh * G + hh;
+        *reinterpret_cast<uint2*>(a.O + orow * D + c) =
+            make_uint2(pack_bf16x2(v0 * inv, v1 * inv), pack_bf16x2(v2 * inv, v3 * inv));
+      }
+      if (tid == 0) a.xcnt[blk * S + rank] = 0u;   // ready for the next launch
+    }
   }
   cluster.sync();   // peers may still be reading this CTA's shared memory
 }
@@ -153,14 +211,31 @@ static_assert(ROWS * (64 + 4) * 4 + 2 * ROWS * 4 + 2 * ROWS * ATTN_MAX_SPLIT * 4
 
 static int g_max_split = 8;   // largest cluster the device runs (set by attn_init)
 
-int attn_pick_splits(const AttnArgs& a, int n_keys_hint) {
+int attn_pick_splits(const AttnArgs& a, int n_keys_hint, bool two_level) {
   if (attn_init() != SUB_OK) return 1;
   const int G = a.n_heads_q / a.n_heads_kv;
   const int blocks = (a.n_q * G + ROWS - 1) / ROWS * a.n_heads_kv;
   const int tiles = (n_keys_hint + KT - 1) / KT;
   int s = (2 * 152 + blocks - 1) / blocks;
+  // past one cluster: four clusters of 8 per row block when the launch still
+  // fits two CTAs per SM and every split keeps four key tiles or more (at
+  // fewer keys the cross-cluster merge costs more than the added CTAs gain)
+  if (two_level && g_max_split == 16 && s >= 32 && tiles >= 128) return 32;
   s = std::max(1, std::min(s, std::min(tiles, g_max_split)));
   return s;
+}
+
+size_t attn_xpart_floats(const AttnArgs& a, int n_split) {
+  if (n_split <= ATTN_MAX_SPLIT) return 0;
+  const int G = a.n_heads_q / a.n_heads_kv;
+  const size_t blocks = (size_t)(a.n_q * G + ROWS - 1) / ROWS * a.n_heads_kv;
+  const size_t C = (size_t)n_split / ATTN_XCLUSTER;
+  return blocks * C * ROWS * (a.head_dim + 2);
+}
+size_t attn_xcnt_count(const AttnArgs& a, int n_split) {
+  if (n_split <= ATTN_MAX_SPLIT) return 0;
+  const int G = a.n_heads_q / a.n_heads_kv;
+  return (size_t)(a.n_q * G + ROWS - 1) / ROWS * a.n_heads_kv * ATTN_XCLUSTER;
 }
 
 // Opt the kernels into the largest dynamic shared memory and into 16-CTA
@@ -205,7 +280,10 @@ int32_t launch_tree_attn(const AttnArgs& a, int n_split, cudaStream_t st) {
   SUB_CHECK_ARG(a.page_size % 16 == 0 && a.page_size > 0, "attn: page_size % 16 != 0");
   SUB_CHECK_ARG(a.n_slots >= 0 && a.n_slots <= 16384, "attn: n_slots out of range");
   SUB_TRY(attn_init());
-  SUB_CHECK_ARG(n_split >= 1 && n_split <= g_max_split, "attn: bad split count");
+  SUB_CHECK_ARG((n_split >= 1 && n_split <= g_max_split) ||
+                    (g_max_split == ATTN_MAX_SPLIT && n_split % ATTN_XCLUSTER == 0 &&
+                     a.xpart && a.xm && a.xl && a.xcnt),
+                "attn: bad split count");
   if (a.n_q == 0) return SUB_OK;
   const int G = a.n_heads_q / a.n_heads_kv;
   const int smem = attn_smem_bytes(a);
@@ -222,7 +300,7 @@ int32_t launch_tree_attn(const AttnArgs& a, int n_split, cudaStream_t st) {
     attr[na].id = cudaLaunchAttributeClusterDimension;
     attr[na].val.clusterDim.x = 1;
     attr[na].val.clusterDim.y = 1;
-    attr[na].val.clusterDim.z = n_split;
+    attr[na].val.clusterDim.z = n_split > ATTN_MAX_SPLIT ? ATTN_XCLUSTER : n_split;
     ++na;
   }
   if (pdl_enabled()) {

@@ -67,6 +67,11 @@ struct sub_model {
   // activations
   float* x = nullptr;        // [rows, H]
   float* xsave = nullptr;    // [tree slots, H]: residual stream at layer n_resident (verify reuse)
+  // draft attention over long key ranges (32 key splits): cross-cluster
+  // partials and counters, sized for the draft's widest level
+  float* attn_x = nullptr;
+  size_t attn_x_floats = 0;
+  unsigned int* attn_xcnt = nullptr;
   uint16_t* xn = nullptr;    // [rows, H]
   float* qkv = nullptr;      // [rows, qkv_dim]
   uint16_t* q = nullptr;     // [rows, Hq*D]
@@ -400,7 +405,15 @@ static int32_t forward(sub_model* m, bool draft, const FwdRows& r, float* logits
   at.chain_slot0 = r.slot0;
   at.scale = 1.0f / sqrtf((float)D);
   at.early_reads = 1;   // predecessors signal only after their own wait
-  const int splits = attn_pick_splits(at, (int)std::min<int64_t>(r.keys_hint, 1 << 30));
+  const bool two_level = m->attn_x && attn_xpart_floats(at, 32) <= m->attn_x_floats;
+  const int splits = attn_pick_splits(at, (int)std::min<int64_t>(r.keys_hint, 1 << 30), two_level);
+  if (splits > ATTN_MAX_SPLIT) {
+    const size_t rows = attn_xpart_floats(at, splits) / (D + 2);
+    at.xpart = m->attn_x;
+    at.xm = m->attn_x + rows * D;
+    at.xl = at.xm + rows;
+    at.xcnt = m->attn_xcnt;
+  }
 
   QkvPostArgs qp{};
   qp.qkv = m->qkv;
@@ -706,6 +719,18 @@ extern "C" int32_t sub_model_create(const sub_model_desc* desc, sub_model** out)
     const size_t n_tree = 1 + (size_t)d.max_depth * d.max_width;
     CREATE_TRY(dalloc_t(m, &m->xsave, n_tree * H));
     CREATE_CUDA(cudaMemset(m->xsave, 0, n_tree * H * 4));
+  }
+  {
+    AttnArgs w{};   // the draft's widest level, for 32-split attention
+    w.n_q = std::max(d.max_width, 1);
+    w.n_heads_q = d.n_heads_q;
+    w.n_heads_kv = d.n_heads_kv;
+    w.head_dim = D;
+    m->attn_x_floats = attn_xpart_floats(w, 2 * ATTN_MAX_SPLIT);
+    const size_t nc = attn_xcnt_count(w, 2 * ATTN_MAX_SPLIT);
+    CREATE_TRY(dalloc_t(m, &m->attn_x, m->attn_x_floats));
+    CREATE_TRY(dalloc_t(m, &m->attn_xcnt, nc));
+    CREATE_CUDA(cudaMemset(m->attn_xcnt, 0, nc * 4));
   }
   CREATE_TRY(dalloc_t(m, &m->xn, R * H));
   CREATE_TRY(dalloc_t(m, &m->qkv, R * m->qkv_dim));
