@@ -18,9 +18,9 @@
 // may be split over up to 16 CTAs (grid.z) that form one thread-block cluster;
 // their partial (max, sum, O) are merged in split order through distributed
 // shared memory, so no global scratch and no second launch are needed.  Long
-// key ranges with few row blocks take 32 splits: two clusters, each merged as
-// above, whose partials meet in a small global scratch and are folded, in
-// cluster order, by the last CTA of each row slice to arrive.
+// key ranges with few row blocks take 32 splits: four clusters of 8, each
+// merged as above, whose partials meet in a small global scratch and are
+// folded, in cluster order, by the last CTA of each row slice to arrive.
 #include <mutex>
 #include <cooperative_groups.h>
 #include "attn_core.cuh"
