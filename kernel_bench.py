@@ -17,7 +17,7 @@ than the 129 MB L2):
   gemv_{bf16,w4}_{down,o}  down projection 3584x18944 / o projection 3584x3584, M = 8
   w4_mix      the four int4 substitute matrices of one layer (o, gate, up, down)
               in turn, M = 8
-  wq_mix2, wq_mix3  the same with 2- or 3-bit substitutes (register-streamed GEMV)
+  wq_mix2, wq_mix3  the same with 2- or 3-bit substitutes
   draft_level one draft forward of 8 tree nodes through the whole Qwen2.5-7B-shaped
               model (11 resident + 17 int4 layers, lm_head), inside the NVTX range
               "draft_level" (the second of two runs)

@@ -76,23 +76,6 @@ __host__ __device__ inline int split_units(int K, int ks) {
   return ((total + ks - 1) / ks + U - 1) / U * U;
 }
 
-// Codes of 2- and 3-bit substitutes spread into the int4 word layout (code i
-// of a lane's run of 8 at bits 4i .. 4i+3), so one unpack serves all widths.
-// spread2: eight 2-bit fields at stride 2 -> stride 4 (bit interleave by
-// shift-or-mask); spread1: eight bits at stride 1 -> stride 4.
-__device__ __forceinline__ uint32_t spread2(uint32_t v) {
-  v &= 0xffffu;
-  v = (v | (v << 8)) & 0x00ff00ffu;
-  v = (v | (v << 4)) & 0x0f0f0f0fu;
-  return (v | (v << 2)) & 0x33333333u;
-}
-__device__ __forceinline__ uint32_t spread1(uint32_t v) {
-  v &= 0xffu;
-  v = (v | (v << 12)) & 0x000f000fu;
-  v = (v | (v << 6)) & 0x03030303u;
-  return (v | (v << 3)) & 0x11111111u;
-}
-
 // One lane's 16 codes of group gi (elements 16 * tig .. 16 * tig + 15 of the
 // group) as two int4-layout words; row points at the row's first group.
 template <int QB>
@@ -603,11 +586,11 @@ int32_t launch_gemv(const GemvArgs& a, bool is_w4, int epi, cudaStream_t st) {
   const int bits = code_bits(a);
   SUB_CHECK_ARG(!is_w4 || bits == 2 || bits == 3 || bits == 4, "gemv: code bits must be 2, 3 or 4");
   if (!is_w4) return launch_bf16_or_tma(a, epi, st);
-  if (bits == 2) return launch_epi<true, 2>(a, epi, st);
-  if (bits == 3) return launch_epi<true, 3>(a, epi, st);
   bool done = false;
   SUB_TRY(launch_gemv_tma(a, true, epi, st, &done));
   if (done) return SUB_OK;
+  if (bits == 2) return launch_epi<true, 2>(a, epi, st);
+  if (bits == 3) return launch_epi<true, 3>(a, epi, st);
   return launch_epi<true, 4>(a, epi, st);
 }
 

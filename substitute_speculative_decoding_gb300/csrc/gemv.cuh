@@ -129,12 +129,29 @@ struct GemvArgs {
   int bits;              // quantised weights: code bits 2, 3 or 4 (0 means 4)
 };
 
+// Codes of 2- and 3-bit substitutes spread into the int4 word layout (code i
+// of a lane's run of 8 at bits 4i .. 4i+3), so one unpack serves all widths.
+// spread2: eight 2-bit fields at stride 2 -> stride 4 (bit interleave by
+// shift-or-mask); spread1: eight bits at stride 1 -> stride 4.
+__device__ __forceinline__ uint32_t spread2(uint32_t v) {
+  v &= 0xffffu;
+  v = (v | (v << 8)) & 0x00ff00ffu;
+  v = (v | (v << 4)) & 0x0f0f0f0fu;
+  return (v | (v << 2)) & 0x33333333u;
+}
+__device__ __forceinline__ uint32_t spread1(uint32_t v) {
+  v &= 0xffu;
+  v = (v | (v << 12)) & 0x000f000fu;
+  v = (v | (v << 6)) & 0x03030303u;
+  return (v | (v << 3)) & 0x11111111u;
+}
+
 // Code bits of a quantised product (0 in GemvArgs means 4).
 inline int code_bits(const GemvArgs& a) { return a.bits ? a.bits : 4; }
 
 // Launch: quantised (is_w4; a.bits code bits) or bf16 weights, epilogue, M <= 16.
-// 2- and 3-bit codes run the register-streamed kernel; 4-bit codes and bf16
-// weights take the TMA variant when it fits.
+// Quantised codes of every width and bf16 weights take the TMA variant when
+// it fits, else the register-streamed kernel.
 int32_t launch_gemv(const GemvArgs& a, bool is_w4, int epi, cudaStream_t stream);
 // Row units (CTAs along grid.x) a launch uses; NormOut::partial holds 16 floats per unit.
 int gemv_grid(const GemvArgs& a, int epi);
@@ -146,7 +163,7 @@ int gemv_ksplit(const GemvArgs& a, bool is_w4, int epi);
 // one CTA per SM with the (block, K-stage) units split evenly.  Launches and
 // sets *done when the shape and the split scratch allow it; otherwise leaves
 // *done false and launches nothing.  launch_gemv tries it first
-// (SUB_GEMV_TMA=0 turns it off).
+// (SUB_GEMV_TMA=0 turns it off).  Quantised codes (is_w4) are code_bits(a) wide.
 int32_t launch_gemv_tma(const GemvArgs& a, bool is_w4, int epi, cudaStream_t stream, bool* done);
 // Partial-sum floats the TMA variant needs in split_part (0: it would not run).
 size_t gemv_tma_scratch_floats(const GemvArgs& a, bool is_w4, int epi);
@@ -156,10 +173,11 @@ int32_t gemv_init();
 int32_t gemv_tma_timeouts(unsigned int* out);
 // The CUDA driver API's tensor-map encoder (null if unavailable), and a 2-D tiled map
 // over a row-major [rows, cols] array with the given row stride and box
-// (128-byte swizzle when swz); false when the encoder or the alignment refuses.
+// (swz: 0 for no swizzle, 64 or 128 for that swizzle span in bytes); false
+// when the encoder or the alignment refuses.
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn();
 bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* ptr, int64_t cols,
-              int64_t rows, int64_t stride_bytes, int box_cols, int box_rows, bool swz);
+              int64_t rows, int64_t stride_bytes, int box_cols, int box_rows, int swz);
 // One bounded wait on an mbarrier nothing arrives on; *polls = polls made
 // before it was satisfied, 0 when it gave up after `limit` polls.
 int32_t bounded_wait_selftest(uint32_t limit, uint32_t* polls);

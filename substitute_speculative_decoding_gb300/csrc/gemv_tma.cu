@@ -2,8 +2,8 @@
 // by the Tensor Memory Accelerator.
 //
 // Y[m, n] = sum_k X[m, k] W[n, k], the same products and epilogues as the
-// register-streamed kernel in gemv.cu, for bf16 weights or int4 substitutes
-// (W = (q - z) * s per 64-column group).  A small M leaves the product bound
+// register-streamed kernel in gemv.cu, for bf16 weights or 4-, 3- or 2-bit
+// substitutes (W = (q - z) * s per 64-column group).  A small M leaves the product bound
 // by the weight stream, and the number of weight bytes in flight per SM is
 // what decides the bandwidth reached.  Here the bytes in flight live in a
 // shared-memory ring instead of registers:
@@ -15,6 +15,10 @@
 //   * eight consumer warps each own a 16-row tile of the block and run
 //     mma.sync m16n8k16 (swap-AB: W is the A operand, X the B operand)
 //     straight from the swizzled stages, then release the stage;
+//   * 2- and 3-bit codes take the same path: a stage's 8 groups are 128
+//     bytes of a row (2-bit) or 192 (3-bit: a 128-byte box and a 64-byte
+//     one with the 64-byte swizzle), and each lane spreads its 16 codes into
+//     the int4 word layout before the common unpack;
 //   * with int4 weights two more warps (even and odd groups) form each
 //     stage's per-group activation sums Sx (an mma with an all-ones A
 //     operand) and, for one token tile, the activation B fragments in lane
@@ -70,12 +74,49 @@ __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(NCW * 32) : "memory");
 }
 
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t r;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r) : "r"(a));
+  return r;
+}
+__device__ __forceinline__ uint32_t lds16(uint32_t a) {
+  unsigned short r;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(r) : "r"(a));
+  return r;
+}
+
+// Shared address of byte `off` of smem row r of a stage's 2/3-bit codes:
+// bytes 0..127 in the 128-byte-swizzled box (16-byte chunk c of row r at
+// c ^ (r & 7)), bytes 128..191 in the 64-byte-swizzled box (chunk c of its
+// 64-byte row r at c ^ ((r >> 1) & 3)).
+__device__ __forceinline__ uint32_t code_addr(uint32_t box128, uint32_t box64, int r, int off) {
+  return off < 128 ? box128 + r * 128 + ((((off >> 4) ^ r) & 7) << 4) + (off & 15)
+                   : box64 + r * 64 + (((((off - 128) >> 4) ^ (r >> 1)) & 3) << 4) + (off & 15);
+}
+
+// One lane's 16 codes of stage group gs (elements 16 tig .. 16 tig + 15 of
+// the group) from smem row r, in the int4 word layout (the same words the
+// register-streamed kernel forms from global memory).
+template <int QB>
+__device__ __forceinline__ uint2 stage_codes(uint32_t box128, uint32_t box64, int r, int gs, int tig) {
+  const int g0 = gs * 8 * QB;
+  const uint32_t w = lds32(code_addr(box128, box64, r, g0 + tig * 4));
+  uint2 q = make_uint2(spread2(w), spread2(w >> 16));
+  if constexpr (QB == 3) {
+    const uint32_t h = lds16(code_addr(box128, box64, r, g0 + 16 + tig * 2));
+    q.x |= spread1(h) << 2;
+    q.y |= spread1(h >> 8) << 2;
+  }
+  return q;
+}
+
 }  // namespace
 
 struct alignas(64) TmaMaps {
   CUtensorMap w[3];   // bf16 weights, or packed int4 codes, per segment
   CUtensorMap s[3];   // int4 scales per segment
   CUtensorMap z[3];   // int4 zeros per segment
+  CUtensorMap w64[3]; // 3-bit codes: bytes 128..191 of a stage's 192 per row
   CUtensorMap x;      // activations [M, K] viewed as [K/64][M][64]: one box per stage
 };
 
@@ -88,16 +129,20 @@ struct TmaPlan {
   int n_maps;         // weight segments with a tensor map
 };
 
-template <bool W4, int MT>
+template <bool W4, int MT, int QB = 4>
 struct TmaGeom {
   static constexpr int KC = W4 ? 512 : 128;              // K columns per stage
-  static constexpr int WBOXES = W4 ? 2 : 2;              // weight boxes per stage (128 B wide)
+  // weight boxes per stage, 128 B wide: bf16 and 4-bit two, 2-bit one, 3-bit
+  // one plus a 64-byte box (W64)
+  static constexpr int WBOXES = W4 && QB < 4 ? 1 : 2;
   static constexpr int WBOX = BR * 128;                  // bytes of one weight box (all rows)
+  static constexpr int W64 = W4 && QB == 3 ? BR * 64 : 0;
   static constexpr int SZBOX = W4 ? BR * 16 : 0;         // scales (or zeros) of 8 groups
   static constexpr int XBOXES = KC / 64;                 // activation boxes (64 columns each)
   static constexpr int XBOX = MT * 8 * 128;              // bytes of one activation box
   static constexpr int W_OFF = 0;
-  static constexpr int S_OFF = WBOXES * WBOX;
+  static constexpr int W64_OFF = WBOXES * WBOX;          // 1024-byte aligned (swizzle span)
+  static constexpr int S_OFF = W64_OFF + W64;
   static constexpr int Z_OFF = S_OFF + SZBOX;
   static constexpr int X_OFF = (Z_OFF + SZBOX + 1023) / 1024 * 1024;
   static constexpr int SX_OFF = X_OFF + XBOXES * XBOX;   // int4: Sx [8 groups][MT * 8 tokens] fp32
@@ -108,7 +153,7 @@ struct TmaGeom {
   static constexpr int XF_OFF = SX_OFF + SXB;
   static constexpr int XFB = XFRAG ? 8 * 2 * 32 * 16 : 0;
   static constexpr int STAGE = (XF_OFF + XFB + 1023) / 1024 * 1024;
-  static constexpr int TX = WBOXES * WBOX + 2 * SZBOX + XBOXES * XBOX;   // bytes per stage
+  static constexpr int TX = WBOXES * WBOX + W64 + 2 * SZBOX + XBOXES * XBOX;   // bytes per stage
   static constexpr int EPI_FLOATS = 4 * MT * 128 + NCW * 16 + 32;   // + flag, row scales
   // alignment slack, ring, barriers and epilogue buffers within the limit
   static constexpr int STAGES =
@@ -117,10 +162,10 @@ struct TmaGeom {
   static_assert(STAGES >= 3 && SMEM <= SMEM_LIMIT, "TMA GEMV ring does not fit");
 };
 
-template <bool W4, int MT, int EPI>
+template <bool W4, int MT, int EPI, int QB = 4>
 __global__ void __launch_bounds__(W4 ? NTHR_W4 : NTHR, 1)
 gemv_tma_kernel(const __grid_constant__ TmaMaps maps, const GemvArgs a, const TmaPlan pl) {
-  using Geo = TmaGeom<W4, MT>;
+  using Geo = TmaGeom<W4, MT, QB>;
   constexpr int S = Geo::STAGES;
   constexpr bool GLU = EPI == EPI_GLU;
   extern __shared__ uint8_t smem_raw[];
@@ -140,6 +185,7 @@ gemv_tma_kernel(const __grid_constant__ TmaMaps maps, const GemvArgs a, const Tm
   if (warp == NCW && lane == 0) {   // descriptors into the TMA unit's cache early
     for (int t = 0; t < pl.n_maps; ++t) {
       tma_prefetch_desc(&maps.w[t]);
+      if (W4 && QB == 3) tma_prefetch_desc(&maps.w64[t]);
       if (W4) {
         tma_prefetch_desc(&maps.s[t]);
         tma_prefetch_desc(&maps.z[t]);
@@ -181,8 +227,16 @@ gemv_tma_kernel(const __grid_constant__ TmaMaps maps, const GemvArgs a, const Tm
             for (int h = 0; h < (GLU ? 2 : 1); ++h) {
               const int sg = GLU ? h : seg, rows = GLU ? BR / 2 : BR;
               const uint32_t ro = h * rows * 128;       // row offset inside a box (bytes)
-              for (int j = 0; j < Geo::WBOXES; ++j)
-                tma_load_2d(st + Geo::W_OFF + j * Geo::WBOX + ro, &maps.w[sg], (gx + 4 * j) * 32, r0, fb);
+              if constexpr (QB == 4) {
+                for (int j = 0; j < Geo::WBOXES; ++j)
+                  tma_load_2d(st + Geo::W_OFF + j * Geo::WBOX + ro, &maps.w[sg], (gx + 4 * j) * 32, r0, fb);
+              } else {
+                // the stage's 8 groups of 8 QB bytes: 128 bytes (2-bit), or
+                // 128 + 64 bytes (3-bit); x in bytes, a multiple of 16
+                tma_load_2d(st + Geo::W_OFF + ro, &maps.w[sg], gx * 8 * QB, r0, fb);
+                if constexpr (QB == 3)
+                  tma_load_2d(st + Geo::W64_OFF + h * rows * 64, &maps.w64[sg], gx * 24 + 128, r0, fb);
+              }
               tma_load_2d(st + Geo::S_OFF + h * rows * 16, &maps.s[sg], gx, r0, fb);
               tma_load_2d(st + Geo::Z_OFF + h * rows * 16, &maps.z[sg], gx, r0, fb);
             }
@@ -347,11 +401,17 @@ gemv_tma_kernel(const __grid_constant__ TmaMaps maps, const GemvArgs a, const Tm
       const uint32_t zw0[4] = {zv0.x, zv0.y, zv0.z, zv0.w}, zw1[4] = {zv1.x, zv1.y, zv1.z, zv1.w};
 #pragma unroll
       for (int gs = 0; gs < 8; ++gs) {
-        const int j = gs >> 2, gq = gs & 3;
-        const uint32_t qb = st + Geo::W_OFF + j * Geo::WBOX;
-        const uint32_t qo = (uint32_t)((((2 * gq + (tig >> 1)) ^ pg) << 4) + (tig & 1) * 8);
-        const uint2 q0 = lds64(qb + r0s * 128 + qo);
-        const uint2 q1 = lds64(qb + r1s * 128 + qo);
+        uint2 q0, q1;
+        if constexpr (QB == 4) {
+          const int j = gs >> 2, gq = gs & 3;
+          const uint32_t qb = st + Geo::W_OFF + j * Geo::WBOX;
+          const uint32_t qo = (uint32_t)((((2 * gq + (tig >> 1)) ^ pg) << 4) + (tig & 1) * 8);
+          q0 = lds64(qb + r0s * 128 + qo);
+          q1 = lds64(qb + r1s * 128 + qo);
+        } else {
+          q0 = stage_codes<QB>(st + Geo::W_OFF, st + Geo::W64_OFF, r0s, gs, tig);
+          q1 = stage_codes<QB>(st + Geo::W_OFF, st + Geo::W64_OFF, r1s, gs, tig);
+        }
         const uint32_t xbox = st + Geo::X_OFF + gs * Geo::XBOX;
         uint32_t bfr[MT][4][2];
         float sx[MT][2];
@@ -623,7 +683,7 @@ gemv_tma_kernel(const __grid_constant__ TmaMaps maps, const GemvArgs a, const Tm
 
 // ------------------------------------------------------------------- host --
 namespace {
-template <bool W4, int MT>
+template <bool W4, int MT, int QB = 4>
 cudaError_t tma_attr_all();
 }  // namespace
 
@@ -634,8 +694,10 @@ int32_t gemv_init() {
   static std::once_flag once;
   static cudaError_t err = cudaSuccess;
   std::call_once(once, [] {
-    const cudaError_t e[4] = {tma_attr_all<false, 1>(), tma_attr_all<false, 2>(),
-                              tma_attr_all<true, 1>(), tma_attr_all<true, 2>()};
+    const cudaError_t e[8] = {tma_attr_all<false, 1>(),   tma_attr_all<false, 2>(),
+                              tma_attr_all<true, 1>(),    tma_attr_all<true, 2>(),
+                              tma_attr_all<true, 1, 2>(), tma_attr_all<true, 2, 2>(),
+                              tma_attr_all<true, 1, 3>(), tma_attr_all<true, 2, 3>()};
     for (cudaError_t x : e)
       if (x != cudaSuccess && err == cudaSuccess) err = x;
   });
@@ -659,7 +721,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // 2-D map over a row-major [rows, cols] array with the given row stride.
 bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* ptr, int64_t cols,
-              int64_t rows, int64_t stride_bytes, int box_cols, int box_rows, bool swz) {
+              int64_t rows, int64_t stride_bytes, int box_cols, int box_rows, int swz) {
   auto fn = encode_fn();
   if (!fn || !aligned16(ptr) || stride_bytes % 16 || (int64_t)box_cols * esize % 16) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
@@ -667,45 +729,47 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* ptr
   const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
   const cuuint32_t es[2] = {1, 1};
   return fn(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            swz == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                       : swz == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 namespace {
 
-template <bool W4, int MT, int EPI>
+template <bool W4, int MT, int EPI, int QB>
 cudaError_t tma_attr() {
-  return cudaFuncSetAttribute(gemv_tma_kernel<W4, MT, EPI>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, TmaGeom<W4, MT>::SMEM);
+  return cudaFuncSetAttribute(gemv_tma_kernel<W4, MT, EPI, QB>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              TmaGeom<W4, MT, QB>::SMEM);
 }
-template <bool W4, int MT>
+template <bool W4, int MT, int QB>
 cudaError_t tma_attr_all() {
-  const cudaError_t e[5] = {tma_attr<W4, MT, EPI_BF16>(), tma_attr<W4, MT, EPI_F32>(),
-                            tma_attr<W4, MT, EPI_RESID>(), tma_attr<W4, MT, EPI_GLU>(),
-                            tma_attr<W4, MT, EPI_QKV>()};
+  const cudaError_t e[5] = {tma_attr<W4, MT, EPI_BF16, QB>(), tma_attr<W4, MT, EPI_F32, QB>(),
+                            tma_attr<W4, MT, EPI_RESID, QB>(), tma_attr<W4, MT, EPI_GLU, QB>(),
+                            tma_attr<W4, MT, EPI_QKV, QB>()};
   for (cudaError_t x : e)
     if (x != cudaSuccess) return x;
   return cudaSuccess;
 }
 
-template <bool W4, int MT, int EPI>
+template <bool W4, int MT, int EPI, int QB>
 int32_t tma_launch(const GemvArgs& a, const TmaMaps& maps, const TmaPlan& pl, int grid,
                    cudaStream_t st) {
   SUB_TRY(gemv_init());
-  SUB_CUDA_TRY(launch_k(gemv_tma_kernel<W4, MT, EPI>, dim3(grid), dim3(W4 ? NTHR_W4 : NTHR),
-                        TmaGeom<W4, MT>::SMEM, st, maps, a, pl));
+  SUB_CUDA_TRY(launch_k(gemv_tma_kernel<W4, MT, EPI, QB>, dim3(grid), dim3(W4 ? NTHR_W4 : NTHR),
+                        TmaGeom<W4, MT, QB>::SMEM, st, maps, a, pl));
   return SUB_OK;
 }
 
-template <bool W4, int MT>
+template <bool W4, int MT, int QB = 4>
 int32_t tma_epi(const GemvArgs& a, int epi, const TmaMaps& maps, const TmaPlan& pl, int grid,
                 cudaStream_t st) {
   switch (epi) {
-    case EPI_BF16: return tma_launch<W4, MT, EPI_BF16>(a, maps, pl, grid, st);
-    case EPI_F32: return tma_launch<W4, MT, EPI_F32>(a, maps, pl, grid, st);
-    case EPI_RESID: return tma_launch<W4, MT, EPI_RESID>(a, maps, pl, grid, st);
-    case EPI_GLU: return tma_launch<W4, MT, EPI_GLU>(a, maps, pl, grid, st);
-    case EPI_QKV: return tma_launch<W4, MT, EPI_QKV>(a, maps, pl, grid, st);
+    case EPI_BF16: return tma_launch<W4, MT, EPI_BF16, QB>(a, maps, pl, grid, st);
+    case EPI_F32: return tma_launch<W4, MT, EPI_F32, QB>(a, maps, pl, grid, st);
+    case EPI_RESID: return tma_launch<W4, MT, EPI_RESID, QB>(a, maps, pl, grid, st);
+    case EPI_GLU: return tma_launch<W4, MT, EPI_GLU, QB>(a, maps, pl, grid, st);
+    case EPI_QKV: return tma_launch<W4, MT, EPI_QKV, QB>(a, maps, pl, grid, st);
   }
   return fail(SUB_EINVAL, "bad gemv epilogue");
 }
@@ -768,21 +832,28 @@ int32_t launch_gemv_tma(const GemvArgs& a, bool w4, int epi, cudaStream_t st, bo
   const int mt = a.M <= 8 ? 1 : 2;
   const int box_rows = glu ? BR / 2 : BR;
   const int G = (a.K + 63) / 64;
+  const int bits = w4 ? code_bits(a) : 16;
+  if (w4 && bits != 2 && bits != 3 && bits != 4) return SUB_OK;
   TmaMaps maps;
   memset(&maps, 0, sizeof(maps));
   for (int s = 0; s < (glu ? 2 : a.n_seg); ++s) {
     const int64_t rows = glu ? a.N : a.seg_end[s] - (s ? a.seg_end[s - 1] : 0);
     bool ok;
     if (w4) {
-      ok = make_map(&maps.w[s], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.W[s], (int64_t)G * 32, rows,
-                    (int64_t)G * 32, 128, box_rows, true) &&
+      // codes: G groups of 8 * bits bytes per row; 3-bit rows also get the
+      // 64-byte box over the same bytes
+      const int64_t cb = (int64_t)G * 8 * bits;
+      ok = make_map(&maps.w[s], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.W[s], cb, rows, cb, 128,
+                    box_rows, 128) &&
+           (bits != 3 || make_map(&maps.w64[s], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.W[s], cb, rows,
+                                  cb, 64, box_rows, 64)) &&
            make_map(&maps.s[s], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.S[s], G, rows,
-                    (int64_t)G * 2, 8, box_rows, false) &&
+                    (int64_t)G * 2, 8, box_rows, 0) &&
            make_map(&maps.z[s], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.Z[s], G, rows,
-                    (int64_t)G * 2, 8, box_rows, false);
+                    (int64_t)G * 2, 8, box_rows, 0);
     } else {
       ok = make_map(&maps.w[s], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.W[s], a.K, rows,
-                    (int64_t)a.K * 2, 64, box_rows, true);
+                    (int64_t)a.K * 2, 64, box_rows, 128);
     }
     if (!ok) return SUB_OK;
   }
@@ -802,6 +873,10 @@ int32_t launch_gemv_tma(const GemvArgs& a, bool w4, int epi, cudaStream_t st, bo
       return SUB_OK;
   }
   *done = true;
+  if (w4 && bits == 2) return mt == 1 ? tma_epi<true, 1, 2>(a, epi, maps, pl, grid, st)
+                                      : tma_epi<true, 2, 2>(a, epi, maps, pl, grid, st);
+  if (w4 && bits == 3) return mt == 1 ? tma_epi<true, 1, 3>(a, epi, maps, pl, grid, st)
+                                      : tma_epi<true, 2, 3>(a, epi, maps, pl, grid, st);
   if (w4) return mt == 1 ? tma_epi<true, 1>(a, epi, maps, pl, grid, st)
                          : tma_epi<true, 2>(a, epi, maps, pl, grid, st);
   return mt == 1 ? tma_epi<false, 1>(a, epi, maps, pl, grid, st)

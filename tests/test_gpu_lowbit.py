@@ -65,10 +65,12 @@ def test_wq_gemm(sub, bits, m, n, k):
 
 
 @pytest.mark.parametrize("bits", [2, 3])
-def test_wq_gemm_identity_is_exact_dequant(sub, bits):
+@pytest.mark.parametrize("k", [256, 1024])
+def test_wq_gemm_identity_is_exact_dequant(sub, bits, k):
     """Identity rows through the GEMV give s (q - z) in fp32, rounded once to
-    bf16 on output: the dequantised values exactly."""
-    k = 256
+    bf16 on output: the dequantised values exactly (K = 256: the
+    register-streamed kernel; K = 1024, whole stages of 8 groups: the
+    TMA-streamed one)."""
     w = synthetic.randn_bf16((64, k), 5 + bits, std=0.02)
     q, s, z = sub.wq_pack(w.to(DEV), bits)
     deq = sub.wq_dequant(q, s, z, k, bits)
