@@ -361,7 +361,8 @@ def kernel_measurements(sub, cfg, weights, model, pk, dev, quick):
         low[f"bits{bits}"] = dict(ms_per_launch=round(msb, 5), bytes_per_launch=int(bb),
                                   gbs=round(bb / (msb / 1e3) / 1e9, 1),
                                   frac_hbm=round(bb / (msb / 1e3) / 1e9 / pk["hbm"], 3),
-                                  kernel="gemv_tma_kernel" if bits == 4 else "gemv_kernel")
+                                  kernel="gemv_tma_kernel" if all(k % 512 == 0 for *_, k in mats_b)
+                                  else "gemv_kernel (K not a multiple of 512)")
         del mats_b, xb, yb
     out["wq_gemv_m8"] = low
     # --- substitute construction: min-max and HQQ (20 iterations) packing of
