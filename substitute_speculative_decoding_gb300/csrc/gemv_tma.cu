@@ -17,8 +17,9 @@
 //     straight from the swizzled stages, then release the stage;
 //   * 2- and 3-bit codes take the same path: a stage's 8 groups are 128
 //     bytes of a row (2-bit) or 192 (3-bit: a 128-byte box and a 64-byte
-//     one with the 64-byte swizzle), and each lane spreads its 16 codes into
-//     the int4 word layout before the common unpack;
+//     one with the 64-byte swizzle); 2-bit codes go straight to the operand
+//     pairs after one byte permute per word, 3-bit codes are first spread
+//     into the int4 word layout;
 //   * with int4 weights two more warps (even and odd groups) form each
 //     stage's per-group activation sums Sx (an mma with an all-ones A
 //     operand) and, for one token tile, the activation B fragments in lane
@@ -401,6 +402,8 @@ gemv_tma_kernel(const __grid_constant__ TmaMaps maps, const GemvArgs a, const Tm
       const uint32_t zw0[4] = {zv0.x, zv0.y, zv0.z, zv0.w}, zw1[4] = {zv1.x, zv1.y, zv1.z, zv1.w};
 #pragma unroll
       for (int gs = 0; gs < 8; ++gs) {
+        // int4 layout words (code i of a run of 8 at bits 4i), or at 2 bits
+        // byte pairs (codes i and i + 4 of a run of 8 at bits 2i and 16 + 2i)
         uint2 q0, q1;
         if constexpr (QB == 4) {
           const int j = gs >> 2, gq = gs & 3;
@@ -408,6 +411,12 @@ gemv_tma_kernel(const __grid_constant__ TmaMaps maps, const GemvArgs a, const Tm
           const uint32_t qo = (uint32_t)((((2 * gq + (tig >> 1)) ^ pg) << 4) + (tig & 1) * 8);
           q0 = lds64(qb + r0s * 128 + qo);
           q1 = lds64(qb + r1s * 128 + qo);
+        } else if constexpr (QB == 2) {
+          const int off = gs * 16 + tig * 4;
+          const uint32_t w0 = lds32(code_addr(st + Geo::W_OFF, st + Geo::W_OFF, r0s, off));
+          const uint32_t w1 = lds32(code_addr(st + Geo::W_OFF, st + Geo::W_OFF, r1s, off));
+          q0 = make_uint2(__byte_perm(w0, 0u, 0x4140), __byte_perm(w0, 0u, 0x4342));
+          q1 = make_uint2(__byte_perm(w1, 0u, 0x4140), __byte_perm(w1, 0u, 0x4342));
         } else {
           q0 = stage_codes<QB>(st + Geo::W_OFF, st + Geo::W64_OFF, r0s, gs, tig);
           q1 = stage_codes<QB>(st + Geo::W_OFF, st + Geo::W64_OFF, r1s, gs, tig);
@@ -442,20 +451,22 @@ gemv_tma_kernel(const __grid_constant__ TmaMaps maps, const GemvArgs a, const Tm
         const float sr0 = __uint_as_float(a0s << 16), sr1 = __uint_as_float(a1s << 16);
         const float zr0 = 128.0f + __uint_as_float(b0z << 16);
         const float zr1 = 128.0f + __uint_as_float(b1z << 16);
-        // nibble pairs (n_i, n_{i+4}) of each word -> bf16x2 (128 + q), K paired
-        // (k, k + 4) on both operands
+        // code pairs (q_i, q_{i+4}) of each word -> bf16x2 (128 + q), K paired
+        // (k, k + 4) on both operands; SH bits per code step
         uint32_t A[4][4];
         {
-          const uint32_t NIB = 0x000f000fu, E = 0x43004300u;
+          constexpr int SH = QB == 2 ? 2 : 4;
+          constexpr uint32_t MK = QB == 2 ? 0x00030003u : 0x000f000fu;
+          const uint32_t E = 0x43004300u;
           const uint32_t a0 = q0.x, a1 = q0.y, c0 = q1.x, c1 = q1.y;
-          A[0][0] = (a0 & NIB) | E;         A[0][2] = ((a0 >> 4) & NIB) | E;
-          A[0][1] = (c0 & NIB) | E;         A[0][3] = ((c0 >> 4) & NIB) | E;
-          A[1][0] = ((a0 >> 8) & NIB) | E;  A[1][2] = ((a0 >> 12) & NIB) | E;
-          A[1][1] = ((c0 >> 8) & NIB) | E;  A[1][3] = ((c0 >> 12) & NIB) | E;
-          A[2][0] = (a1 & NIB) | E;         A[2][2] = ((a1 >> 4) & NIB) | E;
-          A[2][1] = (c1 & NIB) | E;         A[2][3] = ((c1 >> 4) & NIB) | E;
-          A[3][0] = ((a1 >> 8) & NIB) | E;  A[3][2] = ((a1 >> 12) & NIB) | E;
-          A[3][1] = ((c1 >> 8) & NIB) | E;  A[3][3] = ((c1 >> 12) & NIB) | E;
+          A[0][0] = (a0 & MK) | E;               A[0][2] = ((a0 >> SH) & MK) | E;
+          A[0][1] = (c0 & MK) | E;               A[0][3] = ((c0 >> SH) & MK) | E;
+          A[1][0] = ((a0 >> (2 * SH)) & MK) | E; A[1][2] = ((a0 >> (3 * SH)) & MK) | E;
+          A[1][1] = ((c0 >> (2 * SH)) & MK) | E; A[1][3] = ((c0 >> (3 * SH)) & MK) | E;
+          A[2][0] = (a1 & MK) | E;               A[2][2] = ((a1 >> SH) & MK) | E;
+          A[2][1] = (c1 & MK) | E;               A[2][3] = ((c1 >> SH) & MK) | E;
+          A[3][0] = ((a1 >> (2 * SH)) & MK) | E; A[3][2] = ((a1 >> (3 * SH)) & MK) | E;
+          A[3][1] = ((c1 >> (2 * SH)) & MK) | E; A[3][3] = ((c1 >> (3 * SH)) & MK) | E;
         }
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
