@@ -99,9 +99,10 @@ int32_t sub_w4_dequant(const uint8_t* q, const sub_bf16* scale, const sub_bf16* 
                        int64_t N, int64_t K, int32_t group, sub_bf16* W_out, void* stream);
 
 /* Y[M, N] (bf16) = X[M, K] (bf16) . deq(W)^T, fp32 accumulation.
- * M <= 16 runs the warp-level GEMV (one pass over the packed weights; the
- * zero point and scale are folded into the fp32 sums, so deq(W) is not
- * rounded to bf16 there).  Larger M runs the tcgen05 tensor-core GEMM, which
+ * M <= 16, and M <= 32 where K % 512 == 0, runs the warp-level GEMV (one
+ * pass over the packed weights; the zero point and scale are folded into the
+ * fp32 sums, so deq(W) is not rounded to bf16 there, and a row's result does
+ * not depend on M).  Larger M runs the tcgen05 tensor-core GEMM, which
  * dequantises each 64-column group to bf16((q - z) * s), the values
  * sub_w4_dequant returns, before the multiply.  K % 8 == 0. */
 int32_t sub_w4_gemm(const sub_bf16* X, int64_t M, const uint8_t* q, const sub_bf16* scale,
@@ -151,7 +152,7 @@ int32_t sub_wq_pack_hqq(const sub_bf16* W, int64_t N, int64_t K, int32_t group, 
                         void* stream);
 /* Y[M, N] (bf16) = X[M, K] . deq(W)^T.  M <= 16: the warp-level GEMV with the
  * zero point and scale folded into fp32 sums (2- and 3-bit codes are spread
- * into the int4 word layout in registers).  Larger M at 2 or 3 bits:
+ * into the int4 word layout in registers or shared memory).  Larger M at 2 or 3 bits:
  * dequantise into stream-ordered scratch (N * K * 2 bytes, SUB_ENOMEM if it
  * cannot be had) and run the bf16 tensor-core GEMM; at 4 bits as sub_w4_gemm. */
 int32_t sub_wq_gemm(const sub_bf16* X, int64_t M, const uint8_t* q, const sub_bf16* scale,

@@ -15,6 +15,7 @@ than the 129 MB L2):
   gemm_bf16   bf16 weights 18944x3584, M = 385 (a verify FFN matrix, tcgen05)
   gemm_w4     int4 weights 18944x3584, M = 385 (tcgen05 with the dequantising stage)
   gemv_{bf16,w4}_{down,o}  down projection 3584x18944 / o projection 3584x3584, M = 8
+  w4_wide     int4 37888x3584 at M = 8, 16, 24, 32, 48 (TMA GEMV to 32 rows, then tcgen05)
   w4_mix      the four int4 substitute matrices of one layer (o, gate, up, down)
               in turn, M = 8
   wq_mix2, wq_mix3  the same with 2- or 3-bit substitutes
@@ -121,6 +122,19 @@ def main():
             ms = _time(lambda i: sub.bf16_gemm(x, ws[i % reps], out=y), a.iters)
             byt = n * k * 2 + 8 * (n + k) * 2
         res.update(ms=ms, gbs=byt / ms / 1e6)
+    elif a.case == "w4_wide":
+        # int4 37888 x 3584 (a Qwen2.5-7B gate+up pair, 4 packed copies rotate
+        # past L2) at M = 8, 16, 24, 32, 48: the TMA GEMV with 1, 2, 4, 4 token
+        # tiles of 8, then the tensor-core GEMM
+        n, k, reps = 37888, 3584, 4
+        packs = [synthetic.random_w4(n, k, s, dev) for s in range(reps)]
+        for m in (8, 16, 24, 32, 48):
+            x = torch.randn(m, k, device=dev).to(torch.bfloat16)
+            y = torch.empty(m, n, device=dev, dtype=torch.bfloat16)
+            ms = _time(lambda i: sub.w4_gemm(x, *packs[i % reps], n, k, out=y), a.iters)
+            byt = n * (k // 64) * 36 + m * (n + k) * 2
+            res[f"M{m}"] = dict(ms=round(ms, 5), gbs=round(byt / ms / 1e6, 1),
+                                tflops=round(2 * m * n * k / ms / 1e9, 2))
     elif a.case == "w4_mix":
         # the four int4 substitute matrices of a Qwen2.5-7B layer in turn (o,
         # gate, up, down), M = 8: the shapes bench.py's roofline cycles through

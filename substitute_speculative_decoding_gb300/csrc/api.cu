@@ -113,8 +113,10 @@ static int32_t matmul_public(const sub_bf16* X, int64_t M, bool w4, const void* 
   // split scratch: partial sums of K splits (register-streamed kernel) or of
   // blocks shared by several CTAs (TMA kernel), and one counter per row unit
   const int ks = M <= 16 ? gemv_ksplit(a, w4, EPI_BF16) : 1;
-  const size_t tma_floats = M <= 16 ? gemv_tma_scratch_floats(a, w4, EPI_BF16)
-                                    : gemm_tc_scratch_floats(a, w4, EPI_BF16);
+  size_t tma_floats = M <= 16 ? gemv_tma_scratch_floats(a, w4, EPI_BF16)
+                              : gemm_tc_scratch_floats(a, w4, EPI_BF16);
+  if (M > 16 && M <= 32 && w4)   // the four-tile TMA GEMV may take it (int4)
+    tma_floats = std::max(tma_floats, gemv_tma_scratch_floats(a, w4, EPI_BF16));
   if (ks > 1 || tma_floats > 0) {
     // row units of 16, or weight tiles x token tiles of the tensor-core GEMM
     const int units = (int)std::max<int64_t>((N + 15) / 16, ((N + 127) / 128) * ((M + 255) / 256));

@@ -155,7 +155,8 @@ struct TmaGeom {
   static constexpr int XFB = XFRAG ? 8 * 2 * 32 * 16 : 0;
   static constexpr int STAGE = (XF_OFF + XFB + 1023) / 1024 * 1024;
   static constexpr int TX = WBOXES * WBOX + W64 + 2 * SZBOX + XBOXES * XBOX;   // bytes per stage
-  static constexpr int EPI_FLOATS = 4 * MT * 128 + NCW * 16 + 32;   // + flag, row scales
+  // + flag (16 floats), row scales (one per activation row)
+  static constexpr int EPI_FLOATS = 4 * MT * 128 + NCW * 16 + 16 + (MT > 2 ? MT * 8 : 16);
   // alignment slack, ring, barriers and epilogue buffers within the limit
   static constexpr int STAGES =
       std::min(MAX_STAGES, (SMEM_LIMIT - 1024 - 3 * MAX_STAGES * 8 - EPI_FLOATS * 4) / STAGE);
@@ -422,10 +423,13 @@ gemv_tma_kernel(const __grid_constant__ TmaMaps maps, const GemvArgs a, const Tm
           q1 = stage_codes<QB>(st + Geo::W_OFF, st + Geo::W64_OFF, r1s, gs, tig);
         }
         const uint32_t xbox = st + Geo::X_OFF + gs * Geo::XBOX;
-        uint32_t bfr[MT][4][2];
-        float sx[MT][2];
+        // up to two token tiles: every tile's B fragments and sums up front;
+        // four: one tile at a time, after the unpack (registers)
+        constexpr int MTU = MT > 2 ? 1 : MT;
+        uint32_t bfr[MTU][4][2];
+        float sx[MTU][2];
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
+        for (int mt = 0; mt < (MT > 2 ? 0 : MT); ++mt) {
           if constexpr (Geo::XFRAG) {
             const uint32_t xf = st + Geo::XF_OFF + ((gs * 2) * 32 + lane) * 16;
             const uint4 f0 = lds128(xf), f1 = lds128(xf + 32 * 16);
@@ -470,16 +474,23 @@ gemv_tma_kernel(const __grid_constant__ TmaMaps maps, const GemvArgs a, const Tm
         }
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
+          const int mu = MT > 2 ? 0 : mt;   // register slot of this tile's operands
+          if constexpr (MT > 2) {
+            x_frags(xbox, mt, bfr[0]);
+            asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];"
+                         : "=f"(sx[0][0]), "=f"(sx[0][1])
+                         : "r"(st + Geo::SX_OFF + (((gs * MT + mt) * 8 + 2 * tig) << 2)));
+          }
           float p[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint32_t Ak[4] = {A[k][0], A[k][1], A[k][2], A[k][3]};
-            mma_bf16_16816(p, Ak, bfr[mt][k][0], bfr[mt][k][1]);
+            mma_bf16_16816(p, Ak, bfr[mu][k][0], bfr[mu][k][1]);
           }
-          acc[mt][0] = fmaf(sr0, fmaf(-zr0, sx[mt][0], p[0]), acc[mt][0]);
-          acc[mt][1] = fmaf(sr0, fmaf(-zr0, sx[mt][1], p[1]), acc[mt][1]);
-          acc[mt][2] = fmaf(sr1, fmaf(-zr1, sx[mt][0], p[2]), acc[mt][2]);
-          acc[mt][3] = fmaf(sr1, fmaf(-zr1, sx[mt][1], p[3]), acc[mt][3]);
+          acc[mt][0] = fmaf(sr0, fmaf(-zr0, sx[mu][0], p[0]), acc[mt][0]);
+          acc[mt][1] = fmaf(sr0, fmaf(-zr0, sx[mu][1], p[1]), acc[mt][1]);
+          acc[mt][2] = fmaf(sr1, fmaf(-zr1, sx[mu][0], p[2]), acc[mt][2]);
+          acc[mt][3] = fmaf(sr1, fmaf(-zr1, sx[mu][1], p[3]), acc[mt][3]);
         }
       }
     }
@@ -547,17 +558,18 @@ gemv_tma_kernel(const __grid_constant__ TmaMaps maps, const GemvArgs a, const Tm
       }
       consumer_sync();
       if (!*flag) continue;
-      // sum the pieces in CTA order; eight pieces' loads in flight per round
+      // sum the pieces in CTA order; YY pieces' loads in flight per round
       // (one load at a time would put n_c round trips on the kernel's tail)
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
         for (int j = 0; j < 4; ++j) tot[mt][j] = 0.f;
       const float* mine0 = slots + warp * MT * 128 + lane;
-      for (int y0 = 0; y0 < n_c; y0 += 8) {
-        float t[8][MT][4];
+      constexpr int YY = MT > 2 ? 2 : 8;   // pieces per round (registers at 4 tiles)
+      for (int y0 = 0; y0 < n_c; y0 += YY) {
+        float t[YY][MT][4];
 #pragma unroll
-        for (int yy = 0; yy < 8; ++yy)
+        for (int yy = 0; yy < YY; ++yy)
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -566,7 +578,7 @@ gemv_tma_kernel(const __grid_constant__ TmaMaps maps, const GemvArgs a, const Tm
                                  ? __ldcg(mine0 + (size_t)(y0 + yy) * PER + mt * 128 + j * 32)
                                  : 0.f;
 #pragma unroll
-        for (int yy = 0; yy < 8; ++yy)
+        for (int yy = 0; yy < YY; ++yy)
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -696,6 +708,8 @@ gemv_tma_kernel(const __grid_constant__ TmaMaps maps, const GemvArgs a, const Tm
 namespace {
 template <bool W4, int MT, int QB = 4>
 cudaError_t tma_attr_all();
+template <bool W4, int MT, int EPI, int QB>
+cudaError_t tma_attr();
 }  // namespace
 
 // Shared-memory opt-in of every TMA GEMV instantiation and the tensor-map
@@ -709,7 +723,11 @@ int32_t gemv_init() {
                               tma_attr_all<true, 1>(),    tma_attr_all<true, 2>(),
                               tma_attr_all<true, 1, 2>(), tma_attr_all<true, 2, 2>(),
                               tma_attr_all<true, 1, 3>(), tma_attr_all<true, 2, 3>()};
+    // int4 codes, bf16 output, 17..32 activation rows
+    const cudaError_t wide[1] = {tma_attr<true, 4, EPI_BF16, 4>()};
     for (cudaError_t x : e)
+      if (x != cudaSuccess && err == cudaSuccess) err = x;
+    for (cudaError_t x : wide)
       if (x != cudaSuccess && err == cudaSuccess) err = x;
   });
   if (err != cudaSuccess) return fail(SUB_ECUDA, std::string("gemv_init: ") + cudaGetErrorString(err));
@@ -799,11 +817,18 @@ static int sm_count() {
   return n;
 }
 
+// Token tiles of 8 activation rows a launch uses: 1 or 2 up to 16 rows, then
+// 4 (int4 codes, bf16 output) up to 32.  Six tiles (48 rows) leave room for
+// only two stages and ran no faster than the tensor-core GEMM.
+static int tma_tiles(int M) { return M <= 8 ? 1 : M <= 16 ? 2 : 4; }
+
 // Plan of a TMA launch, or false when the shape or the scratch does not fit
 // (the caller then uses the register-streamed kernel).
 static bool tma_plan(const GemvArgs& a, bool w4, int epi, TmaPlan* pl, int* grid) {
   const bool glu = epi == EPI_GLU;
-  if (a.M < 1 || a.M > 16 || a.n_seg < 1 || a.n_seg > 3) return false;
+  if (a.M < 1 || a.M > 32 || a.n_seg < 1 || a.n_seg > 3) return false;
+  // past 16 rows: int4 codes with a bf16 output only (four token tiles)
+  if (a.M > 16 && !(w4 && code_bits(a) == 4 && epi == EPI_BF16)) return false;
   if (glu && a.n_seg != 2) return false;
   const int G = (a.K + 63) / 64;
   if (w4 && G % 8) return false;   // scale/zero rows must be whole 16-byte strides
@@ -827,7 +852,7 @@ static bool tma_plan(const GemvArgs& a, bool w4, int epi, TmaPlan* pl, int* grid
   // a CTA covers at least floor(total / grid) units, so a block of s_blk
   // units meets at most ceil(s_blk / that) + 1 CTAs
   pl->maxc = (pl->s_blk + pl->total / *grid - 1) / (pl->total / *grid) + 1;
-  const int mt = a.M <= 8 ? 1 : 2;
+  const int mt = tma_tiles(a.M);
   const size_t need = (size_t)nb * pl->maxc * NCW * mt * 128;
   return a.split_part && a.split_cnt && need <= a.split_cap && nb <= a.split_cnt_cap;
 }
@@ -840,7 +865,7 @@ int32_t launch_gemv_tma(const GemvArgs& a, bool w4, int epi, cudaStream_t st, bo
   int grid = 0;
   if (!tma_plan(a, w4, epi, &pl, &grid)) return SUB_OK;
   const bool glu = epi == EPI_GLU;
-  const int mt = a.M <= 8 ? 1 : 2;
+  const int mt = tma_tiles(a.M);
   const int box_rows = glu ? BR / 2 : BR;
   const int G = (a.K + 63) / 64;
   const int bits = w4 ? code_bits(a) : 16;
@@ -888,6 +913,7 @@ int32_t launch_gemv_tma(const GemvArgs& a, bool w4, int epi, cudaStream_t st, bo
                                       : tma_epi<true, 2, 2>(a, epi, maps, pl, grid, st);
   if (w4 && bits == 3) return mt == 1 ? tma_epi<true, 1, 3>(a, epi, maps, pl, grid, st)
                                       : tma_epi<true, 2, 3>(a, epi, maps, pl, grid, st);
+  if (w4 && mt > 2) return tma_launch<true, 4, EPI_BF16, 4>(a, maps, pl, grid, st);   // bf16 output only
   if (w4) return mt == 1 ? tma_epi<true, 1>(a, epi, maps, pl, grid, st)
                          : tma_epi<true, 2>(a, epi, maps, pl, grid, st);
   return mt == 1 ? tma_epi<false, 1>(a, epi, maps, pl, grid, st)
@@ -903,7 +929,7 @@ size_t gemv_tma_scratch_floats(const GemvArgs& a, bool w4, int epi) {
   TmaPlan pl{};
   int grid = 0;
   if (!tma_plan(t, w4, epi, &pl, &grid)) return 0;
-  return (size_t)pl.n_blocks * pl.maxc * NCW * (a.M <= 8 ? 1 : 2) * 128;
+  return (size_t)pl.n_blocks * pl.maxc * NCW * tma_tiles(a.M) * 128;
 }
 
 // ------------------------------------------------------ bounded-wait check --

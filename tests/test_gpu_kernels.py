@@ -70,6 +70,27 @@ def test_w4_gemm_identity_is_exact_dequant(sub):
     assert torch.equal(y16.t().contiguous(), sub.w4_dequant(q, s, z, k)[:, :16])
 
 
+def test_w4_wide_gemv_rows_match_narrow(sub):
+    """Up to 32 rows an int4 product with a bf16 output stays on the TMA GEMV
+    (four token tiles of 8 past 16 rows): a row's result is the same, bit for
+    bit, whether it shares the pass with 7 or 31 other rows; identity rows give
+    the dequantised values exactly, on the GEMV and past 32 rows on the
+    tensor-core GEMM."""
+    n, k = 640, 1024
+    w = synthetic.randn_bf16((n, k), 31, std=0.02)
+    q, s, z = sub.w4_pack(w.to(DEV))
+    x = synthetic.randn_bf16((48, k), 33).to(DEV)
+    y32 = sub.w4_gemm(x[:32].contiguous(), q, s, z, n, k)
+    y24 = sub.w4_gemm(x[:24].contiguous(), q, s, z, n, k)
+    y8 = sub.w4_gemm(x[:8].contiguous(), q, s, z, n, k)
+    assert torch.equal(y32[:24], y24) and torch.equal(y32[:8], y8)
+    deq = sub.w4_dequant(q, s, z, k)
+    eye = torch.eye(k, dtype=torch.bfloat16, device=DEV)
+    for r0, m in ((0, 48), (48, 40), (88, 24)):
+        y = sub.w4_gemm(eye[r0:r0 + m].contiguous(), q, s, z, n, k)
+        assert torch.equal(y.t().contiguous(), deq[:, r0:r0 + m])
+
+
 @pytest.mark.parametrize("m", [1, 8, 16, 17, 385])
 @pytest.mark.parametrize("n,k", [(1024, 256), (512, 3584), (144, 688)])
 def test_bf16_gemm(sub, m, n, k):
