@@ -381,7 +381,7 @@ def kernel_measurements(sub, cfg, weights, model, pk, dev, quick):
         wbytes = n * ((k + 63) // 64) * 36
         nc = copies_for(wbytes)
         packs = [synthetic.random_w4(n, k, seed, device=dev) for seed in range(nc)]
-        for mrows in (1, 8, 48, 128, 384):
+        for mrows in (1, 8, 32, 48, 128, 384):
             xx = torch.randn(mrows, k, device=dev).to(torch.bfloat16)
             yy = torch.empty(mrows, n, device=dev, dtype=torch.bfloat16)
             msx = time_launches(lambda i: sub.w4_gemm(xx, *packs[i % nc], n, k, out=yy),

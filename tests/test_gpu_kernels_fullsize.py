@@ -4,7 +4,7 @@ shapes): tree attention with 385 tree nodes (depth 48, width 8) over 4k and
 sampled and computed one by one by the oracle) and draft-shaped (the 8
 deepest nodes, every output checked, the 16-way key split and its cluster
 merge in play); the int4 product on the 32B gate+up (55296 x 5120) and down
-(5120 x 27648, 432 groups) matrices at draft and verify widths, sampled
+(5120 x 27648, 432 groups) matrices at draft, four-tile GEMV and verify widths, sampled
 output rows against the oracle's dequantisation."""
 import numpy as np
 import pytest
@@ -84,7 +84,7 @@ def test_tree_attn_fullsize(sub, n_prefix):
 
 
 @pytest.mark.parametrize("n,k", [(55296, 5120), (5120, 27648)])
-@pytest.mark.parametrize("m", [1, 8, 48, 385])
+@pytest.mark.parametrize("m", [1, 8, 32, 48, 385])
 def test_w4_gemm_fullsize(sub, n, k, m):
     q, s, z = synthetic.random_w4(n, k, 3)
     x = synthetic.randn_bf16((m, k), 7 + m)
